@@ -1,0 +1,580 @@
+// api.cpp -- the C ABI declared in include/gemm.h: argument checks, the
+// tile-shape / split-K planner, tensor-map (TMA descriptor) encoding, the plan
+// object and kernel dispatch.
+#include "gemm.h"
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "kernels.h"
+
+struct gemm_plan {
+  int device = 0;
+  int sms = 0;
+  int* err = nullptr;  // device word, OR of wait codes
+  void* ws = nullptr;  // workspace (split-K partials, GEMV partials + counters)
+  size_t ws_bytes = 0;
+  uint64_t watchdog_ns = 2000000000ull;
+  gemm_config_info_t last{};
+};
+
+namespace {
+
+constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
+
+bool out_is_f32(gemm_dtype_t d) { return d == GEMM_BF16_F32 || d == GEMM_F16_F32; }
+bool in_is_f16(gemm_dtype_t d) { return d == GEMM_F16_F32 || d == GEMM_F16_F16; }
+
+int out_kind(gemm_dtype_t d) {
+  switch (d) {
+    case GEMM_BF16_F32:
+    case GEMM_F16_F32: return dg::OUT_F32;
+    case GEMM_BF16_BF16: return dg::OUT_BF16;
+    default: return dg::OUT_F16;
+  }
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------- validation
+
+gemm_status_t check(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                    int64_t ldb, const void* C, int64_t ldc, float alpha, gemm_dtype_t dtype,
+                    gemm_op_t ta, gemm_op_t tb, gemm_epilogue_t epi) {
+  if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  if (dtype < GEMM_BF16_F32 || dtype > GEMM_F16_F16) return GEMM_ERR_INVALID_ARG;
+  if ((ta != GEMM_OP_N && ta != GEMM_OP_T) || (tb != GEMM_OP_N && tb != GEMM_OP_T))
+    return GEMM_ERR_INVALID_ARG;
+  if (epi.act != GEMM_ACT_NONE && epi.act != GEMM_ACT_LEAKY_RELU) return GEMM_ERR_INVALID_ARG;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_UNSUPPORTED;
+  const int64_t a_cols = ta == GEMM_OP_N ? K : M;
+  const int64_t b_cols = tb == GEMM_OP_N ? N : K;
+  if (lda < std::max<int64_t>(1, a_cols) || ldb < std::max<int64_t>(1, b_cols) ||
+      ldc < std::max<int64_t>(1, N))
+    return GEMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return GEMM_OK;
+  if (C == nullptr) return GEMM_ERR_INVALID_ARG;
+  const bool reads_ab = K > 0 && alpha != 0.f;
+  if (reads_ab && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_ARG;
+  const size_t ces = out_is_f32(dtype) ? 4 : 2;
+  if (!aligned(C, ces)) return GEMM_ERR_ALIGNMENT;
+  if (reads_ab && (!aligned(A, 2) || !aligned(B, 2))) return GEMM_ERR_ALIGNMENT;
+  if (reads_ab && M >= 2 && N >= 2) {
+    if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return GEMM_ERR_ALIGNMENT;
+    if ((lda * 2) % 16 || (ldb * 2) % 16 || (ldc * int64_t(ces)) % 16) return GEMM_ERR_ALIGNMENT;
+  }
+  return GEMM_OK;
+}
+
+// --------------------------------------------------------------- planner
+
+void quantization(int64_t M, int64_t N, int tm, int tn, int splitk, int sms, int ctas_per_sm,
+                  gemm_config_info_t* o) {
+  o->tile_m = tm;
+  o->tile_n = tn;
+  o->splitk = splitk;
+  o->sms = sms;
+  o->tiles = ceil_div(M, tm) * ceil_div(N, tn);
+  o->units = o->tiles * splitk;
+  const int64_t wave = int64_t(sms) * ctas_per_sm;
+  o->waves = double(o->units) / double(wave);
+  const int64_t tail = o->units % wave;
+  o->tail_fraction = double(tail) / double(wave);
+  o->useful_fraction = o->tiles ? double(M) * double(N) / (double(o->tiles) * tm * tn) : 0.0;
+}
+
+// Cost model of the tensor-core path (seconds; absolute scale only matters
+// relative to the other candidates).  Persistent CTAs take units round-robin,
+// so the busiest SM runs ceil(units/SMs) units ("Matrix Multiplication
+// Background User's Guide", section 3.2, wave quantization); every unit pays
+// for a full tile whatever part of it lies inside C (section 3.1, tile
+// quantization); a unit is bound by the tensor core or by the rate at which
+// one SM can pull its A and B blocks; the whole call is at least as long as
+// streaming its unique bytes from HBM (section 2, math vs memory bound).
+struct Model {
+  double peak_flops = 2.25e15;  // dense bf16, whole GPU
+  double hbm_bw = 7.0e12;       // B/s
+  double sm_bw = 2.0e11;        // B/s one SM can pull from L2
+  double unit_fixed = 1.0e-6;   // pipeline fill + epilogue tail per unit
+  double launch = 3.0e-6;       // one extra kernel
+};
+
+double tile_efficiency(int bn) { return bn >= 256 ? 1.0 : (bn >= 128 ? 0.92 : 0.70); }
+
+double estimate(int64_t M, int64_t N, int64_t K, int bn, int splitk, int sms, int c_es,
+                bool beta, const Model& md, int* splitk_eff) {
+  const int64_t kb = ceil_div(K, dg::TC_BK);
+  const int64_t kbps = ceil_div(kb, splitk);
+  const int s_eff = int(ceil_div(kb, kbps));
+  *splitk_eff = s_eff;
+  const int64_t tiles = ceil_div(M, dg::TC_BM) * ceil_div(N, bn);
+  const int64_t units = tiles * s_eff;
+  const double per_sm_flops = md.peak_flops / sms;
+  const double t_mma = 2.0 * dg::TC_BM * bn * double(kbps * dg::TC_BK) / (per_sm_flops * tile_efficiency(bn));
+  const double t_load = double(dg::TC_BM + bn) * double(kbps * dg::TC_BK) * 2.0 / md.sm_bw;
+  const double t_unit = std::max(t_mma, t_load) + md.unit_fixed;
+  const double makespan = double(ceil_div(units, sms)) * t_unit;
+  double bytes = double(M * K + K * N) * 2.0 + double(M) * N * c_es * (beta ? 2.0 : 1.0);
+  double t = 0.0;
+  if (s_eff > 1) {
+    const double part = double(s_eff) * double(ceil_div(M, dg::TC_BM) * dg::TC_BM) * double(N) * 4.0;
+    bytes += part;                             // partials written
+    t += md.launch + part / md.hbm_bw;         // reduction kernel reads them back
+  }
+  return std::max(makespan, bytes / md.hbm_bw) + t;
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  return std::atoi(v);
+}
+
+void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
+               gemm_config_info_t* out) {
+  const Model md;
+  int best_bn = 256, best_s = 1;
+  double best_t = 1e300;
+  int force_bn = 0;
+  if (const char* f = std::getenv("GEMM_FORCE_TILE")) {
+    int fm = 0, fn = 0;
+    if (std::sscanf(f, "%dx%d", &fm, &fn) == 2 && fm == dg::TC_BM && (fn == 64 || fn == 128 || fn == 256))
+      force_bn = fn;
+  }
+  const int force_s = env_int("GEMM_FORCE_SPLITK", 0);
+  const int64_t kb = ceil_div(K, dg::TC_BK);
+  const int bns[3] = {256, 128, 64};
+  for (int bn : bns) {
+    if (force_bn && bn != force_bn) continue;
+    for (int s = 1; s <= 64; ++s) {
+      if (force_s > 0 && s != force_s) continue;
+      if (s > kb) break;
+      int s_eff = 1;
+      const double t = estimate(M, N, K, bn, s, sms, c_es, beta, md, &s_eff);
+      if (s_eff != s) continue;
+      // prefer wider tiles / fewer slices unless clearly faster (2%)
+      if (t < best_t * 0.98) {
+        best_t = t;
+        best_bn = bn;
+        best_s = s;
+      }
+    }
+  }
+  if (force_s > 0 && best_t == 1e300) {  // forced split not reachable exactly: take nearest valid
+    best_s = int(std::min<int64_t>(force_s, kb));
+    best_bn = force_bn ? force_bn : 256;
+  }
+  const int64_t kbps = ceil_div(kb, best_s);
+  best_s = int(ceil_div(kb, kbps));
+  std::memset(out, 0, sizeof(*out));
+  quantization(M, N, dg::TC_BM, best_bn, best_s, sms, 1, out);
+  out->path = best_s > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
+  out->tile_k = dg::TC_BK;
+  out->cta_per_tile = 1;
+  out->stages = dg::tc_stages(best_bn);
+  const int64_t mblocks = ceil_div(M, dg::TC_BM);
+  out->raster_group = int(std::max<int64_t>(1, std::min<int64_t>(env_int("GEMM_RASTER_GROUP", 16), mblocks)));
+  out->grid = int(std::min<int64_t>(out->units, sms));
+}
+
+// ------------------------------------------------------------ tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major tensor: `inner` contiguous elements per row, `outer` rows,
+// `ld` elements between rows; boxes of box_inner x box_outer with 128-byte
+// swizzling (box_inner * esize == 128).  Out-of-range reads give zero.
+bool make_map(CUtensorMap* m, CUtensorMapDataType t, int esize, const void* ptr, int64_t inner,
+              int64_t outer, int64_t ld, int box_inner, int box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+  cuuint64_t strides[1] = {cuuint64_t(ld) * cuuint64_t(esize)};
+  cuuint32_t box[2] = {cuuint32_t(box_inner), cuuint32_t(box_outer)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, t, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// tcgen05 instruction descriptor, kind::f16 with fp32 accumulation:
+// bits 4-5 D type (1 = f32), 7-9 A type and 10-12 B type (0 = f16, 1 = bf16),
+// 15/16 A/B major (0 = K-major, 1 = M/N-major), 17-22 N>>3, 24-28 M>>4.
+uint32_t make_idesc(bool f16, bool a_mn, bool b_mn, int n, int m) {
+  const uint32_t ab = f16 ? 0u : 1u;
+  return (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
+         (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
+}
+
+// ------------------------------------------------------------- workspace
+
+gemm_status_t ensure_ws(gemm_plan* plan, size_t bytes, cudaStream_t s) {
+  if (bytes <= plan->ws_bytes) return GEMM_OK;
+  size_t nb = std::max<size_t>(bytes, size_t(1) << 20);
+  nb = (nb + (size_t(1) << 20) - 1) & ~((size_t(1) << 20) - 1);
+  if (plan->ws) cudaFreeAsync(plan->ws, s);
+  plan->ws = nullptr;
+  plan->ws_bytes = 0;
+  if (cudaMallocAsync(&plan->ws, nb, s) != cudaSuccess) {
+    cudaGetLastError();
+    plan->ws = nullptr;
+    return GEMM_ERR_OUT_OF_MEMORY;
+  }
+  if (cudaMemsetAsync(plan->ws, 0, nb, s) != cudaSuccess) return GEMM_ERR_CUDA;
+  plan->ws_bytes = nb;
+  return GEMM_OK;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != dev) cudaSetDevice(dev);
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+// --------------------------------------------------------------- dispatch
+
+gemm_status_t run_gemv(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* A,
+                       int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                       gemm_dtype_t dtype, gemm_op_t ta, gemm_op_t tb, const dg::EpiParams& e,
+                       cudaStream_t s, gemm_config_info_t* info) {
+  dg::GemvArgs g{};
+  g.K = int(K);
+  g.in_f16 = in_is_f16(dtype);
+  g.out = C;
+  g.e = e;
+  bool row_major_w;  // true: W rows run along K (rowdot); false: W rows run along R (colstream)
+  if (N == 1) {      // C(i,0) = sum_k op(A)(i,k) op(B)(k,0)
+    g.R = int(M);
+    g.inc_out = ldc;
+    g.x = B;
+    g.incx = tb == GEMM_OP_N ? ldb : 1;
+    g.W = A;
+    g.ldw = lda;
+    row_major_w = ta == GEMM_OP_N;
+    g.w_rs = row_major_w ? lda : 1;
+    g.w_cs = row_major_w ? 1 : lda;
+  } else {           // M == 1: C(0,j) = sum_k op(A)(0,k) op(B)(k,j)
+    g.R = int(N);
+    g.inc_out = 1;
+    g.x = A;
+    g.incx = ta == GEMM_OP_N ? 1 : lda;
+    g.W = B;
+    g.ldw = ldb;
+    row_major_w = tb == GEMM_OP_T;
+    g.w_rs = row_major_w ? ldb : 1;
+    g.w_cs = row_major_w ? 1 : ldb;
+  }
+  const bool vec_ok = aligned(g.W, 16) && (g.ldw * 2) % 16 == 0;
+  cudaError_t err;
+  info->path = GEMM_PATH_GEMV_GENERIC;
+  info->splitk = 1;
+  info->launches = 1;
+  if (row_major_w && (vec_ok || g.R == 1) && aligned(g.W, 16) && K <= dg::gemv_rowdot_max_k()) {
+    info->path = GEMM_PATH_GEMV_ROWDOT;
+    err = dg::launch_gemv_rowdot(g, s, plan->sms);
+  } else if (!row_major_w && (vec_ok || K == 1) && aligned(g.W, 16)) {
+    const dg::ColstreamPlan cp = dg::plan_gemv_colstream(g.R, g.K, plan->sms);
+    if (cp.ws_bytes > 0) {
+      const gemm_status_t st = ensure_ws(plan, size_t(cp.ws_bytes), s);
+      if (st != GEMM_OK) return st;
+    }
+    info->path = GEMM_PATH_GEMV_COLSTREAM;
+    info->splitk = cp.ksplit;
+    info->grid = cp.panels * cp.ksplit;
+    info->workspace_bytes = cp.ws_bytes;
+    err = dg::launch_gemv_colstream(g, cp, plan->ws, s);
+  } else {
+    err = dg::launch_gemv_generic(g, s, plan->sms);
+  }
+  return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                     const void* B, int64_t ldb, void* C, int64_t ldc, float alpha, float beta,
+                     gemm_dtype_t dtype, gemm_op_t ta, gemm_op_t tb, gemm_epilogue_t epi,
+                     cudaStream_t s, gemm_config_info_t* info) {
+  const int c_es = out_is_f32(dtype) ? 4 : 2;
+  choose_tc(M, N, K, plan->sms, c_es, beta != 0.f, info);
+  const int bn = info->tile_n;
+  const int S = info->splitk;
+  const bool f16 = in_is_f16(dtype);
+  const CUtensorMapDataType in_t = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const bool a_mn = ta == GEMM_OP_T, b_mn = tb == GEMM_OP_N;
+  CUtensorMap ma, mb, mc;
+  bool ok = a_mn ? make_map(&ma, in_t, 2, A, M, K, lda, 64, 64)
+                 : make_map(&ma, in_t, 2, A, K, M, lda, 64, dg::TC_BM);
+  ok = ok && (b_mn ? make_map(&mb, in_t, 2, B, N, K, ldb, 64, 64)
+                   : make_map(&mb, in_t, 2, B, K, N, ldb, 64, bn));
+  dg::TcParams p{};
+  p.M = int(M);
+  p.N = int(N);
+  p.K = int(K);
+  p.num_m_blocks = int(ceil_div(M, dg::TC_BM));
+  p.num_n_blocks = int(ceil_div(N, bn));
+  p.k_blocks = int(ceil_div(K, dg::TC_BK));
+  p.splitk = S;
+  p.kb_per_split = int(ceil_div(p.k_blocks, S));
+  p.raster_group = info->raster_group;
+  p.units = int(info->units);
+  p.ws_rows = p.num_m_blocks * dg::TC_BM;
+  p.a_mn_major = a_mn;
+  p.b_mn_major = b_mn;
+  p.idesc = make_idesc(f16, a_mn, b_mn, bn, dg::TC_BM);
+  p.alpha = alpha;
+  p.beta = beta;
+  p.act = epi.act;
+  p.slope = epi.slope;
+  p.err = plan->err;
+  p.timeout_ns = plan->watchdog_ns;
+  int64_t ws_ld = 0, ws_slice = 0;
+  if (S == 1) {
+    p.out_kind = out_kind(dtype);
+    const CUtensorMapDataType ct = out_is_f32(dtype) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : in_t;
+    ok = ok && make_map(&mc, ct, c_es, C, N, M, ldc, 128 / c_es, 32);
+  } else {
+    p.out_kind = dg::OUT_PARTIAL;
+    ws_ld = (N + 3) & ~int64_t(3);
+    ws_slice = int64_t(p.ws_rows) * ws_ld;
+    const size_t bytes = size_t(S) * size_t(ws_slice) * 4;
+    const gemm_status_t st = ensure_ws(plan, bytes, s);
+    if (st != GEMM_OK) return st;
+    info->workspace_bytes = int64_t(bytes);
+    ok = ok && make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, plan->ws, N, int64_t(S) * p.ws_rows,
+                        ws_ld, 32, 32);
+  }
+  if (!ok) return GEMM_ERR_CUDA;
+  if (dg::launch_gemm_tc(bn, ma, mb, mc, p, info->grid, s) != cudaSuccess) return GEMM_ERR_CUDA;
+  info->launches = 1;
+  if (S > 1) {
+    const dg::EpiParams e{alpha, beta, epi.slope, epi.act, out_kind(dtype)};
+    if (dg::launch_splitk_reduce(static_cast<const float*>(plan->ws), ws_ld, ws_slice, S, int(M),
+                                 int(N), C, ldc, e, s, plan->sms) != cudaSuccess)
+      return GEMM_ERR_CUDA;
+    info->launches = 2;
+  }
+  return GEMM_OK;
+}
+
+}  // namespace
+
+// =================================================================== C ABI
+
+extern "C" {
+
+const char* gemm_status_string(gemm_status_t st) {
+  switch (st) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG: invalid argument";
+    case GEMM_ERR_ALIGNMENT: return "GEMM_ERR_ALIGNMENT: pointer or leading dimension misaligned";
+    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: size not supported";
+    case GEMM_ERR_NO_DEVICE: return "GEMM_ERR_NO_DEVICE: no compute capability 10.x CUDA device";
+    case GEMM_ERR_OUT_OF_MEMORY: return "GEMM_ERR_OUT_OF_MEMORY: workspace allocation failed";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: CUDA call or kernel launch failed";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a kernel wait ran out (watchdog)";
+  }
+  return "unknown gemm_status_t";
+}
+
+gemm_status_t gemm_plan_create(gemm_plan_t* plan, int device) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  *plan = nullptr;
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || device < 0 || device >= count) {
+    cudaGetLastError();
+    return GEMM_ERR_NO_DEVICE;
+  }
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess || prop.major != 10) {
+    cudaGetLastError();
+    return GEMM_ERR_NO_DEVICE;
+  }
+  if (!encode_fn()) return GEMM_ERR_NO_DEVICE;
+  DeviceGuard guard(device);
+  gemm_plan* p = new gemm_plan();
+  p->device = device;
+  p->sms = prop.multiProcessorCount;
+  if (const char* w = std::getenv("GEMM_WATCHDOG_NS")) {
+    const unsigned long long v = std::strtoull(w, nullptr, 10);
+    if (v >= 1000) p->watchdog_ns = v;
+  }
+  if (cudaMalloc(&p->err, sizeof(int)) != cudaSuccess || cudaMemset(p->err, 0, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    if (p->err) cudaFree(p->err);
+    delete p;
+    return GEMM_ERR_OUT_OF_MEMORY;
+  }
+  *plan = p;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
+  if (!plan) return GEMM_OK;
+  DeviceGuard guard(plan->device);
+  cudaDeviceSynchronize();
+  if (plan->ws) cudaFree(plan->ws);
+  if (plan->err) cudaFree(plan->err);
+  delete plan;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_check_args(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                              const void* B, int64_t ldb, const void* C, int64_t ldc, float alpha,
+                              gemm_dtype_t dtype, gemm_op_t transA, gemm_op_t transB,
+                              gemm_epilogue_t epilogue) {
+  return check(M, N, K, A, lda, B, ldb, C, ldc, alpha, dtype, transA, transB, epilogue);
+}
+
+gemm_status_t gemm_run(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, const void* A,
+                       int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, float alpha,
+                       float beta, gemm_dtype_t dtype, gemm_op_t transA, gemm_op_t transB,
+                       gemm_epilogue_t epilogue, void* stream) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  const gemm_status_t st =
+      check(M, N, K, A, lda, B, ldb, C, ldc, alpha, dtype, transA, transB, epilogue);
+  if (st != GEMM_OK) return st;
+  gemm_config_info_t info{};
+  info.sms = plan->sms;
+  info.splitk = 1;
+  if (M == 0 || N == 0) {
+    info.path = GEMM_PATH_NONE;
+    plan->last = info;
+    return GEMM_OK;
+  }
+  DeviceGuard guard(plan->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const dg::EpiParams e{alpha, beta, epilogue.slope, epilogue.act, out_kind(dtype)};
+  gemm_status_t r;
+  if (K == 0 || alpha == 0.f) {
+    info.path = GEMM_PATH_SCALE;
+    info.launches = 1;
+    r = dg::launch_scale(int(M), int(N), C, ldc, e, s, plan->sms) == cudaSuccess ? GEMM_OK
+                                                                                  : GEMM_ERR_CUDA;
+  } else if (M == 1 || N == 1) {
+    r = run_gemv(plan, M, N, K, A, lda, B, ldb, C, ldc, dtype, transA, transB, e, s, &info);
+  } else {
+    r = run_tc(plan, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype, transA, transB, epilogue,
+               s, &info);
+  }
+  if (r != GEMM_OK) cudaGetLastError();
+  plan->last = info;
+  return r;
+}
+
+gemm_status_t gemm_plan_last_config(gemm_plan_t plan, gemm_config_info_t* out) {
+  if (!plan || !out) return GEMM_ERR_INVALID_ARG;
+  *out = plan->last;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_poll_error(gemm_plan_t plan, void* stream) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->device);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  int h = 0;
+  if (cudaMemcpy(&h, plan->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (h == 0) return GEMM_OK;
+  if (cudaMemset(plan->err, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+  return GEMM_ERR_TIMEOUT;
+}
+
+gemm_status_t gemm_plan_set_watchdog(gemm_plan_t plan, uint64_t timeout_ns) {
+  if (!plan || timeout_ns < 1000) return GEMM_ERR_INVALID_ARG;
+  plan->watchdog_ns = timeout_ns;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_selftest_watchdog(gemm_plan_t plan, void* stream) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  DeviceGuard guard(plan->device);
+  if (dg::launch_watchdog_selftest(plan->err, plan->watchdog_ns, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return GEMM_ERR_CUDA;
+  }
+  return gemm_plan_poll_error(plan, stream);
+}
+
+gemm_status_t gemm_choose_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                                 gemm_op_t transA, gemm_op_t transB, int32_t sms,
+                                 gemm_config_info_t* out) {
+  if (!out || sms <= 0 || M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+  if (dtype < GEMM_BF16_F32 || dtype > GEMM_F16_F16) return GEMM_ERR_INVALID_ARG;
+  if ((transA != GEMM_OP_N && transA != GEMM_OP_T) || (transB != GEMM_OP_N && transB != GEMM_OP_T))
+    return GEMM_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  out->sms = sms;
+  out->splitk = 1;
+  if (M == 0 || N == 0) {
+    out->path = GEMM_PATH_NONE;
+    return GEMM_OK;
+  }
+  if (K == 0) {
+    out->path = GEMM_PATH_SCALE;
+    out->launches = 1;
+    return GEMM_OK;
+  }
+  if (M == 1 || N == 1) {
+    const bool row_major_w = N == 1 ? transA == GEMM_OP_N : transB == GEMM_OP_T;
+    const int64_t R = N == 1 ? M : N;
+    out->launches = 1;
+    if (row_major_w) {
+      out->path = K <= dg::gemv_rowdot_max_k() ? GEMM_PATH_GEMV_ROWDOT : GEMM_PATH_GEMV_GENERIC;
+    } else {
+      const dg::ColstreamPlan cp = dg::plan_gemv_colstream(int(R), int(K), sms);
+      out->path = GEMM_PATH_GEMV_COLSTREAM;
+      out->splitk = cp.ksplit;
+      out->grid = cp.panels * cp.ksplit;
+      out->workspace_bytes = cp.ws_bytes;
+    }
+    return GEMM_OK;
+  }
+  choose_tc(M, N, K, sms, out_is_f32(dtype) ? 4 : 2, false, out);
+  out->launches = out->splitk > 1 ? 2 : 1;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_quantization(int64_t M, int64_t N, int32_t tile_m, int32_t tile_n,
+                                int32_t splitk, int32_t sms, int32_t ctas_per_sm,
+                                gemm_config_info_t* out) {
+  if (!out || M < 0 || N < 0 || tile_m <= 0 || tile_n <= 0 || splitk <= 0 || sms <= 0 ||
+      ctas_per_sm <= 0)
+    return GEMM_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  quantization(M, N, tile_m, tile_n, splitk, sms, ctas_per_sm, out);
+  return GEMM_OK;
+}
+
+}  // extern "C"

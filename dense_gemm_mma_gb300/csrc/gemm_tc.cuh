@@ -1,0 +1,393 @@
+// gemm_tc.cuh -- persistent, warp-specialised tcgen05 GEMM for sm_103a.
+//
+// What it computes ("Matrix Multiplication Background User's Guide", section
+// 2.1, GPU Implementation, Fig. 1): the output is cut into TC_BM x BN tiles;
+// each tile walks K in TC_BK steps, loading the A and B blocks it needs and
+// accumulating their products ("Learning Triton One Kernel at a Time: Matrix
+// Multiplication", section Tiled GEMM: partial dot products over blocks of the
+// shared dimension sum to the same result).  Blocks are staged on chip and
+// reused by every output of the tile ("GEMM kernels", section Improving the
+// naive matrix multiplier: shared-memory tiles; register coarsening becomes
+// the 128 x BN fp32 accumulator held in tensor memory).
+//
+// GB300 mapping:
+//  - warp 0, one lane: TMA producer.  For each k-block it waits for a free
+//    stage of an S-deep shared-memory ring (mbarrier "empty"), arms "full"
+//    with the expected byte count and issues 2-D tensor-map loads of the A
+//    and B blocks (128-byte swizzle, out-of-range elements read as zero, which
+//    handles every ragged M/N/K edge -- the zero padding of the block-pointer
+//    loads in "Learning Triton ...", section Triton implementation).
+//  - warp 1, one lane: MMA issuer.  Waits for "full", issues TC_BK/16
+//    tcgen05.mma (M=128, N=BN, K=16, kind::f16) into an fp32 accumulator in
+//    tensor memory, and commits to "empty" so the stage is refilled as soon
+//    as the tensor core is done with it.  At the end of a tile it commits to
+//    "tmem_full".  Tensor memory holds two accumulators (2*BN columns), so the
+//    epilogue of one tile overlaps the main loop of the next.
+//  - warps 2-5: epilogue.  Each warp owns the 32 tensor-memory lanes (output
+//    rows) that its warp index allows, reads 32-column slices with
+//    tcgen05.ld, applies alpha/beta/LeakyReLU, converts with round-to-nearest-
+//    even, writes a 32 x 128-byte swizzled box to shared memory and stores it
+//    with one TMA store (coalesced 128-byte rows, clipped at the matrix edge).
+//    With beta != 0 the same box of C is first TMA-loaded into that buffer.
+//  - persistence: gridDim.x <= #SMs CTAs walk the work units
+//    u = blockIdx.x, blockIdx.x + gridDim.x, ... ("GEMM kernels", section
+//    Understanding the naive matrix multiplier: blocks are queued onto SMs and
+//    stay there; here the queue is explicit).  Units are ordered slice-major,
+//    then in groups of `raster_group` tile rows so that concurrently running
+//    tiles share A and B blocks in L2.
+//  - split-K: a unit may cover only a K slice; then the epilogue writes raw
+//    fp32 partials to the workspace and a separate kernel sums the slices in a
+//    fixed order ("Matrix Multiplication Background User's Guide", section 2.3:
+//    splitting along K needs a final reduction).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dg {
+
+template <int BN>
+struct TcCfg {
+  static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int A_STAGE = TC_BM * TC_BK * 2;  // 16 KB
+  static constexpr int B_STAGE = BN * TC_BK * 2;
+  static constexpr int STG_BYTES = 32 * 128;         // one 32-row x 128-byte epilogue box
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+  static constexpr int OFF_STG = OFF_B + STAGES * B_STAGE;
+  static constexpr int OFF_BAR = OFF_STG + TC_EPI_WARPS * 2 * STG_BYTES;
+  // full[S], empty[S], tmem_full[2], tmem_empty[2], c_load[4], drain[1]
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + TC_EPI_WARPS + 1;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem address, abort flag
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-B alignment
+  static constexpr int TMEM_COLS = 2 * BN;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(TMEM_COLS <= 512, "tensor memory budget");
+};
+
+struct Unit {
+  int m_blk, n_blk, split, kb_begin, kb_end;
+};
+
+// Work unit u -> (tile, K slice).  Slice-major; inside a slice, groups of
+// raster_group tile rows, each group walked column by column.
+__device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
+  const int tiles = p.num_m_blocks * p.num_n_blocks;
+  Unit x;
+  x.split = u / tiles;
+  const int t = u - x.split * tiles;
+  const int per_group = p.raster_group * p.num_n_blocks;
+  const int g = t / per_group;
+  const int first_m = g * p.raster_group;
+  const int rows_in_group = min(p.num_m_blocks - first_m, p.raster_group);
+  const int r = t - g * per_group;
+  x.m_blk = first_m + r % rows_in_group;
+  x.n_blk = r / rows_in_group;
+  x.kb_begin = x.split * p.kb_per_split;
+  x.kb_end = min(p.k_blocks, x.kb_begin + p.kb_per_split);
+  return x;
+}
+
+__device__ __forceinline__ float epi_value(float acc, float c, const TcParams& p, bool has_beta) {
+  float v = p.alpha * acc;
+  if (has_beta) v = fmaf(p.beta, c, v);
+  if (p.act == 1) v = v < 0.f ? v * p.slope : v;
+  return v;
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, int out_kind) {
+  if (out_kind == OUT_BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float2 unpack2(uint32_t w, int out_kind) {
+  if (out_kind == OUT_BF16) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
+    return __bfloat1622float2(h);
+  }
+  __half2 h = *reinterpret_cast<__half2*>(&w);
+  return __half22float2(h);
+}
+
+template <int BN>
+__global__ void __launch_bounds__(TC_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ TcParams p) {
+  using Cfg = TcCfg<BN>;
+  constexpr int S = Cfg::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const sbase = smem_raw + (base - raw);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t bar0 = base + Cfg::OFF_BAR;
+  const uint32_t full0 = bar0, empty0 = bar0 + 8 * S;
+  const uint32_t tfull0 = bar0 + 16 * S, tempty0 = tfull0 + 16;
+  const uint32_t cload0 = tempty0 + 16, drain_bar = cload0 + 8 * TC_EPI_WARPS;
+  uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + Cfg::OFF_MISC);
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(sbase + Cfg::OFF_MISC + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull0 + 8 * b, 1);
+      mbar_init(tempty0 + 8 * b, TC_EPI_WARPS);
+    }
+    for (int e = 0; e < TC_EPI_WARPS; ++e) mbar_init(cload0 + 8 * e, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmC);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const Watch w{abort_flag, p.err, p.timeout_ns};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        const Unit x = decode_unit(u, p);
+        const int m0 = x.m_blk * TC_BM, n0 = x.n_blk * BN;
+        for (int kb = x.kb_begin; kb < x.kb_end; ++kb) {
+          if (!wait_bar(empty0 + 8 * stage, phase ^ 1u, w, WAIT_PRODUCER_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * stage;
+          const uint32_t sa = base + Cfg::OFF_A + stage * Cfg::A_STAGE;
+          const uint32_t sb = base + Cfg::OFF_B + stage * Cfg::B_STAGE;
+          mbar_arrive_expect_tx(fb, Cfg::A_STAGE + Cfg::B_STAGE);
+          const int k0 = kb * TC_BK;
+          if (!p.a_mn_major) {
+            tma_load_2d(sa, &tmA, fb, k0, m0);  // 128 rows x 64 K
+          } else {
+            tma_load_2d(sa, &tmA, fb, m0, k0);  // 64 K rows x 64 M, twice
+            tma_load_2d(sa + 64 * 128, &tmA, fb, m0 + 64, k0);
+          }
+          if (!p.b_mn_major) {
+            tma_load_2d(sb, &tmB, fb, k0, n0);  // BN rows x 64 K
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 64 * 128, &tmB, fb, n0 + 64 * j, k0);
+          }
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // Let the loads already in flight land before the CTA can exit.
+        for (int s = 0; s < S; ++s) {
+          const int n_s = issued > s ? (issued - s + S - 1) / S : 0;
+          if (n_s > 0) wait_bar(full0 + 8 * s, (uint32_t)((n_s - 1) & 1), Watch{abort_flag, p.err, p.timeout_ns}, 0);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t lbo_a = p.a_mn_major ? 64 * 128 : 16;
+      const uint32_t lbo_b = p.b_mn_major ? 64 * 128 : 16;
+      const uint32_t kstep_a = p.a_mn_major ? 16 * 128 : 32;
+      const uint32_t kstep_b = p.b_mn_major ? 16 * 128 : 32;
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+        const Unit x = decode_unit(u, p);
+        if (!wait_bar(tempty0 + 8 * acc, acc_phase ^ 1u, w, WAIT_MMA_TMEM_EMPTY)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = x.kb_begin; kb < x.kb_end; ++kb) {
+          if (!wait_bar(full0 + 8 * stage, phase, w, WAIT_MMA_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = base + Cfg::OFF_A + stage * Cfg::A_STAGE;
+          const uint32_t sb = base + Cfg::OFF_B + stage * Cfg::B_STAGE;
+#pragma unroll
+          for (int kk = 0; kk < TC_BK / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(sa + kk * kstep_a, lbo_a, 1024);
+            const uint64_t bd = smem_desc_sw128(sb + kk * kstep_b, lbo_b, 1024);
+            tc_mma_f16(d_tmem, ad, bd, p.idesc, (kb > x.kb_begin || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(empty0 + 8 * stage);  // stage free once these MMAs finish
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull0 + 8 * acc);  // accumulator ready for the epilogue
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // Every MMA issued by this thread completes before tensor memory is freed.
+      tc_commit(drain_bar);
+      wait_bar(drain_bar, 0, Watch{abort_flag, p.err, p.timeout_ns}, WAIT_DRAIN);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int e = warp - 2;  // staging buffers / C-load barrier of this warp
+    const int q = warp & 3;  // tensor-memory lane quarter this warp may read
+    const bool partial = p.out_kind == OUT_PARTIAL;
+    const bool has_beta = !partial && p.beta != 0.f;
+    const int esize = (p.out_kind == OUT_F32 || partial) ? 4 : 2;
+    const int cw = 128 / esize;  // columns per 128-byte box row
+    const uint32_t stg0 = base + Cfg::OFF_STG + e * 2 * Cfg::STG_BYTES;
+    uint8_t* const stg_p0 = sbase + Cfg::OFF_STG + e * 2 * Cfg::STG_BYTES;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int sbuf = 0;
+    uint32_t cphase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      const Unit x = decode_unit(u, p);
+      // All lanes wait; the warp leaves together if any lane gave up, because the
+      // tcgen05.ld below must be executed by the whole warp.
+      if (!__all_sync(0xffffffffu, wait_bar(tfull0 + 8 * acc, acc_phase, w, WAIT_EPI_TMEM_FULL)))
+        break;
+      tc_fence_after();
+      const int n0 = x.n_blk * BN;
+      const int row0 = x.m_blk * TC_BM + 32 * q;
+      const int y0 = partial ? x.split * p.ws_rows + row0 : row0;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+      const int chunks = BN / cw;
+      for (int c = 0; c < chunks; ++c) {
+        const uint32_t stg = stg0 + sbuf * Cfg::STG_BYTES;
+        uint8_t* const stg_p = stg_p0 + sbuf * Cfg::STG_BYTES;
+        const int x0 = n0 + c * cw;
+        if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
+        __syncwarp();
+        if (has_beta) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(cload0 + 8 * e, Cfg::STG_BYTES);
+            tma_load_2d(stg, &tmC, cload0 + 8 * e, x0, y0);
+          }
+          if (!__all_sync(0xffffffffu, wait_bar(cload0 + 8 * e, cphase, w, WAIT_EPI_C_LOAD))) {
+            ok = false;
+            break;
+          }
+          cphase ^= 1u;
+        }
+        __syncwarp();
+        uint8_t* const row_p = stg_p + lane * 128;
+        const int sw = lane & 7;  // 128-byte swizzle: 16-byte chunk j lives at j ^ (row % 8)
+        if (esize == 4) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(t_row + c * 32, r);
+          tmem_ld_wait(r);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            float4* dst = reinterpret_cast<float4*>(row_p + ((j ^ sw) << 4));
+            float4 cv = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (has_beta) cv = *dst;
+            float4 o;
+            if (partial) {
+              o = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+            } else {
+              o.x = epi_value(__uint_as_float(r[4 * j + 0]), cv.x, p, has_beta);
+              o.y = epi_value(__uint_as_float(r[4 * j + 1]), cv.y, p, has_beta);
+              o.z = epi_value(__uint_as_float(r[4 * j + 2]), cv.z, p, has_beta);
+              o.w = epi_value(__uint_as_float(r[4 * j + 3]), cv.w, p, has_beta);
+            }
+            *dst = o;
+          }
+        } else {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32x32b_x32(t_row + c * 64, r0);
+          tmem_ld_32x32b_x32(t_row + c * 64 + 32, r1);
+          tmem_ld_wait(r0);
+          tmem_ld_wait(r1);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint4* dst = reinterpret_cast<uint4*>(row_p + ((j ^ sw) << 4));
+            uint4 cv = make_uint4(0u, 0u, 0u, 0u);
+            if (has_beta) cv = *dst;
+            const uint32_t* src = j < 4 ? &r0[8 * j] : &r1[8 * (j - 4)];
+            const uint32_t cw4[4] = {cv.x, cv.y, cv.z, cv.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const float2 cc = unpack2(cw4[t], p.out_kind);
+              const float a = epi_value(__uint_as_float(src[2 * t]), cc.x, p, has_beta);
+              const float b = epi_value(__uint_as_float(src[2 * t + 1]), cc.y, p, has_beta);
+              o[t] = pack2(a, b, p.out_kind);
+            }
+            *dst = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&tmC, stg, x0, y0);
+          bulk_commit();
+        }
+        sbuf ^= 1;
+      }
+      // This warp's reads of the accumulator are complete: release it.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait<0>();
+  }
+
+  // ------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+  }
+}
+
+template <int BN>
+cudaError_t launch_gemm_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                              const TcParams& p, int grid, cudaStream_t s) {
+  constexpr int smem = TcCfg<BN>::SMEM_BYTES;
+  cudaError_t err =
+      cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  gemm_tc_kernel<BN><<<grid, TC_THREADS, smem, s>>>(a, b, c, p);
+  return cudaGetLastError();
+}
+
+}  // namespace dg

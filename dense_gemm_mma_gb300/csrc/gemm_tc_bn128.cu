@@ -1,0 +1,7 @@
+// Tensor-core GEMM kernel instantiated for 128-column output tiles.
+#include "gemm_tc.cuh"
+
+namespace dg {
+template cudaError_t launch_gemm_tc_bn<128>(const CUtensorMap&, const CUtensorMap&,
+                                           const CUtensorMap&, const TcParams&, int, cudaStream_t);
+}  // namespace dg

@@ -1,0 +1,409 @@
+// gemv.cu -- memory-bound kernels: GEMV (M == 1 or N == 1), the fixed-order
+// split-K reduction, C <- act(beta*C), and the watchdog self-test.
+//
+// "Matrix Multiplication Background User's Guide", section 2: a
+// matrix-vector product (M == 1 or N == 1) has an arithmetic intensity below
+// one FLOP per byte and is always memory-bound, so these kernels use no tensor
+// cores: they stream the matrix once with 128-bit loads, coalesced across the
+// warp ("Learning Triton One Kernel at a Time: Matrix Multiplication", section
+// Memory coalescing: consecutive threads read consecutive addresses), and
+// reduce with warp shuffles.  Every sum is taken in a fixed order, so results
+// do not depend on scheduling.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dg {
+
+namespace {
+
+constexpr int kRowdotThreads = 256;
+constexpr int kRowdotMaxK = 32768;  // x staged in shared memory: 64 KB of 16-bit values
+constexpr int kColThreads = 256;
+constexpr int kColGroups = 4;             // K-interleaved thread groups per CTA
+constexpr int kColCols = 8 * (kColThreads / kColGroups);  // 512 columns per CTA
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+template <bool F16>
+__device__ __forceinline__ float2 to_f2(uint32_t w) {
+  if (F16) {
+    __half2 h = *reinterpret_cast<__half2*>(&w);
+    return __half22float2(h);
+  }
+  __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&w);
+  return __bfloat1622float2(h);
+}
+
+template <bool F16>
+__device__ __forceinline__ float to_f(uint16_t v) {
+  if (F16) return __half2float(__ushort_as_half(v));
+  return __bfloat162float(__ushort_as_bfloat16(v));
+}
+
+// acc += dot of 8 packed elements
+template <bool F16>
+__device__ __forceinline__ float dot8(uint4 a, uint4 b, float acc) {
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+  const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float2 fa = to_f2<F16>(aw[t]);
+    const float2 fb = to_f2<F16>(bw[t]);
+    acc = fmaf(fa.x, fb.x, acc);
+    acc = fmaf(fa.y, fb.y, acc);
+  }
+  return acc;
+}
+
+__device__ __forceinline__ float load_c(const void* C, int64_t idx, int kind) {
+  if (kind == OUT_F32) return static_cast<const float*>(C)[idx];
+  const uint16_t v = static_cast<const uint16_t*>(C)[idx];
+  if (kind == OUT_BF16) return __bfloat162float(__ushort_as_bfloat16(v));
+  return __half2float(__ushort_as_half(v));
+}
+
+__device__ __forceinline__ void store_c(void* C, int64_t idx, float v, int kind) {
+  if (kind == OUT_F32) {
+    static_cast<float*>(C)[idx] = v;
+  } else if (kind == OUT_BF16) {
+    static_cast<__nv_bfloat16*>(C)[idx] = __float2bfloat16_rn(v);
+  } else {
+    static_cast<__half*>(C)[idx] = __float2half_rn(v);
+  }
+}
+
+// alpha*acc + beta*C (C not read when beta == 0), then the activation.
+__device__ __forceinline__ float epilogue(float acc, const void* C, int64_t idx, const EpiParams& e) {
+  float v = e.alpha * acc;
+  if (e.beta != 0.f) v = fmaf(e.beta, load_c(C, idx, e.out_kind), v);
+  if (e.act == 1 && v < 0.f) v *= e.slope;
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ------------------------------------------------------------------ rowdot
+// One warp per row of W (row-contiguous, 16-byte aligned rows); x staged in
+// shared memory; each lane reads 16 bytes per step, four steps in flight.
+template <bool F16>
+__global__ void __launch_bounds__(kRowdotThreads)
+    gemv_rowdot_kernel(const GemvArgs g) {
+  extern __shared__ __align__(16) uint16_t xs[];
+  const uint16_t* x = static_cast<const uint16_t*>(g.x);
+  const int K = g.K;
+  const int K8 = (K + 7) & ~7;
+  for (int k = threadIdx.x; k < K8; k += blockDim.x) xs[k] = k < K ? x[k * g.incx] : 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wpb = kRowdotThreads / 32;
+  const int nvec = K >> 3;
+  const uint4* xv = reinterpret_cast<const uint4*>(xs);
+  for (int r = blockIdx.x * wpb + warp; r < g.R; r += gridDim.x * wpb) {
+    const uint16_t* wrow = static_cast<const uint16_t*>(g.W) + static_cast<int64_t>(r) * g.ldw;
+    const uint4* wv = reinterpret_cast<const uint4*>(wrow);
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int v = lane;
+    for (; v + 96 < nvec; v += 128) {
+      const uint4 w0 = ldg_stream(wv + v), w1 = ldg_stream(wv + v + 32);
+      const uint4 w2 = ldg_stream(wv + v + 64), w3 = ldg_stream(wv + v + 96);
+      a0 = dot8<F16>(w0, xv[v], a0);
+      a1 = dot8<F16>(w1, xv[v + 32], a1);
+      a2 = dot8<F16>(w2, xv[v + 64], a2);
+      a3 = dot8<F16>(w3, xv[v + 96], a3);
+    }
+    for (; v < nvec; v += 32) a0 = dot8<F16>(ldg_stream(wv + v), xv[v], a0);
+    for (int k = nvec * 8 + lane; k < K; k += 32) a1 = fmaf(to_f<F16>(wrow[k]), to_f<F16>(xs[k]), a1);
+    const float acc = warp_sum((a0 + a1) + (a2 + a3));
+    if (lane == 0) {
+      const int64_t idx = static_cast<int64_t>(r) * g.inc_out;
+      store_c(g.out, idx, epilogue(acc, g.out, idx, g.e), g.e.out_kind);
+    }
+  }
+}
+
+// --------------------------------------------------------------- colstream
+// W is K x R with R contiguous.  CTA (panel, z) covers columns
+// [panel*512, panel*512+512) and K rows [z*kc, z*kc+kc); its 256 threads form
+// 4 groups of 64, each thread owning 8 adjacent columns (one 16-byte load per
+// row) and every 4th row of the slice.  The groups are summed in shared
+// memory in a fixed order.  With ksplit > 1 each CTA writes its 512 partial
+// sums to the workspace; the CTA that finishes a panel last (per-panel
+// counter) sums the slices in order z = 0, 1, ... and applies the epilogue,
+// then resets the counter for the next call.
+template <bool F16>
+__global__ void __launch_bounds__(kColThreads)
+    gemv_colstream_kernel(const GemvArgs g, const ColstreamPlan cp, float* ws, unsigned* counters) {
+  __shared__ float red[kColGroups][kColCols];
+  __shared__ unsigned ticket;
+  const int panel = blockIdx.x, z = blockIdx.y;
+  const int t = threadIdx.x % (kColThreads / kColGroups);
+  const int grp = threadIdx.x / (kColThreads / kColGroups);
+  const int col0 = panel * kColCols + t * 8;
+  const int kb = z * cp.kc;
+  const int ke = min(g.K, kb + cp.kc);
+  const uint16_t* W = static_cast<const uint16_t*>(g.W);
+  const uint16_t* x = static_cast<const uint16_t*>(g.x);
+  float acc[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+
+  if (col0 + 8 <= g.R) {
+    int k = kb + grp;
+    for (; k + 3 * kColGroups < ke; k += 4 * kColGroups) {
+      uint4 wv[4];
+      float xf[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        wv[i] = ldg_stream(W + static_cast<int64_t>(k + i * kColGroups) * g.ldw + col0);
+        xf[i] = to_f<F16>(x[static_cast<int64_t>(k + i * kColGroups) * g.incx]);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 f = to_f2<F16>(ww[q]);
+          acc[2 * q] = fmaf(f.x, xf[i], acc[2 * q]);
+          acc[2 * q + 1] = fmaf(f.y, xf[i], acc[2 * q + 1]);
+        }
+      }
+    }
+    for (; k < ke; k += kColGroups) {
+      const uint4 wv = ldg_stream(W + static_cast<int64_t>(k) * g.ldw + col0);
+      const float xf = to_f<F16>(x[static_cast<int64_t>(k) * g.incx]);
+      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = to_f2<F16>(ww[q]);
+        acc[2 * q] = fmaf(f.x, xf, acc[2 * q]);
+        acc[2 * q + 1] = fmaf(f.y, xf, acc[2 * q + 1]);
+      }
+    }
+  } else if (col0 < g.R) {
+    const int nc = g.R - col0;
+    for (int k = kb + grp; k < ke; k += kColGroups) {
+      const float xf = to_f<F16>(x[static_cast<int64_t>(k) * g.incx]);
+      for (int j = 0; j < nc; ++j)
+        acc[j] = fmaf(to_f<F16>(W[static_cast<int64_t>(k) * g.ldw + col0 + j]), xf, acc[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) red[grp][t * 8 + j] = acc[j];
+  __syncthreads();
+
+  const int rpad = cp.panels * kColCols;
+  for (int c = threadIdx.x; c < kColCols; c += kColThreads) {
+    const int col = panel * kColCols + c;
+    float s = red[0][c];
+#pragma unroll
+    for (int q = 1; q < kColGroups; ++q) s += red[q][c];
+    if (col < g.R) {
+      if (cp.ksplit == 1) {
+        const int64_t idx = static_cast<int64_t>(col) * g.inc_out;
+        store_c(g.out, idx, epilogue(s, g.out, idx, g.e), g.e.out_kind);
+      } else {
+        ws[static_cast<int64_t>(z) * rpad + col] = s;
+      }
+    }
+  }
+  if (cp.ksplit == 1) return;
+
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) ticket = atomicAdd(&counters[panel], 1u);
+  __syncthreads();
+  if (ticket != static_cast<unsigned>(cp.ksplit - 1)) return;
+  __threadfence();
+  for (int c = threadIdx.x; c < kColCols; c += kColThreads) {
+    const int col = panel * kColCols + c;
+    if (col >= g.R) break;
+    float s = 0.f;
+    for (int zz = 0; zz < cp.ksplit; ++zz) s += __ldcg(ws + static_cast<int64_t>(zz) * rpad + col);
+    const int64_t idx = static_cast<int64_t>(col) * g.inc_out;
+    store_c(g.out, idx, epilogue(s, g.out, idx, g.e), g.e.out_kind);
+  }
+  if (threadIdx.x == 0) counters[panel] = 0u;
+}
+
+// ----------------------------------------------------------------- generic
+// Any strides: one warp per output, lanes interleaved over K.
+template <bool F16>
+__global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvArgs g) {
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const uint16_t* W = static_cast<const uint16_t*>(g.W);
+  const uint16_t* x = static_cast<const uint16_t*>(g.x);
+  for (int r = gw; r < g.R; r += nw) {
+    float acc = 0.f;
+    for (int k = lane; k < g.K; k += 32)
+      acc = fmaf(to_f<F16>(W[static_cast<int64_t>(r) * g.w_rs + static_cast<int64_t>(k) * g.w_cs]),
+                 to_f<F16>(x[static_cast<int64_t>(k) * g.incx]), acc);
+    acc = warp_sum(acc);
+    if (lane == 0) {
+      const int64_t idx = static_cast<int64_t>(r) * g.inc_out;
+      store_c(g.out, idx, epilogue(acc, g.out, idx, g.e), g.e.out_kind);
+    }
+  }
+}
+
+// ------------------------------------------------------------ split-K reduce
+// One thread per 4 adjacent columns of a row: sums the slices s = 0..S-1 in
+// order (16-byte loads; the workspace row stride is a multiple of 4 floats),
+// applies the epilogue and stores 4 outputs.
+__global__ void __launch_bounds__(256)
+    splitk_reduce_kernel(const float* __restrict__ ws, int64_t ws_ld, int64_t ws_slice, int splits,
+                         int M, int N, void* C, int64_t ldc, const EpiParams e) {
+  const int gpr = (N + 3) >> 2;
+  const int64_t total = static_cast<int64_t>(M) * gpr;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int m = static_cast<int>(i / gpr);
+    const int n = static_cast<int>(i - static_cast<int64_t>(m) * gpr) * 4;
+    const float* src = ws + static_cast<int64_t>(m) * ws_ld + n;
+    float4 s = __ldcs(reinterpret_cast<const float4*>(src));
+    for (int sp = 1; sp < splits; ++sp) {
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(src + sp * ws_slice));
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
+    }
+    const float sv[4] = {s.x, s.y, s.z, s.w};
+    const int64_t base = static_cast<int64_t>(m) * ldc + n;
+    const int nn = min(4, N - n);
+    for (int j = 0; j < nn; ++j) store_c(C, base + j, epilogue(sv[j], C, base + j, e), e.out_kind);
+  }
+}
+
+// ------------------------------------------------------------------- scale
+__global__ void __launch_bounds__(256) scale_kernel(int M, int N, void* C, int64_t ldc, const EpiParams e) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int m = static_cast<int>(i / N);
+    const int n = static_cast<int>(i - static_cast<int64_t>(m) * N);
+    const int64_t idx = static_cast<int64_t>(m) * ldc + n;
+    float v = e.beta != 0.f ? e.beta * load_c(C, idx, e.out_kind) : 0.f;
+    if (e.act == 1 && v < 0.f) v *= e.slope;
+    store_c(C, idx, v, e.out_kind);
+  }
+}
+
+// --------------------------------------------------------- watchdog self-test
+__global__ void watchdog_selftest_kernel(int* err, uint64_t timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const Watch w{&abort_flag, err, timeout_ns};
+    wait_bar(smem_u32(&bar), 0, w, WAIT_SELFTEST);  // nothing ever arrives
+  }
+}
+
+int grid_for(int64_t items, int per_block, int sms, int blocks_per_sm) {
+  int64_t g = (items + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(sms) * blocks_per_sm;
+  if (g > cap) g = cap;
+  return g < 1 ? 1 : static_cast<int>(g);
+}
+
+}  // namespace
+
+int gemv_rowdot_max_k() { return kRowdotMaxK; }
+
+cudaError_t launch_gemv_rowdot(const GemvArgs& g, cudaStream_t s, int sms) {
+  const int smem = ((g.K + 7) & ~7) * 2;
+  const int grid = grid_for(g.R, kRowdotThreads / 32, sms, 8);
+  if (g.in_f16) {
+    if (smem > 48 * 1024)
+      cudaFuncSetAttribute(gemv_rowdot_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    gemv_rowdot_kernel<true><<<grid, kRowdotThreads, smem, s>>>(g);
+  } else {
+    if (smem > 48 * 1024)
+      cudaFuncSetAttribute(gemv_rowdot_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    gemv_rowdot_kernel<false><<<grid, kRowdotThreads, smem, s>>>(g);
+  }
+  return cudaGetLastError();
+}
+
+ColstreamPlan plan_gemv_colstream(int R, int K, int sms) {
+  ColstreamPlan cp;
+  cp.panels = (R + kColCols - 1) / kColCols;
+  const int target = sms * 8;  // eight 256-thread CTAs per SM
+  int ksplit = (target + cp.panels - 1) / cp.panels;
+  const int max_split = (K + 63) / 64;  // at least 64 rows (16 per thread) per slice
+  if (ksplit > max_split) ksplit = max_split;
+  if (ksplit < 1) ksplit = 1;
+  cp.kc = (K + ksplit - 1) / ksplit;
+  cp.ksplit = (K + cp.kc - 1) / cp.kc;
+  if (cp.ksplit < 1) cp.ksplit = 1;
+  cp.ws_bytes = cp.ksplit > 1
+                    ? static_cast<int64_t>(cp.ksplit) * cp.panels * kColCols * 4 + cp.panels * 4
+                    : 0;
+  return cp;
+}
+
+cudaError_t launch_gemv_colstream(const GemvArgs& g, const ColstreamPlan& cp, void* ws,
+                                  cudaStream_t s) {
+  float* part = static_cast<float*>(ws);
+  unsigned* counters =
+      cp.ksplit > 1
+          ? reinterpret_cast<unsigned*>(part + static_cast<int64_t>(cp.ksplit) * cp.panels * kColCols)
+          : nullptr;
+  const dim3 grid(cp.panels, cp.ksplit);
+  if (g.in_f16)
+    gemv_colstream_kernel<true><<<grid, kColThreads, 0, s>>>(g, cp, part, counters);
+  else
+    gemv_colstream_kernel<false><<<grid, kColThreads, 0, s>>>(g, cp, part, counters);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_generic(const GemvArgs& g, cudaStream_t s, int sms) {
+  const int grid = grid_for(g.R, 8, sms, 8);
+  if (g.in_f16)
+    gemv_generic_kernel<true><<<grid, 256, 0, s>>>(g);
+  else
+    gemv_generic_kernel<false><<<grid, 256, 0, s>>>(g);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_splitk_reduce(const float* ws, int64_t ws_ld, int64_t ws_slice, int splits,
+                                 int M, int N, void* C, int64_t ldc, EpiParams e, cudaStream_t s,
+                                 int sms) {
+  const int64_t items = static_cast<int64_t>(M) * ((N + 3) / 4);
+  splitk_reduce_kernel<<<grid_for(items, 256, sms, 8), 256, 0, s>>>(ws, ws_ld, ws_slice, splits, M,
+                                                                    N, C, ldc, e);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale(int M, int N, void* C, int64_t ldc, EpiParams e, cudaStream_t s, int sms) {
+  const int64_t items = static_cast<int64_t>(M) * N;
+  scale_kernel<<<grid_for(items, 256, sms, 8), 256, 0, s>>>(M, N, C, ldc, e);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_watchdog_selftest(int* err, uint64_t timeout_ns, cudaStream_t s) {
+  watchdog_selftest_kernel<<<1, 32, 0, s>>>(err, timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace dg

@@ -1,0 +1,112 @@
+// kernels.h -- parameter blocks and launchers shared by the host planner
+// (api.cpp) and the CUDA kernels.  Internal to the library.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dg {
+
+// Output kinds of the tensor-core epilogue and of the GEMV / reduction kernels.
+enum OutKind : int {
+  OUT_F32 = 0,
+  OUT_BF16 = 1,
+  OUT_F16 = 2,
+  OUT_PARTIAL = 3  // raw fp32 partial sums of one K slice into the workspace
+};
+
+// Codes OR-ed into the plan's error word by a wait that ran out.
+enum WaitCode : int {
+  WAIT_PRODUCER_EMPTY = 1,
+  WAIT_MMA_FULL = 2,
+  WAIT_MMA_TMEM_EMPTY = 4,
+  WAIT_EPI_TMEM_FULL = 8,
+  WAIT_EPI_C_LOAD = 16,
+  WAIT_DRAIN = 32,
+  WAIT_SELFTEST = 64
+};
+
+constexpr int TC_BM = 128;       // output rows per tile (one tcgen05.mma M=128)
+constexpr int TC_BK = 64;        // K elements per stage: 64 x 2 B = one 128-B swizzle row
+constexpr int TC_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
+constexpr int TC_EPI_WARPS = 4;
+
+struct TcParams {
+  int M, N, K;
+  int num_m_blocks, num_n_blocks;
+  int k_blocks;      // ceil(K / TC_BK)
+  int splitk;        // K slices (1 = plain GEMM)
+  int kb_per_split;  // k-blocks per slice (the last one may be shorter)
+  int raster_group;  // output-tile rows per rasterisation group
+  int units;         // num_m_blocks * num_n_blocks * splitk
+  int ws_rows;       // workspace rows per slice (num_m_blocks * TC_BM), OUT_PARTIAL only
+  int out_kind;      // OutKind
+  int a_mn_major;    // A stored K x M (M contiguous)
+  int b_mn_major;    // B stored K x N (N contiguous)
+  uint32_t idesc;    // tcgen05 instruction descriptor
+  float alpha, beta, slope;
+  int act;
+  int* err;          // plan error word
+  uint64_t timeout_ns;
+};
+
+// Shared-memory footprint of the tensor-core kernel for a tile width.
+int tc_smem_bytes(int bn);
+int tc_stages(int bn);
+
+cudaError_t launch_gemm_tc(int bn, const CUtensorMap& a, const CUtensorMap& b,
+                           const CUtensorMap& c, const TcParams& p, int grid, cudaStream_t s);
+
+struct EpiParams {
+  float alpha, beta, slope;
+  int act;
+  int out_kind;  // OUT_F32 / OUT_BF16 / OUT_F16
+};
+
+// Fixed-order sum of `splits` fp32 partial slices, then the epilogue into C.
+cudaError_t launch_splitk_reduce(const float* ws, int64_t ws_ld, int64_t ws_slice, int splits,
+                                 int M, int N, void* C, int64_t ldc, EpiParams e,
+                                 cudaStream_t s, int sms);
+
+// C <- act(beta * C) (K == 0 or alpha == 0).
+cudaError_t launch_scale(int M, int N, void* C, int64_t ldc, EpiParams e, cudaStream_t s,
+                         int sms);
+
+// GEMV, operand type in_f16 (0 = bf16, 1 = fp16).
+// rowdot:    out[r*inc_out] = epi(sum_k W[r*ldw + k] * x[k*incx]),  r < R
+// colstream: out[c*inc_out] = epi(sum_k W[k*ldw + c] * x[k*incx]),  c < R
+// generic:   out[r*inc_out] = epi(sum_k W[r*w_rs + k*w_cs] * x[k*incx])
+struct GemvArgs {
+  const void* W;
+  int64_t ldw;
+  int64_t w_rs, w_cs;  // generic strides (elements)
+  int R, K;
+  const void* x;
+  int64_t incx;
+  void* out;
+  int64_t inc_out;
+  int in_f16;
+  EpiParams e;
+};
+
+int gemv_rowdot_max_k();
+cudaError_t launch_gemv_rowdot(const GemvArgs& g, cudaStream_t s, int sms);
+
+// Plan of the column-stream kernel: `ksplit` K slices of `kc` rows each.
+struct ColstreamPlan {
+  int panels;  // ceil(R / 512)
+  int ksplit;
+  int kc;
+  int64_t ws_bytes;  // partials + per-panel counters (0 when ksplit == 1)
+};
+ColstreamPlan plan_gemv_colstream(int R, int K, int sms);
+cudaError_t launch_gemv_colstream(const GemvArgs& g, const ColstreamPlan& cp, void* ws,
+                                  cudaStream_t s);
+
+cudaError_t launch_gemv_generic(const GemvArgs& g, cudaStream_t s, int sms);
+
+// One CTA waits on a barrier that nothing arrives on; gives up after timeout_ns.
+cudaError_t launch_watchdog_selftest(int* err, uint64_t timeout_ns, cudaStream_t s);
+
+}  // namespace dg

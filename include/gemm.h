@@ -1,0 +1,218 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) dense GEMM / GEMV library
+ * (libdgemm_gb300.so).
+ *
+ * Operation (one call):
+ *
+ *     C <- act(alpha * op(A) @ op(B) + beta * C)
+ *
+ * op(A) is M x K, op(B) is K x N and C is M x N, following the BLAS naming of
+ * "Matrix Multiplication Background User's Guide", section 2 (Math and Memory
+ * Bounds); every output is a K-long dot product, 2*M*N*K floating-point
+ * operations in all.  The guide's display formula for GEMM is lost in the
+ * extracted text: the BLAS form above is the reading taken.  act is the
+ * identity or LeakyReLU, the fused output transform motivated by "OpenAI
+ * open-sources the Triton GPU language (part 2)", section Matrix
+ * multiplication.  Operands are bf16 or fp16, products are accumulated in
+ * fp32, C is fp32 or the operand type.
+ *
+ * Storage is row-major ("Learning Triton One Kernel at a Time: Matrix
+ * Multiplication", section Memory coalescing: a row is contiguous, a
+ * transpose changes the strides, not the memory):
+ *   transA = GEMM_OP_N: A is stored M x K,  op(A)(i,k) = A[i*lda + k]
+ *   transA = GEMM_OP_T: A is stored K x M,  op(A)(i,k) = A[k*lda + i]
+ *   transB = GEMM_OP_N: B is stored K x N,  op(B)(k,j) = B[k*ldb + j]
+ *   transB = GEMM_OP_T: B is stored N x K,  op(B)(k,j) = B[j*ldb + k]
+ *   C is stored M x N,                      C(i,j)     = C[i*ldc + j]
+ * Leading dimensions count elements.  Entries of a row beyond its logical
+ * width (the ld padding) are never read or written.
+ *
+ * Execution: gemm_run is asynchronous and stream-ordered on the caller's CUDA
+ * stream; it returns after enqueueing its kernels.  All device pointers are
+ * owned by the caller and must stay valid until the stream has run the call.
+ * The plan owns its workspace (split-K partials, GEMV partials, the watchdog
+ * word) and frees it in gemm_plan_destroy.  One plan must not be used by two
+ * host threads, or on two streams whose work may overlap, at the same time.
+ *
+ * Errors: argument problems are reported synchronously, before anything is
+ * launched, as a gemm_status_t; nothing aborts or throws across this ABI.
+ * There is no CPU fallback: without a usable sm_100-family GPU,
+ * gemm_plan_create returns GEMM_ERR_NO_DEVICE.
+ */
+#ifndef DGEMM_GB300_GEMM_H
+#define DGEMM_GB300_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct gemm_plan* gemm_plan_t;
+
+typedef enum {
+  GEMM_OK = 0,
+  GEMM_ERR_INVALID_ARG = 1,   /* null pointer, negative size, ld too small, bad enum  */
+  GEMM_ERR_ALIGNMENT = 2,     /* pointer or leading dimension breaks the rules below */
+  GEMM_ERR_UNSUPPORTED = 3,   /* size beyond what the kernels index (see gemm_run)   */
+  GEMM_ERR_NO_DEVICE = 4,     /* no CUDA device, or not compute capability 10.x      */
+  GEMM_ERR_OUT_OF_MEMORY = 5, /* workspace allocation failed                         */
+  GEMM_ERR_CUDA = 6,          /* a CUDA runtime/driver call or a launch failed       */
+  GEMM_ERR_TIMEOUT = 7        /* a kernel's bounded wait ran out (watchdog)          */
+} gemm_status_t;
+
+typedef enum { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
+
+/* operand type _ C type */
+typedef enum {
+  GEMM_BF16_F32 = 0,
+  GEMM_BF16_BF16 = 1,
+  GEMM_F16_F32 = 2,
+  GEMM_F16_F16 = 3
+} gemm_dtype_t;
+
+typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_LEAKY_RELU = 1 } gemm_act_t;
+
+/* act = GEMM_ACT_LEAKY_RELU applies x < 0 ? slope*x : x after alpha and beta. */
+typedef struct {
+  int32_t act;
+  float slope;
+} gemm_epilogue_t;
+
+/* Which kernels a call used. */
+typedef enum {
+  GEMM_PATH_NONE = 0,          /* M == 0 or N == 0: nothing launched                    */
+  GEMM_PATH_TC = 1,            /* tcgen05 tensor-core GEMM, epilogue fused               */
+  GEMM_PATH_TC_SPLITK = 2,     /* tcgen05 GEMM over K slices + fixed-order reduction     */
+  GEMM_PATH_GEMV_ROWDOT = 3,   /* GEMV: one warp per contiguous row                      */
+  GEMM_PATH_GEMV_COLSTREAM = 4,/* GEMV: threads own 8 contiguous columns, K split       */
+  GEMM_PATH_GEMV_GENERIC = 5,  /* GEMV with strided operands (no 128-bit loads)          */
+  GEMM_PATH_SCALE = 6          /* K == 0 or alpha == 0: C <- act(beta*C)                 */
+} gemm_path_t;
+
+/* Plan decisions and the tile/wave quantization they imply ("Matrix
+ * Multiplication Background User's Guide", section 3, Dimension Quantization
+ * Effects: section 3.1 tile quantization, section 3.2 wave quantization). */
+typedef struct {
+  int32_t path;            /* gemm_path_t                                              */
+  int32_t tile_m;          /* output tile rows (tensor-core paths)                     */
+  int32_t tile_n;          /* output tile columns                                      */
+  int32_t tile_k;          /* K elements per pipeline stage                            */
+  int32_t cta_per_tile;    /* CTAs that share one tile's MMA (1; 2 = CTA pair)         */
+  int32_t splitk;          /* K slices (1 = none)                                      */
+  int32_t stages;          /* shared-memory pipeline depth                             */
+  int32_t raster_group;    /* output-tile rows per rasterisation group                 */
+  int32_t grid;            /* CTAs launched for the main kernel                        */
+  int32_t sms;             /* streaming multiprocessors used for the wave size         */
+  int64_t tiles;           /* output tiles = ceil(M/tile_m) * ceil(N/tile_n)           */
+  int64_t units;           /* work units = tiles * splitk                              */
+  double waves;            /* units / wave size                                        */
+  double tail_fraction;    /* (units mod wave) / wave: SMs busy in the last wave, 0=full */
+  double useful_fraction;  /* M*N / (tiles*tile_m*tile_n): share of tile area in C     */
+  int32_t launches;        /* kernels the call launched                                */
+  int32_t reserved;
+  int64_t workspace_bytes; /* plan workspace the call used                             */
+} gemm_config_info_t;
+
+/* Create a plan bound to CUDA device `device` (the caller's current device is
+ * restored before returning).  Queries the SM count and allocates the
+ * watchdog word.  Returns GEMM_ERR_NO_DEVICE if the device does not exist or
+ * is not compute capability 10.x, GEMM_ERR_INVALID_ARG if plan is NULL. */
+gemm_status_t gemm_plan_create(gemm_plan_t* plan, int device);
+
+/* C <- act(alpha * op(A) @ op(B) + beta * C), enqueued on `stream` (a
+ * cudaStream_t; NULL means the legacy default stream).  See the top of this
+ * file for the layout of A, B and C; all three are device pointers.
+ *
+ * Dispatch: M == 0 or N == 0 launches nothing; K == 0 or alpha == 0 gives
+ * C <- act(beta*C) without reading A or B; M == 1 or N == 1 takes the
+ * memory-bound GEMV kernels (no tensor cores: "Matrix Multiplication
+ * Background User's Guide", section 2 notes that matrix-vector products are
+ * always memory-bound); everything else takes the tcgen05 tensor-core kernel,
+ * split along K when the output has too few tiles to fill the GPU (section
+ * 2.3 mentions splitting along K followed by a reduction).  With beta == 0,
+ * C is not read (NaN in C does not propagate).
+ *
+ * Rules, checked before any launch:
+ *  - M, N, K >= 0 and each < 2^31; lda >= stored columns of A (K for N, M
+ *    for T), ldb >= stored columns of B (N for N, K for T), ldc >= N; all >= 1.
+ *  - A and B may be NULL only if M*N == 0 or K == 0 or alpha == 0; C may be
+ *    NULL only if M*N == 0.  C must not overlap A or B.
+ *  - Every pointer is aligned to its element size.
+ *  - Tensor-core path (M >= 2 and N >= 2): A, B and C are 16-byte aligned and
+ *    lda, ldb, ldc times the element size are multiples of 16 bytes -- the
+ *    rule of Table 1 of the guide's section 2.2 for FP16 (multiples of 8
+ *    elements), which the Tensor Memory Accelerator requires here.
+ * Violations return GEMM_ERR_INVALID_ARG or GEMM_ERR_ALIGNMENT.
+ *
+ * Split-K and GEMV with K split use the plan's workspace; the first call that
+ * needs more than the plan holds grows it (stream-ordered allocation on
+ * `stream`) and can return GEMM_ERR_OUT_OF_MEMORY.  Launch failures return
+ * GEMM_ERR_CUDA.  A kernel whose bounded wait ran out sets the plan's
+ * watchdog word (see gemm_plan_poll_error); the call itself still returns
+ * GEMM_OK because it does not wait for the kernel.
+ *
+ * Results are deterministic: the same call on the same device gives the same
+ * bits every time (split-K sums its slices in a fixed order). */
+gemm_status_t gemm_run(gemm_plan_t plan, int64_t M, int64_t N, int64_t K,
+                       const void* A, int64_t lda, const void* B, int64_t ldb,
+                       void* C, int64_t ldc, float alpha, float beta,
+                       gemm_dtype_t dtype, gemm_op_t transA, gemm_op_t transB,
+                       gemm_epilogue_t epilogue, void* stream);
+
+/* Free the plan and its workspace (synchronises the plan's device).  NULL is
+ * accepted and ignored. */
+gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
+
+/* Static, human-readable text for a status code. */
+const char* gemm_status_string(gemm_status_t status);
+
+/* Decisions of the plan's most recent gemm_run (path, tile, split-K, grid,
+ * waves, tail fraction, kernels launched).  GEMM_ERR_INVALID_ARG on NULL. */
+gemm_status_t gemm_plan_last_config(gemm_plan_t plan, gemm_config_info_t* out);
+
+/* Wait for `stream`, then read and clear the plan's watchdog word: returns
+ * GEMM_ERR_TIMEOUT if any kernel of this plan gave up on a bounded wait since
+ * the last poll, GEMM_OK otherwise, GEMM_ERR_CUDA if the stream failed. */
+gemm_status_t gemm_plan_poll_error(gemm_plan_t plan, void* stream);
+
+/* Limit, in nanoseconds, of every bounded wait inside this plan's kernels
+ * (default 2e9; the environment variable GEMM_WATCHDOG_NS overrides the
+ * default at plan creation).  Values < 1000 are rejected. */
+gemm_status_t gemm_plan_set_watchdog(gemm_plan_t plan, uint64_t timeout_ns);
+
+/* Watchdog self-test: launch one CTA that waits on a barrier nothing will
+ * ever arrive on, with this plan's limit, then wait for `stream`.  Returns
+ * GEMM_ERR_TIMEOUT when the wait ran out and the kernel returned on its own
+ * (the expected result; the context stays usable), GEMM_OK if it did not. */
+gemm_status_t gemm_plan_selftest_watchdog(gemm_plan_t plan, void* stream);
+
+/* The argument checks of gemm_run without a plan or a device: returns the
+ * status gemm_run would return before launching anything. */
+gemm_status_t gemm_check_args(int64_t M, int64_t N, int64_t K,
+                              const void* A, int64_t lda, const void* B, int64_t ldb,
+                              const void* C, int64_t ldc, float alpha,
+                              gemm_dtype_t dtype, gemm_op_t transA, gemm_op_t transB,
+                              gemm_epilogue_t epilogue);
+
+/* The planner of gemm_run as a pure host function: the decisions it would
+ * make for this problem on a GPU with `sms` multiprocessors.  Does not need a
+ * device.  Honours the GEMM_FORCE_TILE / GEMM_FORCE_SPLITK overrides. */
+gemm_status_t gemm_choose_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
+                                 gemm_op_t transA, gemm_op_t transB, int32_t sms,
+                                 gemm_config_info_t* out);
+
+/* Tile and wave quantization of an M x N output cut into tile_m x tile_n
+ * tiles, each split into `splitk` K slices, on `sms` multiprocessors running
+ * `ctas_per_sm` tiles at a time ("Matrix Multiplication Background User's
+ * Guide", sections 3.1 and 3.2).  Fills tiles, units, waves, tail_fraction,
+ * useful_fraction, tile_m, tile_n, splitk and sms.  Pure host arithmetic. */
+gemm_status_t gemm_quantization(int64_t M, int64_t N, int32_t tile_m, int32_t tile_n,
+                                int32_t splitk, int32_t sms, int32_t ctas_per_sm,
+                                gemm_config_info_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DGEMM_GB300_GEMM_H */

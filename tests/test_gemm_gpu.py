@@ -1,0 +1,199 @@
+"""GPU parity tests: the CUDA path through the C ABI against the CPU oracle.
+
+Small and medium shapes are compared in full; the full-size workloads of the
+benchmark configurations are compared on 4096 sampled outputs (corners, last
+row and column, tile boundaries and random entries) recomputed one by one by
+the oracle.  Tolerance: see tests/gemm_case.py.
+"""
+import os
+
+import numpy as np
+import pytest
+
+from tests.gemm_case import run_case
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def plan():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    from dense_gemm_mma_gb300 import gemm
+    p = gemm.Plan(0)
+    yield p
+    p.close()
+
+
+# ------------------------------------------------------------------ basics
+
+def test_watchdog_selftest_returns_and_context_survives(plan):
+    from dense_gemm_mma_gb300 import gemm
+    assert gemm.gemm_plan_set_watchdog(plan.handle, 50_000_000) == gemm.GEMM_OK
+    assert gemm.gemm_plan_selftest_watchdog(plan.handle, None) == gemm.GEMM_ERR_TIMEOUT
+    assert gemm.gemm_plan_set_watchdog(plan.handle, 2_000_000_000) == gemm.GEMM_OK
+    assert plan.poll_error() == gemm.GEMM_OK        # cleared by the self-test's poll
+    run_case(plan, 128, 64, 64, env={"GEMM_FORCE_TILE": "128x64"})
+
+
+@pytest.mark.parametrize("bn", [64, 128, 256])
+def test_single_tile_single_kblock(plan, bn):
+    r = run_case(plan, 128, bn, 64, env={"GEMM_FORCE_TILE": f"128x{bn}"})
+    assert r.info["path"] == "tc" and r.info["tile_n"] == bn and r.info["tiles"] == 1
+
+
+def test_config1_512_cubed(plan):
+    r = run_case(plan, 512, 512, 512, seed=1234)
+    assert r.info["path"] == "tc"
+
+
+@pytest.mark.parametrize("bn", [64, 128, 256])
+@pytest.mark.parametrize("shape", [(300, 520, 200), (129, 257, 1000), (640, 384, 77)])
+def test_tile_widths_ragged(plan, bn, shape):
+    r = run_case(plan, *shape, env={"GEMM_FORCE_TILE": f"128x{bn}"}, seed=sum(shape) + bn)
+    assert r.info["tile_n"] == bn
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+@pytest.mark.parametrize("ta", [False, True])
+@pytest.mark.parametrize("tb", [False, True])
+def test_transpose_flags(plan, fmt, ta, tb):
+    run_case(plan, 200, 300, 136, in_fmt=fmt, ta=ta, tb=tb, seed=5 + 2 * ta + tb)
+
+
+@pytest.mark.parametrize("in_fmt,out_fmt", [("bf16", "bf16"), ("f16", "f16"), ("f16", "f32"),
+                                            ("bf16", "f32")])
+def test_dtypes(plan, in_fmt, out_fmt):
+    run_case(plan, 257, 200, 513, in_fmt=in_fmt, out_fmt=out_fmt, seed=17)
+
+
+@pytest.mark.parametrize("out_fmt", ["f32", "bf16", "f16"])
+def test_beta_alpha_leaky_relu(plan, out_fmt):
+    in_fmt = "f16" if out_fmt == "f16" else "bf16"
+    run_case(plan, 260, 390, 300, in_fmt=in_fmt, out_fmt=out_fmt, alpha=1.0, beta=0.5, act=1,
+             slope=0.01, seed=31)
+    run_case(plan, 130, 200, 96, in_fmt=in_fmt, out_fmt=out_fmt, alpha=-2.5, beta=-1.0, seed=32)
+    run_case(plan, 130, 200, 96, in_fmt=in_fmt, out_fmt=out_fmt, alpha=0.75, act=1, slope=0.2,
+             seed=33, ta=True)
+
+
+def test_alpha_zero_and_k_zero_scale_c(plan):
+    r = run_case(plan, 100, 70, 50, alpha=0.0, beta=0.5, act=1, slope=0.25, seed=41)
+    assert r.info["path"] == "scale"
+    r = run_case(plan, 100, 70, 0, beta=2.0, seed=42)
+    assert r.info["path"] == "scale"
+    r = run_case(plan, 100, 70, 0, beta=0.0, seed=43)            # C <- 0 without reading C
+    assert r.info["path"] == "scale"
+
+
+@pytest.mark.parametrize("ta,tb", [(False, False), (True, True)])
+def test_leading_dimension_padding(plan, ta, tb):
+    run_case(plan, 200, 136, 264, ta=ta, tb=tb, pad=(8, 24, 4), seed=51)
+    run_case(plan, 200, 136, 264, out_fmt="bf16", ta=ta, tb=tb, pad=(16, 8, 8), seed=52)
+
+
+EDGE = [1, 7, 8, 15, 16, 17, 127, 128, 129, 255, 257]
+
+
+@pytest.mark.parametrize("M", EDGE)
+def test_edge_shapes_m_by_n(plan, M):
+    for N in EDGE:
+        run_case(plan, M, N, 129, seed=1000 + M * 7 + N)
+
+
+def test_edge_shapes_k(plan):
+    for K in [1, 2, 7, 8, 15, 16, 17, 63, 64, 65, 127, 128, 129, 255, 257]:
+        run_case(plan, 129, 257, K, seed=2000 + K)
+        run_case(plan, 129, 257, K, ta=True, tb=True, seed=3000 + K)
+
+
+# -------------------------------------------------------------------- split-K
+
+@pytest.mark.parametrize("splits", [2, 3, 7])
+def test_splitk_forced_and_deterministic(plan, splits):
+    r = run_case(plan, 256, 256, 4096, env={"GEMM_FORCE_SPLITK": str(splits)}, repeat=2, seed=60)
+    assert r.info["path"] == "tc_splitk" and r.info["splitk"] == splits
+    assert np.array_equal(r.outputs[0].view(np.uint8), r.outputs[1].view(np.uint8))
+
+
+def test_splitk_ragged_with_beta(plan):
+    r = run_case(plan, 200, 150, 3000, out_fmt="bf16", beta=0.5, act=1, slope=0.1,
+                 env={"GEMM_FORCE_SPLITK": "5", "GEMM_FORCE_TILE": "128x64"}, seed=61)
+    assert r.info["splitk"] == 5
+
+
+# ----------------------------------------------------------------------- GEMV
+
+@pytest.mark.parametrize("tb", [False, True])
+def test_gemv_m1_config(plan, tb):
+    r = run_case(plan, 1, 8192, 8192, tb=tb, seed=1235)
+    assert r.info["path"] == ("gemv_rowdot" if tb else "gemv_colstream")
+
+
+@pytest.mark.parametrize("ta", [False, True])
+def test_gemv_n1(plan, ta):
+    r = run_case(plan, 8192, 1, 4096, ta=ta, seed=71)
+    assert r.info["path"] == ("gemv_colstream" if ta else "gemv_rowdot")
+
+
+@pytest.mark.parametrize("shape", [(1, 1000, 777), (1000, 1, 777), (1, 1, 333), (1, 13, 5),
+                                   (9, 1, 70000)])
+@pytest.mark.parametrize("ta,tb", [(False, False), (True, True), (False, True)])
+def test_gemv_odd_shapes(plan, shape, ta, tb):
+    run_case(plan, *shape, ta=ta, tb=tb, seed=sum(shape) + ta)
+
+
+def test_gemv_epilogue_and_dtypes(plan):
+    run_case(plan, 1, 3000, 1000, in_fmt="f16", out_fmt="f16", beta=0.5, act=1, slope=0.01, seed=81)
+    run_case(plan, 3000, 1, 1000, out_fmt="bf16", alpha=2.0, beta=-1.0, seed=82)
+    run_case(plan, 1, 3000, 1000, tb=True, out_fmt="f32", alpha=0.5, beta=1.0, act=1, slope=0.3,
+             seed=83)
+
+
+def test_gemv_misaligned_pointers_take_generic_path(plan):
+    r = run_case(plan, 1, 500, 300, tb=True, offsets=(1, 1, 1), seed=91)
+    assert r.info["path"] == "gemv_generic"
+    r = run_case(plan, 500, 1, 300, offsets=(1, 3, 1), seed=92)
+    assert r.info["path"] == "gemv_generic"
+
+
+def test_gemv_deterministic(plan):
+    r = run_case(plan, 1, 8192, 8192, repeat=3, seed=93, check=False)
+    assert all(np.array_equal(r.outputs[0], o) for o in r.outputs[1:])
+
+
+# ------------------------------------------------------- full-size workloads
+
+SAMPLE = 4096
+
+
+def test_full_config2_skinny_both_b_layouts(plan):
+    for tb in (False, True):
+        run_case(plan, 8192, 128, 8192, tb=tb, seed=1235, sample=SAMPLE)
+
+
+def test_full_config3_square_bf16_out(plan):
+    r = run_case(plan, 8192, 8192, 8192, out_fmt="bf16", seed=1236, sample=SAMPLE)
+    assert r.info["path"] == "tc"
+
+
+def test_full_config3_beta_leaky_relu(plan):
+    run_case(plan, 8192, 8192, 8192, out_fmt="f32", beta=0.5, act=1, slope=0.01, seed=1236,
+             sample=SAMPLE)
+
+
+def test_full_config4_tile_sweep_points(plan):
+    run_case(plan, 6912, 2048, 4096, seed=1237, sample=SAMPLE)
+    for n in (128, 136, 200, 256):
+        run_case(plan, 27648, n, 4096, seed=1237, sample=SAMPLE)
+
+
+def test_full_config5_wave_sweep_points_and_splitk(plan):
+    for n in (1024, 1536, 1544, 3080, 6400):
+        run_case(plan, 2304, n, 4096, in_fmt="f16", seed=1238, sample=SAMPLE)
+    r = run_case(plan, 256, 256, 65536, in_fmt="f16", seed=1238, sample=SAMPLE, repeat=2)
+    assert r.info["path"] == "tc_splitk"
+    assert np.array_equal(r.outputs[0].view(np.uint8), r.outputs[1].view(np.uint8))

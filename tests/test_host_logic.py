@@ -1,0 +1,232 @@
+"""CPU tests of the product's host logic: the C ABI loads and exports what
+include/gemm.h declares, argument checks, the tile/wave quantization
+arithmetic against the figures printed in "Matrix Multiplication Background
+User's Guide" sections 2 and 3, the planner's invariants, and the FLOP/byte
+accounting of the benchmark."""
+import json
+import os
+import re
+
+import pytest
+
+from dense_gemm_mma_gb300 import gemm as g
+from dense_gemm_mma_gb300 import roofline as rl
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FIG = json.load(open(os.path.join(ROOT, "tests", "golden", "guide_figures.json")))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built_library():
+    import __graft_entry__
+    __graft_entry__.build_library()
+    g.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "gemm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gemm_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol():
+    import ctypes
+    lib = g.load()
+    names = declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(g.exported_symbols()) == names
+    # nothing else is exported under the gemm_ prefix
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", g.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = sorted(set(re.findall(r" T (gemm_\w+)", out)))
+    assert exported == names
+    assert isinstance(ctypes.sizeof(g.gemm_config_info_t), int)
+    assert ctypes.sizeof(g.gemm_config_info_t) == 96
+
+
+def test_status_strings():
+    for s in range(8):
+        assert g.gemm_status_string(s).startswith("GEMM_")
+    assert "unknown" in g.gemm_status_string(99)
+
+
+def test_no_device_without_gpu():
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("a GPU is present")
+    except ImportError:
+        pass
+    with pytest.raises(g.GemmError) as e:
+        g.gemm_plan_create(0)
+    assert e.value.status == g.GEMM_ERR_NO_DEVICE
+    assert g.load().gemm_run(None, 4, 4, 4, 16, 8, 16, 8, 16, 8, 1.0, 0.0, 0, 0, 0,
+                             g.gemm_epilogue_t(0, 0.0), None) == g.GEMM_ERR_INVALID_ARG
+    assert g.gemm_plan_destroy(None) == g.GEMM_OK
+
+
+# -------------------------------------------------------------- argument checks
+
+A16, B16, C16 = 0x10000, 0x20000, 0x30000   # fake, 16-byte aligned addresses (never dereferenced)
+
+
+def chk(M, N, K, A=A16, lda=None, B=B16, ldb=None, C=C16, ldc=None, alpha=1.0, dtype=0,
+        ta=0, tb=0, act=0):
+    lda = lda if lda is not None else max(1, (M if ta else K))
+    ldb = ldb if ldb is not None else max(1, (K if tb else N))
+    ldc = ldc if ldc is not None else max(1, N)
+    return g.gemm_check_args(M, N, K, A, lda, B, ldb, C, ldc, alpha, dtype, ta, tb, act)
+
+
+def test_check_args_accepts_good_calls():
+    assert chk(512, 512, 512) == g.GEMM_OK
+    assert chk(8192, 128, 8192, tb=1) == g.GEMM_OK
+    assert chk(24, 40, 16, ta=1, tb=1, dtype=3) == g.GEMM_OK
+
+
+def test_check_args_rejects():
+    E, AL, U = g.GEMM_ERR_INVALID_ARG, g.GEMM_ERR_ALIGNMENT, g.GEMM_ERR_UNSUPPORTED
+    assert chk(-1, 8, 8) == E
+    assert chk(8, -1, 8) == E
+    assert chk(8, 8, -1) == E
+    assert chk(8, 8, 8, dtype=4) == E
+    assert chk(8, 8, 8, ta=2) == E
+    assert chk(8, 8, 8, act=5) == E
+    assert chk(2 ** 31, 8, 8) == U
+    assert chk(8, 8, 16, lda=8) == E                 # lda < K
+    assert chk(8, 16, 8, ldb=8) == E                 # ldb < N
+    assert chk(8, 16, 8, ldc=8) == E                 # ldc < N
+    assert chk(16, 8, 8, ta=1, lda=8) == E           # transposed A: lda >= M
+    assert chk(8, 16, 8, tb=1, ldb=4) == E           # transposed B: ldb >= K
+    assert chk(8, 8, 8, C=0) == E
+    assert chk(8, 8, 8, A=0) == E
+    assert chk(8, 8, 8, B=0) == E
+    assert chk(8, 8, 8, A=A16 + 2) == AL             # tensor-core path: 16-byte pointers
+    assert chk(8, 8, 8, C=C16 + 8) == AL
+    assert chk(8, 8, 12, lda=12) == AL               # lda * 2 not a multiple of 16
+    assert chk(8, 12, 8, ldc=12, dtype=1) == AL      # bf16 C: ldc * 2
+    assert chk(8, 8, 8, A=A16 + 1) == AL             # not even element-aligned
+    assert chk(8, 8, 8, C=C16 + 2) == AL             # fp32 C needs 4-byte alignment
+
+
+def test_check_args_degenerate_and_gemv_relaxations():
+    assert chk(0, 8, 8, A=0, B=0, C=0) == g.GEMM_OK          # nothing to do
+    assert chk(8, 0, 8, A=0, B=0, C=0) == g.GEMM_OK
+    assert chk(8, 8, 0, A=0, B=0) == g.GEMM_OK               # C <- beta*C, A/B unused
+    assert chk(8, 8, 8, A=0, B=0, alpha=0.0) == g.GEMM_OK    # alpha == 0: A/B unused
+    # GEMV: vectors need only element alignment, strides are free
+    assert chk(1, 100, 7, A=A16 + 2, ldb=100) == g.GEMM_OK
+    assert chk(100, 1, 7, B=B16 + 2, ldb=1, lda=7, ldc=3, C=C16 + 4) == g.GEMM_OK
+
+
+# --------------------------------------------------- tile / wave quantization pins
+
+def test_wave_quantization_matches_guide_fig8():
+    w = FIG["wave_quantization"]
+    tm, tn = w["tile"]
+    for case in w["cases"]:
+        q = g.gemm_quantization(w["M"], case["N"], tm, tn, 1, w["sms"])
+        assert q.tiles == case["tiles"] == w["m_tiles"] * case["n_tiles"]
+        assert int(q.waves) == case["full_waves"]
+        tail = q.units % w["sms"]
+        assert tail == case["tail_tiles"]
+        if "tail_percent" in case:
+            assert round(100 * q.tail_fraction, 2) == case["tail_percent"]
+    for n in w["full_wave_N"]:
+        full = g.gemm_quantization(w["M"], n, tm, tn, 1, w["sms"])
+        after = g.gemm_quantization(w["M"], n + 8, tm, tn, 1, w["sms"])
+        assert full.tail_fraction == 0.0 and full.waves == int(full.waves)
+        assert after.tail_fraction > 0.0           # a new wave starts right after
+
+
+def test_tile_quantization_matches_guide_fig7_and_fig6():
+    t = FIG["tile_quantization"]
+    tm, tn = t["tile"]
+    for n in range(t["N_from"], t["N_to"] + 1, t["N_step"]):
+        q = g.gemm_quantization(t["M"], n, tm, tn, 1, 108)
+        assert q.tiles == (t["M"] // tm) * t["n_tiles"]
+    assert g.gemm_quantization(t["M"], 128, tm, tn, 1, 108).tiles == (t["M"] // tm) * t["n_tiles_at_128"]
+    q136 = g.gemm_quantization(t["M"], 136, tm, tn, 1, 108)
+    second_tile_useful = (136 - tn) / tn
+    assert round(100 * second_tile_useful, 2) == t["second_tile_useful_percent_at_136"]
+    assert q136.useful_fraction == pytest.approx(136 / 256)
+    f = FIG["fig6"]
+    best = g.gemm_quantization(*f["best"], *f["tile"], 1, 108)
+    worst = g.gemm_quantization(*f["worst"], *f["tile"], 1, 108)
+    assert best.tiles == f["tiles_best"] and worst.tiles == f["tiles_worst"]
+    assert worst.tiles / best.tiles == f["math_ratio"]
+    extra = (f["worst"][0] * f["worst"][1]) / (f["best"][0] * f["best"][1]) - 1
+    assert round(100 * extra, 2) == f["extra_useful_percent"]
+
+
+def test_arithmetic_intensity_matches_guide_section2():
+    a = FIG["arithmetic_intensity"]
+    for c in a["cases"]:
+        ai = rl.intensity(c["M"], c["N"], c["K"], c["fmt"], c["fmt"])
+        assert round(ai, c["decimals"]) == c["value"] or int(ai) == c["value"]
+        on_v100 = "math" if ai > a["v100_ops_per_byte"] else "memory"
+        assert on_v100 == c["bound_on_v100"]
+    # GEMV intensity stays below 1 FLOP/B
+    assert rl.intensity(1, 8192, 8192, "f16", "f16") < a["gemv_intensity_below"]
+    assert rl.intensity(8192, 1, 8192, "bf16", "f32") < a["gemv_intensity_below"]
+
+
+def test_tflops_formula_matches_t4_benchmark():
+    t = FIG["t4_benchmark"]
+    v = rl.tflops(rl.gemm_flops(t["M"], t["N"], t["K"]), t["median_latency_ms"] / 1e3)
+    assert abs(v - t["tflops"]) <= t["tflops_std"]
+    assert round(v, 2) == round(t["tflops"], 2)
+
+
+def test_roofline_bound():
+    assert rl.bound(rl.intensity(8192, 8192, 8192, "bf16", "bf16"), 2.25e15, 8e12) == "tensor"
+    assert rl.bound(rl.intensity(8192, 128, 8192, "bf16", "f32"), 2.25e15, 8e12) == "hbm"
+    assert rl.attainable(100.0, 2.25e15, 8e12) == 8e14
+
+
+# ----------------------------------------------------------------------- planner
+
+@pytest.mark.parametrize("M,N,K", [(512, 512, 512), (8192, 8192, 8192), (8192, 128, 8192),
+                                   (6912, 2048, 4096), (27648, 136, 4096), (2304, 1544, 4096),
+                                   (256, 256, 65536), (2, 2, 1), (129, 257, 10000)])
+def test_planner_invariants(M, N, K):
+    for sms in (108, 148, 152):
+        c = g.gemm_choose_config(M, N, K, g.GEMM_BF16_F32, 0, 0, sms)
+        assert c.path in (1, 2)
+        assert c.tile_m == 128 and c.tile_n in (64, 128, 256) and c.tile_k == 64
+        assert 1 <= c.grid <= sms and c.grid <= c.units
+        assert c.units == c.tiles * c.splitk
+        kb = -(-K // 64)
+        assert 1 <= c.splitk <= kb
+        per = -(-kb // c.splitk)
+        assert -(-kb // per) == c.splitk                  # no empty K slice
+        assert (c.path == 2) == (c.splitk > 1)
+        assert c.launches == (2 if c.splitk > 1 else 1)
+
+
+def test_planner_splits_small_output_with_long_k():
+    c = g.gemm_choose_config(256, 256, 65536, g.GEMM_F16_F32, 0, 0, 152)
+    assert c.splitk > 1 and c.units >= 64
+    big = g.gemm_choose_config(8192, 8192, 8192, g.GEMM_BF16_BF16, 0, 0, 152)
+    assert big.splitk == 1 and big.tile_n == 256
+
+
+def test_planner_gemv_paths():
+    assert g.PATH_NAMES[g.gemm_choose_config(1, 8192, 8192, 0, 0, 0, 152).path] == "gemv_colstream"
+    assert g.PATH_NAMES[g.gemm_choose_config(1, 8192, 8192, 0, 0, 1, 152).path] == "gemv_rowdot"
+    assert g.PATH_NAMES[g.gemm_choose_config(8192, 1, 8192, 0, 0, 0, 152).path] == "gemv_rowdot"
+    assert g.PATH_NAMES[g.gemm_choose_config(8192, 1, 8192, 0, 1, 0, 152).path] == "gemv_colstream"
+    assert g.PATH_NAMES[g.gemm_choose_config(0, 5, 5, 0, 0, 0, 152).path] == "none"
+    assert g.PATH_NAMES[g.gemm_choose_config(5, 5, 0, 0, 0, 0, 152).path] == "scale"
+
+
+def test_planner_env_overrides(monkeypatch):
+    monkeypatch.setenv("GEMM_FORCE_TILE", "128x128")
+    monkeypatch.setenv("GEMM_FORCE_SPLITK", "4")
+    c = g.gemm_choose_config(1024, 1024, 4096, 0, 0, 0, 152)
+    assert c.tile_n == 128 and c.splitk == 4
+    monkeypatch.setenv("GEMM_RASTER_GROUP", "3")
+    assert g.gemm_choose_config(1024, 1024, 4096, 0, 0, 0, 152).raster_group == 3
