@@ -21,8 +21,10 @@ struct gemm_plan {
   int device = 0;
   int sms = 0;
   int* err = nullptr;  // device word, OR of wait codes
-  void* ws = nullptr;  // workspace (split-K partials, GEMV partials + counters)
+  void* ws = nullptr;  // workspace (split-K partials, GEMV partials)
   size_t ws_bytes = 0;
+  unsigned* counters = nullptr;  // GEMV per-panel arrival counters: zero between calls
+  size_t counter_count = 0;
   uint64_t watchdog_ns = 2000000000ull;
   gemm_config_info_t last{};
 };
@@ -248,6 +250,24 @@ gemm_status_t ensure_ws(gemm_plan* plan, size_t bytes, cudaStream_t s) {
   return GEMM_OK;
 }
 
+// The counters are zeroed once when allocated; every kernel that uses one
+// leaves it at zero again.
+gemm_status_t ensure_counters(gemm_plan* plan, size_t count, cudaStream_t s) {
+  if (count <= plan->counter_count) return GEMM_OK;
+  size_t nc = std::max<size_t>(count, 4096);
+  if (plan->counters) cudaFreeAsync(plan->counters, s);
+  plan->counters = nullptr;
+  plan->counter_count = 0;
+  if (cudaMallocAsync(reinterpret_cast<void**>(&plan->counters), nc * sizeof(unsigned), s) != cudaSuccess) {
+    cudaGetLastError();
+    plan->counters = nullptr;
+    return GEMM_ERR_OUT_OF_MEMORY;
+  }
+  if (cudaMemsetAsync(plan->counters, 0, nc * sizeof(unsigned), s) != cudaSuccess) return GEMM_ERR_CUDA;
+  plan->counter_count = nc;
+  return GEMM_OK;
+}
+
 struct DeviceGuard {
   int prev = -1;
   explicit DeviceGuard(int dev) {
@@ -304,14 +324,15 @@ gemm_status_t run_gemv(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const v
   } else if (!row_major_w && (vec_ok || K == 1) && aligned(g.W, 16)) {
     const dg::ColstreamPlan cp = dg::plan_gemv_colstream(g.R, g.K, plan->sms);
     if (cp.ws_bytes > 0) {
-      const gemm_status_t st = ensure_ws(plan, size_t(cp.ws_bytes), s);
+      gemm_status_t st = ensure_ws(plan, size_t(cp.ws_bytes), s);
+      if (st == GEMM_OK) st = ensure_counters(plan, size_t(cp.panels), s);
       if (st != GEMM_OK) return st;
     }
     info->path = GEMM_PATH_GEMV_COLSTREAM;
     info->splitk = cp.ksplit;
     info->grid = cp.panels * cp.ksplit;
     info->workspace_bytes = cp.ws_bytes;
-    err = dg::launch_gemv_colstream(g, cp, plan->ws, s);
+    err = dg::launch_gemv_colstream(g, cp, plan->ws, plan->counters, s);
   } else {
     err = dg::launch_gemv_generic(g, s, plan->sms);
   }
@@ -355,13 +376,19 @@ gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const voi
   p.slope = epi.slope;
   p.err = plan->err;
   p.timeout_ns = plan->watchdog_ns;
+  p.c_ptr = C;
+  p.ldc = ldc;
   int64_t ws_ld = 0, ws_slice = 0;
   if (S == 1) {
     p.out_kind = out_kind(dtype);
+    // TMA stores write whole 16-byte pieces of a row: the map covers only the
+    // 16-byte-aligned prefix of each row of C; the kernel writes the rest.
+    p.n_tma = int((N * c_es) / 16 * 16 / c_es);
     const CUtensorMapDataType ct = out_is_f32(dtype) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : in_t;
-    ok = ok && make_map(&mc, ct, c_es, C, N, M, ldc, 128 / c_es, 32);
+    ok = ok && make_map(&mc, ct, c_es, C, std::max<int64_t>(p.n_tma, 1), M, ldc, 128 / c_es, 32);
   } else {
     p.out_kind = dg::OUT_PARTIAL;
+    p.n_tma = int(N);  // the workspace rows are padded to 16 bytes: no tail
     ws_ld = (N + 3) & ~int64_t(3);
     ws_slice = int64_t(p.ws_rows) * ws_ld;
     const size_t bytes = size_t(S) * size_t(ws_slice) * 4;
@@ -441,6 +468,7 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
   DeviceGuard guard(plan->device);
   cudaDeviceSynchronize();
   if (plan->ws) cudaFree(plan->ws);
+  if (plan->counters) cudaFree(plan->counters);
   if (plan->err) cudaFree(plan->err);
   delete plan;
   return GEMM_OK;

@@ -290,9 +290,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const uint32_t stg = stg0 + sbuf * Cfg::STG_BYTES;
         uint8_t* const stg_p = stg_p0 + sbuf * Cfg::STG_BYTES;
         const int x0 = n0 + c * cw;
+        // A TMA store writes whole 16-byte pieces of a row, so columns past the
+        // last 16-byte boundary inside C, [n_tma, N), are written by the threads.
+        const bool tma_cols = x0 < p.n_tma;
+        const int tail_lo = max(x0, p.n_tma), tail_hi = min(x0 + cw, p.N);
+        const int row = y0 + lane;
+        const bool has_tail = !partial && tail_lo < tail_hi && row < p.M;
         if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
         __syncwarp();
-        if (has_beta) {
+        if (has_beta && tma_cols) {
           if (lane == 0) {
             mbar_arrive_expect_tx(cload0 + 8 * e, Cfg::STG_BYTES);
             tma_load_2d(stg, &tmC, cload0 + 8 * e, x0, y0);
@@ -306,6 +312,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         __syncwarp();
         uint8_t* const row_p = stg_p + lane * 128;
         const int sw = lane & 7;  // 128-byte swizzle: 16-byte chunk j lives at j ^ (row % 8)
+        if (has_beta && has_tail) {
+          for (int col = tail_lo; col < tail_hi; ++col) {
+            const int b = (col - x0) * esize;
+            uint8_t* dst = row_p + ((((b >> 4) ^ sw)) << 4) + (b & 15);
+            const uint8_t* src = static_cast<const uint8_t*>(p.c_ptr) + (int64_t(row) * p.ldc + col) * esize;
+            if (esize == 4)
+              *reinterpret_cast<float*>(dst) = *reinterpret_cast<const float*>(src);
+            else
+              *reinterpret_cast<uint16_t*>(dst) = *reinterpret_cast<const uint16_t*>(src);
+          }
+        }
         if (esize == 4) {
           uint32_t r[32];
           tmem_ld_32x32b_x32(t_row + c * 32, r);
@@ -351,11 +368,22 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             *dst = make_uint4(o[0], o[1], o[2], o[3]);
           }
         }
+        if (has_tail) {
+          for (int col = tail_lo; col < tail_hi; ++col) {
+            const int b = (col - x0) * esize;
+            const uint8_t* src = row_p + ((((b >> 4) ^ sw)) << 4) + (b & 15);
+            uint8_t* dst = static_cast<uint8_t*>(p.c_ptr) + (int64_t(row) * p.ldc + col) * esize;
+            if (esize == 4)
+              *reinterpret_cast<float*>(dst) = *reinterpret_cast<const float*>(src);
+            else
+              *reinterpret_cast<uint16_t*>(dst) = *reinterpret_cast<const uint16_t*>(src);
+          }
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&tmC, stg, x0, y0);
-          bulk_commit();
+          if (tma_cols) tma_store_2d(&tmC, stg, x0, y0);
+          bulk_commit();  // one group per chunk (possibly empty) keeps the buffer accounting exact
         }
         sbuf ^= 1;
       }

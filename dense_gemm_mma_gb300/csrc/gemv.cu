@@ -141,8 +141,8 @@ __global__ void __launch_bounds__(kRowdotThreads)
 // row) and every 4th row of the slice.  The groups are summed in shared
 // memory in a fixed order.  With ksplit > 1 each CTA writes its 512 partial
 // sums to the workspace; the CTA that finishes a panel last (per-panel
-// counter) sums the slices in order z = 0, 1, ... and applies the epilogue,
-// then resets the counter for the next call.
+// arrival counter, zero on entry) sums the slices in order z = 0, 1, ... and
+// applies the epilogue, then sets the counter back to zero for the next call.
 template <bool F16>
 __global__ void __launch_bounds__(kColThreads)
     gemv_colstream_kernel(const GemvArgs g, const ColstreamPlan cp, float* ws, unsigned* counters) {
@@ -356,19 +356,13 @@ ColstreamPlan plan_gemv_colstream(int R, int K, int sms) {
   cp.kc = (K + ksplit - 1) / ksplit;
   cp.ksplit = (K + cp.kc - 1) / cp.kc;
   if (cp.ksplit < 1) cp.ksplit = 1;
-  cp.ws_bytes = cp.ksplit > 1
-                    ? static_cast<int64_t>(cp.ksplit) * cp.panels * kColCols * 4 + cp.panels * 4
-                    : 0;
+  cp.ws_bytes = cp.ksplit > 1 ? static_cast<int64_t>(cp.ksplit) * cp.panels * kColCols * 4 : 0;
   return cp;
 }
 
 cudaError_t launch_gemv_colstream(const GemvArgs& g, const ColstreamPlan& cp, void* ws,
-                                  cudaStream_t s) {
+                                  unsigned* counters, cudaStream_t s) {
   float* part = static_cast<float*>(ws);
-  unsigned* counters =
-      cp.ksplit > 1
-          ? reinterpret_cast<unsigned*>(part + static_cast<int64_t>(cp.ksplit) * cp.panels * kColCols)
-          : nullptr;
   const dim3 grid(cp.panels, cp.ksplit);
   if (g.in_f16)
     gemv_colstream_kernel<true><<<grid, kColThreads, 0, s>>>(g, cp, part, counters);

@@ -42,6 +42,9 @@ struct TcParams {
   int units;         // num_m_blocks * num_n_blocks * splitk
   int ws_rows;       // workspace rows per slice (num_m_blocks * TC_BM), OUT_PARTIAL only
   int out_kind;      // OutKind
+  int n_tma;         // columns [0, n_tma) of C go through TMA (a 16-byte multiple per row)
+  void* c_ptr;       // C, for the columns [n_tma, N) written directly
+  int64_t ldc;
   int a_mn_major;    // A stored K x M (M contiguous)
   int b_mn_major;    // B stored K x N (N contiguous)
   uint32_t idesc;    // tcgen05 instruction descriptor
@@ -98,11 +101,12 @@ struct ColstreamPlan {
   int panels;  // ceil(R / 512)
   int ksplit;
   int kc;
-  int64_t ws_bytes;  // partials + per-panel counters (0 when ksplit == 1)
+  int64_t ws_bytes;  // fp32 partials, ksplit x panels x 512 (0 when ksplit == 1)
 };
 ColstreamPlan plan_gemv_colstream(int R, int K, int sms);
+// counters: `panels` words that are zero on entry and are left zero on exit.
 cudaError_t launch_gemv_colstream(const GemvArgs& g, const ColstreamPlan& cp, void* ws,
-                                  cudaStream_t s);
+                                  unsigned* counters, cudaStream_t s);
 
 cudaError_t launch_gemv_generic(const GemvArgs& g, cudaStream_t s, int sms);
 

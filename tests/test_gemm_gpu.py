@@ -110,6 +110,18 @@ def test_edge_shapes_k(plan):
         run_case(plan, 129, 257, K, ta=True, tb=True, seed=3000 + K)
 
 
+@pytest.mark.parametrize("out_fmt", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("N", [2, 3, 9, 257, 258, 263])
+def test_unaligned_row_tail_of_c(plan, out_fmt, N):
+    """Rows of C whose byte length is not a multiple of 16: the last partial
+    16-byte piece is written by the kernel's threads, never by a TMA store, so
+    the ld padding next to it keeps its sentinel."""
+    in_fmt = "f16" if out_fmt == "f16" else "bf16"
+    run_case(plan, 130, N, 200, in_fmt=in_fmt, out_fmt=out_fmt, seed=N, pad=(0, 0, 8))
+    run_case(plan, 130, N, 200, in_fmt=in_fmt, out_fmt=out_fmt, beta=0.5, act=1, slope=0.1,
+             seed=N + 1, pad=(0, 0, 8))
+
+
 # -------------------------------------------------------------------- split-K
 
 @pytest.mark.parametrize("splits", [2, 3, 7])
