@@ -80,6 +80,8 @@ _SIGNATURES = {
                                   ctypes.POINTER(gemm_config_info_t)]),
     "gemm_quantization": (_I32, [_I64, _I64, _I32, _I32, _I32, _I32, _I32,
                                  ctypes.POINTER(gemm_config_info_t)]),
+    "gemm_gemv_noalloc": (_I32, [_I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64, _F, _F,
+                                 _I32, _I32, _I32, gemm_epilogue_t, _VP]),
 }
 
 
@@ -169,6 +171,12 @@ def gemm_quantization(M, N, tile_m, tile_n, splitk, sms, ctas_per_sm=1) -> gemm_
     if st != GEMM_OK:
         raise GemmError(st, "gemm_quantization")
     return info
+
+
+def gemm_gemv_noalloc(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype, transA, transB,
+                      act=GEMM_ACT_NONE, slope=0.0, stream=None) -> int:
+    return load().gemm_gemv_noalloc(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype,
+                                    transA, transB, gemm_epilogue_t(act, slope), stream)
 
 
 # ------------------------------------------------------------------ torch helpers

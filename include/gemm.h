@@ -211,6 +211,36 @@ gemm_status_t gemm_quantization(int64_t M, int64_t N, int32_t tile_m, int32_t ti
                                 int32_t splitk, int32_t sms, int32_t ctas_per_sm,
                                 gemm_config_info_t* out);
 
+/* GEMV that allocates nothing.  The pages have no counterpart: this entry
+ * point exists for callers that may not call cudaMalloc where they run a
+ * GEMV -- a plugin inside a framework or inference server that owns all
+ * device memory through its own pool allocator, or a latency-critical loop
+ * that cannot take cudaMalloc's implicit device synchronisation -- and so
+ * cannot create a plan (gemm_plan_create allocates) or let one grow.
+ *
+ * Same arguments as gemm_run, without the plan; same results as gemm_run for
+ * the shapes it accepts: the column-stream GEMV, i.e. M == 1 with B stored
+ * K x N (transB = GEMM_OP_N) and N >= 2, or N == 1 with A stored K x M
+ * (transA = GEMM_OP_T); K >= 1, alpha != 0; the matrix operand 16-byte
+ * aligned with ld * 2 a multiple of 16 bytes.  Other shapes, and outputs
+ * longer than 2,097,152 elements (the fixed scratch), return
+ * GEMM_ERR_UNSUPPORTED before anything is launched; argument errors are
+ * those of gemm_run.
+ *
+ * Runs on the calling thread's current device; `stream` must belong to it.
+ * Its scratch is a fixed 4 MiB device array of the library, held by every
+ * GPU that loads the library until the process exits; the call zeroes the
+ * part that must start at zero.  The first call on a device looks up that
+ * array's address (cudaGetSymbolAddress) and should come before any stream
+ * capture.  All calls on a device share the array: calls whose kernels may
+ * overlap on the GPU race and must be ordered by the caller (one stream, or
+ * events).  No cudaMalloc, cudaFree or other allocating call is made. */
+gemm_status_t gemm_gemv_noalloc(int64_t M, int64_t N, int64_t K,
+                                const void* A, int64_t lda, const void* B, int64_t ldb,
+                                void* C, int64_t ldc, float alpha, float beta,
+                                gemm_dtype_t dtype, gemm_op_t transA, gemm_op_t transB,
+                                gemm_epilogue_t epilogue, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
