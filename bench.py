@@ -13,8 +13,8 @@ on): one step is four calls of the C ABI, all memory-bound on GB300 --
 over its device time, in GB/s; per-call TFLOP/s and GB/s are in `parts`.
 
 Timing: inputs are resident in HBM; each call streams more than the 129 MB L2
-from buffers no other call of the step touches, and a 512 MiB write flushes
-L2 between steps (outside the timed events).  Every call is bracketed by
+from buffers no other call of the step touches, and a 512 MiB read flushes
+L2 between steps (outside the timed events) without leaving dirty lines.  Every call is bracketed by
 CUDA events on the stream it is launched on; the step time is the sum.
 `e2e` repeats the step through the same C ABI with the inputs copied from
 pinned host memory and the outputs copied back inside the timed region.
@@ -346,7 +346,13 @@ def main():
         if c.group:
             group_buf[c.group] = devbuf[c.name]
     gen_s = time.time() - t_gen
-    flush = torch.empty(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
+    # L2 flush: reading 512 MiB leaves L2 full of clean lines of this buffer,
+    # so no dirty data is written back inside a timed call.
+    flush = torch.zeros(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
+    flush_out = torch.zeros((), dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        torch.sum(flush, dim=0, out=flush_out)
 
     def launch(c, bufs, a_ptr=None, b_ptr=None, c_ptr=None):
         (ar, ac), (br, bc) = stored_shapes(c)
@@ -379,7 +385,7 @@ def main():
 
     # warm-up
     for _ in range(args.warmup):
-        flush.zero_()
+        flush_l2()
         one_step()
     torch.cuda.synchronize(dev)
     if plan.poll_error() != gemm.GEMM_OK:
@@ -396,7 +402,7 @@ def main():
     t_begin = time.time()
     gpu_launches = 0
     for s in range(args.steps):
-        flush.zero_()
+        flush_l2()
         # beta != 0 calls update C in place: restore it outside the timed events
         for c in calls:
             if devbuf[c.name]["C0"] is not None:
@@ -479,7 +485,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": calls[0].in_fmt, "data": "synthetic",
             "config": {"workload": wl_name, "calls": [c.desc() for c in calls],
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                       "l2": "flushed between steps (512 MiB write, untimed); each call reads "
+                       "l2": "flushed between steps (512 MiB read, untimed); each call reads "
                              "device buffers no other call of the step touches"
                              + ("" if not any(c.group for c in calls) else
                                 " (except the calls of one sweep, which share A and B)"),

@@ -12,6 +12,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstdlib>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -24,6 +26,7 @@ constexpr int kRowdotMaxK = 32768;  // x staged in shared memory: 64 KB of 16-bi
 constexpr int kColThreads = 256;
 constexpr int kColGroups = 4;             // K-interleaved thread groups per CTA
 constexpr int kColCols = 8 * (kColThreads / kColGroups);  // 512 columns per CTA
+constexpr int kColMaxKc = 2048;           // rows of x staged in shared memory at a time
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 r;
@@ -96,37 +99,51 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ------------------------------------------------------------------ rowdot
-// One warp per row of W (row-contiguous, 16-byte aligned rows); x staged in
-// shared memory; each lane reads 16 bytes per step, four steps in flight.
+// One warp per row of W (row-contiguous, 16-byte aligned rows).  Each lane
+// keeps kRowU 16-byte loads of its row in flight; x is read with 16-byte loads
+// through L1 when it is contiguous and aligned (kXDirect), else it is first
+// gathered into shared memory.
+constexpr int kRowU = 8;
+
 template <bool F16>
+__device__ __forceinline__ uint4 load_x_vec(const uint16_t* x, const uint16_t* xs, int v, bool direct) {
+  if (direct) return __ldg(reinterpret_cast<const uint4*>(x) + v);
+  return reinterpret_cast<const uint4*>(xs)[v];
+}
+
+template <bool F16, bool kXDirect>
 __global__ void __launch_bounds__(kRowdotThreads)
     gemv_rowdot_kernel(const GemvArgs g) {
   extern __shared__ __align__(16) uint16_t xs[];
   const uint16_t* x = static_cast<const uint16_t*>(g.x);
   const int K = g.K;
-  const int K8 = (K + 7) & ~7;
-  for (int k = threadIdx.x; k < K8; k += blockDim.x) xs[k] = k < K ? x[k * g.incx] : 0;
-  __syncthreads();
+  if (!kXDirect) {
+    const int K8 = (K + 7) & ~7;
+    for (int k = threadIdx.x; k < K8; k += blockDim.x) xs[k] = k < K ? x[k * g.incx] : 0;
+    __syncthreads();
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wpb = kRowdotThreads / 32;
   const int nvec = K >> 3;
-  const uint4* xv = reinterpret_cast<const uint4*>(xs);
   for (int r = blockIdx.x * wpb + warp; r < g.R; r += gridDim.x * wpb) {
     const uint16_t* wrow = static_cast<const uint16_t*>(g.W) + static_cast<int64_t>(r) * g.ldw;
     const uint4* wv = reinterpret_cast<const uint4*>(wrow);
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    float a0 = 0.f, a1 = 0.f;
     int v = lane;
-    for (; v + 96 < nvec; v += 128) {
-      const uint4 w0 = ldg_stream(wv + v), w1 = ldg_stream(wv + v + 32);
-      const uint4 w2 = ldg_stream(wv + v + 64), w3 = ldg_stream(wv + v + 96);
-      a0 = dot8<F16>(w0, xv[v], a0);
-      a1 = dot8<F16>(w1, xv[v + 32], a1);
-      a2 = dot8<F16>(w2, xv[v + 64], a2);
-      a3 = dot8<F16>(w3, xv[v + 96], a3);
+    for (; v + 32 * (kRowU - 1) < nvec; v += 32 * kRowU) {
+      uint4 w[kRowU];
+#pragma unroll
+      for (int u = 0; u < kRowU; ++u) w[u] = ldg_stream(wv + v + 32 * u);
+#pragma unroll
+      for (int u = 0; u < kRowU; u += 2) {
+        a0 = dot8<F16>(w[u], load_x_vec<F16>(x, xs, v + 32 * u, kXDirect), a0);
+        a1 = dot8<F16>(w[u + 1], load_x_vec<F16>(x, xs, v + 32 * (u + 1), kXDirect), a1);
+      }
     }
-    for (; v < nvec; v += 32) a0 = dot8<F16>(ldg_stream(wv + v), xv[v], a0);
-    for (int k = nvec * 8 + lane; k < K; k += 32) a1 = fmaf(to_f<F16>(wrow[k]), to_f<F16>(xs[k]), a1);
-    const float acc = warp_sum((a0 + a1) + (a2 + a3));
+    for (; v < nvec; v += 32) a0 = dot8<F16>(ldg_stream(wv + v), load_x_vec<F16>(x, xs, v, kXDirect), a0);
+    for (int k = nvec * 8 + lane; k < K; k += 32)
+      a1 = fmaf(to_f<F16>(wrow[k]), to_f<F16>(kXDirect ? x[k] : xs[k]), a1);
+    const float acc = warp_sum(a0 + a1);
     if (lane == 0) {
       const int64_t idx = static_cast<int64_t>(r) * g.inc_out;
       store_c(g.out, idx, epilogue(acc, g.out, idx, g.e), g.e.out_kind);
@@ -138,15 +155,30 @@ __global__ void __launch_bounds__(kRowdotThreads)
 // W is K x R with R contiguous.  CTA (panel, z) covers columns
 // [panel*512, panel*512+512) and K rows [z*kc, z*kc+kc); its 256 threads form
 // 4 groups of 64, each thread owning 8 adjacent columns (one 16-byte load per
-// row) and every 4th row of the slice.  The groups are summed in shared
-// memory in a fixed order.  With ksplit > 1 each CTA writes its 512 partial
-// sums to the workspace; the CTA that finishes a panel last (per-panel
-// arrival counter, zero on entry) sums the slices in order z = 0, 1, ... and
-// applies the epilogue, then sets the counter back to zero for the next call.
+// row, kColU rows in flight) and every 4th row of the slice; the slice of x is
+// staged in shared memory as fp32.  The groups are summed in shared memory in
+// a fixed order.  With ksplit > 1 each CTA writes its 512 partial sums to the
+// workspace; the CTA that finishes a panel last (per-panel arrival counter,
+// zero on entry) sums the slices -- two fixed halves in slice order, then the
+// halves -- applies the epilogue and sets the counter back to zero.
+constexpr int kColU = 8;
+
+template <bool F16>
+__device__ __forceinline__ void fma_row(float (&acc)[8], uint4 wv, float xf) {
+  const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 f = to_f2<F16>(ww[q]);
+    acc[2 * q] = fmaf(f.x, xf, acc[2 * q]);
+    acc[2 * q + 1] = fmaf(f.y, xf, acc[2 * q + 1]);
+  }
+}
+
 template <bool F16>
 __global__ void __launch_bounds__(kColThreads)
     gemv_colstream_kernel(const GemvArgs g, const ColstreamPlan cp, float* ws, unsigned* counters) {
   __shared__ float red[kColGroups][kColCols];
+  __shared__ float xsl[kColMaxKc];
   __shared__ unsigned ticket;
   const int panel = blockIdx.x, z = blockIdx.y;
   const int t = threadIdx.x % (kColThreads / kColGroups);
@@ -159,45 +191,38 @@ __global__ void __launch_bounds__(kColThreads)
   float acc[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) acc[j] = 0.f;
-
-  if (col0 + 8 <= g.R) {
-    int k = kb + grp;
-    for (; k + 3 * kColGroups < ke; k += 4 * kColGroups) {
-      uint4 wv[4];
-      float xf[4];
+  // The slice is walked in chunks of kColMaxKc rows whose x values are staged
+  // in shared memory (chunk starts are multiples of 4 rows past kb, so row k
+  // stays with group (k - kb) % 4).
+  for (int cb = kb; cb < ke; cb += kColMaxKc) {
+    const int ce = min(ke, cb + kColMaxKc);
+    __syncthreads();  // the previous chunk's x is no longer read
+    for (int k = cb + threadIdx.x; k < ce; k += kColThreads)
+      xsl[k - cb] = to_f<F16>(x[static_cast<int64_t>(k) * g.incx]);
+    __syncthreads();
+    if (col0 + 8 <= g.R) {
+      const uint16_t* wp = W + static_cast<int64_t>(cb + grp) * g.ldw + col0;
+      const int64_t step = static_cast<int64_t>(kColGroups) * g.ldw;
+      int k = cb + grp;
+      for (; k + (kColU - 1) * kColGroups < ce; k += kColU * kColGroups) {
+        uint4 wv[kColU];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        wv[i] = ldg_stream(W + static_cast<int64_t>(k + i * kColGroups) * g.ldw + col0);
-        xf[i] = to_f<F16>(x[static_cast<int64_t>(k + i * kColGroups) * g.incx]);
+        for (int i = 0; i < kColU; ++i) wv[i] = ldg_stream(wp + i * step);
+#pragma unroll
+        for (int i = 0; i < kColU; ++i) fma_row<F16>(acc, wv[i], xsl[k - cb + i * kColGroups]);
+        wp += kColU * step;
       }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t ww[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 f = to_f2<F16>(ww[q]);
-          acc[2 * q] = fmaf(f.x, xf[i], acc[2 * q]);
-          acc[2 * q + 1] = fmaf(f.y, xf[i], acc[2 * q + 1]);
-        }
+      for (; k < ce; k += kColGroups) {
+        fma_row<F16>(acc, ldg_stream(wp), xsl[k - cb]);
+        wp += step;
       }
-    }
-    for (; k < ke; k += kColGroups) {
-      const uint4 wv = ldg_stream(W + static_cast<int64_t>(k) * g.ldw + col0);
-      const float xf = to_f<F16>(x[static_cast<int64_t>(k) * g.incx]);
-      const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float2 f = to_f2<F16>(ww[q]);
-        acc[2 * q] = fmaf(f.x, xf, acc[2 * q]);
-        acc[2 * q + 1] = fmaf(f.y, xf, acc[2 * q + 1]);
+    } else if (col0 < g.R) {
+      const int nc = g.R - col0;
+      for (int k = cb + grp; k < ce; k += kColGroups) {
+        const float xf = xsl[k - cb];
+        for (int j = 0; j < nc; ++j)
+          acc[j] = fmaf(to_f<F16>(W[static_cast<int64_t>(k) * g.ldw + col0 + j]), xf, acc[j]);
       }
-    }
-  } else if (col0 < g.R) {
-    const int nc = g.R - col0;
-    for (int k = kb + grp; k < ke; k += kColGroups) {
-      const float xf = to_f<F16>(x[static_cast<int64_t>(k) * g.incx]);
-      for (int j = 0; j < nc; ++j)
-        acc[j] = fmaf(to_f<F16>(W[static_cast<int64_t>(k) * g.ldw + col0 + j]), xf, acc[j]);
     }
   }
 #pragma unroll
@@ -227,11 +252,44 @@ __global__ void __launch_bounds__(kColThreads)
   __syncthreads();
   if (ticket != static_cast<unsigned>(cp.ksplit - 1)) return;
   __threadfence();
+  // Last CTA of the panel: thread (h, q) sums columns 4q..4q+3 over slice half h.
+  const int q = threadIdx.x % (kColCols / 4);
+  const int h = threadIdx.x / (kColCols / 4);  // 0 or 1
+  const int zmid = (cp.ksplit + 1) / 2;
+  const int z0 = h == 0 ? 0 : zmid, z1 = h == 0 ? zmid : cp.ksplit;
+  const float* src = ws + panel * kColCols + 4 * q;
+  float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  int zz = z0;
+  for (; zz + 7 < z1; zz += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __ldcg(reinterpret_cast<const float4*>(src + static_cast<int64_t>(zz + i) * rpad));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      s4.x += v[i].x;
+      s4.y += v[i].y;
+      s4.z += v[i].z;
+      s4.w += v[i].w;
+    }
+  }
+  for (; zz < z1; ++zz) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(src + static_cast<int64_t>(zz) * rpad));
+    s4.x += v.x;
+    s4.y += v.y;
+    s4.z += v.z;
+    s4.w += v.w;
+  }
+  float* half = &red[0][0];  // reuse: [2][512]
+  __syncthreads();
+  half[h * kColCols + 4 * q + 0] = s4.x;
+  half[h * kColCols + 4 * q + 1] = s4.y;
+  half[h * kColCols + 4 * q + 2] = s4.z;
+  half[h * kColCols + 4 * q + 3] = s4.w;
+  __syncthreads();
   for (int c = threadIdx.x; c < kColCols; c += kColThreads) {
     const int col = panel * kColCols + c;
     if (col >= g.R) break;
-    float s = 0.f;
-    for (int zz = 0; zz < cp.ksplit; ++zz) s += __ldcg(ws + static_cast<int64_t>(zz) * rpad + col);
+    const float s = half[c] + half[kColCols + c];
     const int64_t idx = static_cast<int64_t>(col) * g.inc_out;
     store_c(g.out, idx, epilogue(s, g.out, idx, g.e), g.e.out_kind);
   }
@@ -331,16 +389,17 @@ int grid_for(int64_t items, int per_block, int sms, int blocks_per_sm) {
 int gemv_rowdot_max_k() { return kRowdotMaxK; }
 
 cudaError_t launch_gemv_rowdot(const GemvArgs& g, cudaStream_t s, int sms) {
-  const int smem = ((g.K + 7) & ~7) * 2;
+  const bool direct = g.incx == 1 && (reinterpret_cast<uintptr_t>(g.x) & 15u) == 0;
+  const int smem = direct ? 0 : ((g.K + 7) & ~7) * 2;
   const int grid = grid_for(g.R, kRowdotThreads / 32, sms, 8);
+  auto go = [&](auto kern) {
+    if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    kern<<<grid, kRowdotThreads, smem, s>>>(g);
+  };
   if (g.in_f16) {
-    if (smem > 48 * 1024)
-      cudaFuncSetAttribute(gemv_rowdot_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    gemv_rowdot_kernel<true><<<grid, kRowdotThreads, smem, s>>>(g);
+    if (direct) go(gemv_rowdot_kernel<true, true>); else go(gemv_rowdot_kernel<true, false>);
   } else {
-    if (smem > 48 * 1024)
-      cudaFuncSetAttribute(gemv_rowdot_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    gemv_rowdot_kernel<false><<<grid, kRowdotThreads, smem, s>>>(g);
+    if (direct) go(gemv_rowdot_kernel<false, true>); else go(gemv_rowdot_kernel<false, false>);
   }
   return cudaGetLastError();
 }
@@ -348,10 +407,14 @@ cudaError_t launch_gemv_rowdot(const GemvArgs& g, cudaStream_t s, int sms) {
 ColstreamPlan plan_gemv_colstream(int R, int K, int sms) {
   ColstreamPlan cp;
   cp.panels = (R + kColCols - 1) / kColCols;
-  const int target = sms * 8;  // eight 256-thread CTAs per SM
+  const int target = sms * 4;  // four 256-thread CTAs per SM, each with 8 rows in flight per thread
   int ksplit = (target + cp.panels - 1) / cp.panels;
   const int max_split = (K + 63) / 64;  // at least 64 rows (16 per thread) per slice
   if (ksplit > max_split) ksplit = max_split;
+  if (const char* f = std::getenv("GEMM_FORCE_GEMV_SPLITK")) {  // tests and sweeps
+    const int v = std::atoi(f);
+    if (v > 0) ksplit = v < K ? v : K;
+  }
   if (ksplit < 1) ksplit = 1;
   cp.kc = (K + ksplit - 1) / ksplit;
   cp.ksplit = (K + cp.kc - 1) / cp.kc;

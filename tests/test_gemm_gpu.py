@@ -172,6 +172,13 @@ def test_gemv_misaligned_pointers_take_generic_path(plan):
     assert r.info["path"] == "gemv_generic"
 
 
+@pytest.mark.parametrize("splits", [1, 2, 3])
+def test_gemv_colstream_long_slices(plan, splits):
+    """Slices longer than the shared-memory x chunk (2048 rows) are walked in chunks."""
+    r = run_case(plan, 1, 1500, 5000, env={"GEMM_FORCE_GEMV_SPLITK": str(splits)}, seed=95 + splits)
+    assert r.info["path"] == "gemv_colstream" and r.info["splitk"] == splits
+
+
 def test_gemv_deterministic(plan):
     r = run_case(plan, 1, 8192, 8192, repeat=3, seed=93, check=False)
     assert all(np.array_equal(r.outputs[0], o) for o in r.outputs[1:])
