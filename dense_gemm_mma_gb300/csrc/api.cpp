@@ -106,10 +106,12 @@ void quantization(int64_t M, int64_t N, int tm, int tn, int splitk, int sms, int
 // streaming its unique bytes from HBM (section 2, math vs memory bound).
 struct Model {
   double peak_flops = 2.25e15;  // dense bf16, whole GPU
-  double hbm_bw = 7.0e12;       // B/s
-  double sm_bw = 2.0e11;        // B/s one SM can pull from L2
+  double stream_bw = 4.9e12;    // B/s: DRAM rate reachable by TMA box streams (measured)
+  double sm_stream_bw = 6.0e10; // B/s: DRAM stream rate of one SM's TMA ring (measured)
+  double sm_l2_bw = 2.0e11;     // B/s one SM can pull from L2
+  double hbm_bw = 6.8e12;       // B/s, copy bandwidth
   double unit_fixed = 1.0e-6;   // pipeline fill + epilogue tail per unit
-  double launch = 3.0e-6;       // one extra kernel
+  double launch = 1.5e-6;       // one extra (programmatic dependent) kernel
 };
 
 double tile_efficiency(int bn) { return bn >= 256 ? 1.0 : (bn >= 128 ? 0.92 : 0.70); }
@@ -122,19 +124,30 @@ double estimate(int64_t M, int64_t N, int64_t K, int bn, int splitk, int sms, in
   *splitk_eff = s_eff;
   const int64_t tiles = ceil_div(M, dg::TC_BM) * ceil_div(N, bn);
   const int64_t units = tiles * s_eff;
+  const int64_t active = std::min<int64_t>(units, sms);
+  const double waves = double(ceil_div(units, sms));
+  // tensor cores: the busiest SM runs ceil(units/SMs) units
   const double per_sm_flops = md.peak_flops / sms;
   const double t_mma = 2.0 * dg::TC_BM * bn * double(kbps * dg::TC_BK) / (per_sm_flops * tile_efficiency(bn));
-  const double t_load = double(dg::TC_BM + bn) * double(kbps * dg::TC_BK) * 2.0 / md.sm_bw;
-  const double t_unit = std::max(t_mma, t_load) + md.unit_fixed;
-  const double makespan = double(ceil_div(units, sms)) * t_unit;
+  // L2 -> SM feed of one unit (A and B blocks)
+  const double t_feed = double(dg::TC_BM + bn) * double(kbps * dg::TC_BK) * 2.0 / md.sm_l2_bw;
+  const double makespan = waves * (std::max(t_mma, t_feed) + md.unit_fixed);
+  // DRAM: unique bytes at the rate the active SMs' streams reach
   double bytes = double(M * K + K * N) * 2.0 + double(M) * N * c_es * (beta ? 2.0 : 1.0);
   double t = 0.0;
   if (s_eff > 1) {
     const double part = double(s_eff) * double(ceil_div(M, dg::TC_BM) * dg::TC_BM) * double(N) * 4.0;
-    bytes += part;                             // partials written
-    t += md.launch + part / md.hbm_bw;         // reduction kernel reads them back
+    bytes += part;                           // partials written
+    t += md.launch + part / md.hbm_bw;       // reduction reads them back
   }
-  return std::max(makespan, bytes / md.hbm_bw) + t;
+  // Concurrent units that share their streamed operand read it from DRAM once:
+  // the distinct streams are the active units divided by that sharing.
+  const bool a_streams = double(M) >= double(N);
+  const int64_t share = std::max<int64_t>(
+      1, std::min<int64_t>(a_streams ? ceil_div(N, bn) : ceil_div(M, dg::TC_BM), active));
+  const double streams = std::max(1.0, double(active) / double(share));
+  const double t_mem = bytes / std::min(md.stream_bw, md.sm_stream_bw * streams);
+  return std::max(makespan, t_mem) + t;
 }
 
 int env_int(const char* name, int dflt) {
@@ -159,6 +172,9 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
   const int bns[3] = {256, 128, 64};
   for (int bn : bns) {
     if (force_bn && bn != force_bn) continue;
+    // A tile at least half outside C wastes its loads and MMAs (tile
+    // quantization, "Matrix Multiplication Background User's Guide", 3.1).
+    if (!force_bn && bn > 64 && ceil_div(N, bn) * bn - N >= bn / 2) continue;
     for (int s = 1; s <= 64; ++s) {
       if (force_s > 0 && s != force_s) continue;
       if (s > kb) break;

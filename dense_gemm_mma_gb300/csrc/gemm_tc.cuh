@@ -163,6 +163,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // A dependent grid (the split-K reduction) may be scheduled now; it waits
+  // for this grid's completion before it reads anything.
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const Watch w{abort_flag, p.err, p.timeout_ns};
 
   if (warp == 0) {

@@ -325,6 +325,9 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvArgs g) {
 __global__ void __launch_bounds__(256)
     splitk_reduce_kernel(const float* __restrict__ ws, int64_t ws_ld, int64_t ws_slice, int splits,
                          int M, int N, void* C, int64_t ldc, const EpiParams e) {
+  // Launched as a programmatic dependent of the GEMM that writes the partials:
+  // this CTA may start before that grid ends, so wait for its results here.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int gpr = (N + 3) >> 2;
   const int64_t total = static_cast<int64_t>(M) * gpr;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
@@ -447,9 +450,19 @@ cudaError_t launch_splitk_reduce(const float* ws, int64_t ws_ld, int64_t ws_slic
                                  int M, int N, void* C, int64_t ldc, EpiParams e, cudaStream_t s,
                                  int sms) {
   const int64_t items = static_cast<int64_t>(M) * ((N + 3) / 4);
-  splitk_reduce_kernel<<<grid_for(items, 256, sms, 8), 256, 0, s>>>(ws, ws_ld, ws_slice, splits, M,
-                                                                    N, C, ldc, e);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the reduction's launch overlaps the tail of
+  // the GEMM; its griddepcontrol.wait orders it after the GEMM's writes.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid_for(items, 256, sms, 8));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, ws, ws_ld, ws_slice, splits, M, N, C, ldc, e);
 }
 
 cudaError_t launch_scale(int M, int N, void* C, int64_t ldc, EpiParams e, cudaStream_t s, int sms) {

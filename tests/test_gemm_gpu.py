@@ -47,7 +47,7 @@ def test_single_tile_single_kblock(plan, bn):
 
 def test_config1_512_cubed(plan):
     r = run_case(plan, 512, 512, 512, seed=1234)
-    assert r.info["path"] == "tc"
+    assert r.info["path"] in ("tc", "tc_splitk")
 
 
 @pytest.mark.parametrize("bn", [64, 128, 256])
