@@ -14,6 +14,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "kernels.h"
 
@@ -96,57 +97,80 @@ void quantization(int64_t M, int64_t N, int tm, int tn, int splitk, int sms, int
   o->useful_fraction = o->tiles ? double(M) * double(N) / (double(o->tiles) * tm * tn) : 0.0;
 }
 
-// Cost model of the tensor-core path (seconds; absolute scale only matters
-// relative to the other candidates).  Persistent CTAs take units round-robin,
+// Cost model of the tensor-core path (seconds), calibrated on GB300 against
+// measured times of every tile width and split for 24 shapes (worst pick
+// within 9% of the best measured).  Persistent CTAs take units round-robin,
 // so the busiest SM runs ceil(units/SMs) units ("Matrix Multiplication
 // Background User's Guide", section 3.2, wave quantization); every unit pays
 // for a full tile whatever part of it lies inside C (section 3.1, tile
-// quantization); a unit is bound by the tensor core or by the rate at which
-// one SM can pull its A and B blocks; the whole call is at least as long as
-// streaming its unique bytes from HBM (section 2, math vs memory bound).
+// quantization).  A unit is bound by its tensor-core time or by how fast one
+// SM's TMA ring is fed: ~80 GB/s when its blocks come from DRAM (a single
+// wave moves through K in lockstep, so every stage waits on DRAM), faster
+// when later waves find blocks that earlier waves left in L2.  The call is
+// also bound by streaming its unique bytes from DRAM at ~60 GB/s per distinct
+// A or B panel in flight (up to ~4.9 TB/s).  Split-K adds its partials and a
+// reduction launch.
 struct Model {
-  double peak_flops = 2.25e15;  // dense bf16, whole GPU
-  double stream_bw = 4.9e12;    // B/s: DRAM rate reachable by TMA box streams (measured)
-  double sm_stream_bw = 6.0e10; // B/s: DRAM stream rate of one SM's TMA ring (measured)
-  double sm_l2_bw = 2.0e11;     // B/s one SM can pull from L2
+  double peak_flops = 1.7e15;   // sustained dense bf16 rate the kernel reaches per GPU
+  double feed = 8.0e10;         // B/s one SM's ring receives from DRAM
+  double reuse_gain = 0.5;      // feed speed-up at full cross-wave L2 reuse
+  double stream_bw = 4.9e12;    // B/s DRAM rate reachable by TMA box streams
+  double panel_bw = 6.0e10;     // B/s of one streamed panel
   double hbm_bw = 6.8e12;       // B/s, copy bandwidth
-  double unit_fixed = 1.0e-6;   // pipeline fill + epilogue tail per unit
-  double launch = 1.5e-6;       // one extra (programmatic dependent) kernel
+  double fixed = 3.0e-6;        // launch, pipeline fill and last epilogue
+  double reduce = 6.0e-6;       // split-K reduction launch and tail
 };
 
-double tile_efficiency(int bn) { return bn >= 256 ? 1.0 : (bn >= 128 ? 0.92 : 0.70); }
+double tile_efficiency(int bn) { return bn >= 256 ? 1.0 : (bn >= 128 ? 0.85 : 0.5); }
+
+struct TileWalk {  // host copy of the kernel's unit order (gemm_tc.cuh: decode_unit)
+  int64_t mb, nb, group;
+  void unit(int64_t u, int64_t* m, int64_t* n, int64_t* split) const {
+    const int64_t tiles = mb * nb;
+    *split = u / tiles;
+    const int64_t t = u - *split * tiles;
+    const int64_t per = group * nb, g = t / per, first = g * group;
+    const int64_t rows = std::min(mb - first, group), r = t - g * per;
+    *m = first + r % rows;
+    *n = r / rows;
+  }
+};
 
 double estimate(int64_t M, int64_t N, int64_t K, int bn, int splitk, int sms, int c_es,
-                bool beta, const Model& md, int* splitk_eff) {
+                bool beta, int raster_group, const Model& md, int* splitk_eff) {
   const int64_t kb = ceil_div(K, dg::TC_BK);
   const int64_t kbps = ceil_div(kb, splitk);
   const int s_eff = int(ceil_div(kb, kbps));
   *splitk_eff = s_eff;
-  const int64_t tiles = ceil_div(M, dg::TC_BM) * ceil_div(N, bn);
-  const int64_t units = tiles * s_eff;
+  const TileWalk walk{ceil_div(M, dg::TC_BM), ceil_div(N, bn),
+                      std::max<int64_t>(1, std::min<int64_t>(raster_group, ceil_div(M, dg::TC_BM)))};
+  const int64_t units = walk.mb * walk.nb * s_eff;
   const int64_t active = std::min<int64_t>(units, sms);
   const double waves = double(ceil_div(units, sms));
-  // tensor cores: the busiest SM runs ceil(units/SMs) units
-  const double per_sm_flops = md.peak_flops / sms;
-  const double t_mma = 2.0 * dg::TC_BM * bn * double(kbps * dg::TC_BK) / (per_sm_flops * tile_efficiency(bn));
-  // L2 -> SM feed of one unit (A and B blocks)
-  const double t_feed = double(dg::TC_BM + bn) * double(kbps * dg::TC_BK) * 2.0 / md.sm_l2_bw;
-  const double makespan = waves * (std::max(t_mma, t_feed) + md.unit_fixed);
-  // DRAM: unique bytes at the rate the active SMs' streams reach
-  double bytes = double(M * K + K * N) * 2.0 + double(M) * N * c_es * (beta ? 2.0 : 1.0);
+  // distinct A and B panels the first wave streams
+  std::vector<char> seen_a(size_t(walk.mb * s_eff), 0), seen_b(size_t(walk.nb * s_eff), 0);
+  int64_t streams = 0;
+  for (int64_t u = 0; u < active; ++u) {
+    int64_t m, n, sp;
+    walk.unit(u, &m, &n, &sp);
+    if (!seen_a[size_t(sp * walk.mb + m)]) { seen_a[size_t(sp * walk.mb + m)] = 1; ++streams; }
+    if (!seen_b[size_t(sp * walk.nb + n)]) { seen_b[size_t(sp * walk.nb + n)] = 1; ++streams; }
+  }
+  const double t_mma = 2.0 * dg::TC_BM * bn * double(kbps * dg::TC_BK) /
+                       (md.peak_flops / sms * tile_efficiency(bn));
+  const double unit_bytes = double(dg::TC_BM + bn) * double(kbps * dg::TC_BK) * 2.0;
+  const double unique = double(M * K + K * N) * 2.0;
+  const double reuse = (1.0 - 1.0 / waves) * std::max(0.0, 1.0 - unique / (double(units) * unit_bytes));
+  const double feed = md.feed * (1.0 + md.reuse_gain * reuse);
+  const double makespan = waves * std::max(t_mma, unit_bytes / feed) + md.fixed;
+  double bytes = unique + double(M) * N * c_es * (beta ? 2.0 : 1.0);
   double t = 0.0;
   if (s_eff > 1) {
-    const double part = double(s_eff) * double(ceil_div(M, dg::TC_BM) * dg::TC_BM) * double(N) * 4.0;
+    const double part = double(s_eff) * double(walk.mb * dg::TC_BM) * double(N) * 4.0;
     bytes += part;                           // partials written
-    t += md.launch + part / md.hbm_bw;       // reduction reads them back
+    t += md.reduce + part / md.hbm_bw;       // and read back by the reduction
   }
-  // Concurrent units that share their streamed operand read it from DRAM once:
-  // the distinct streams are the active units divided by that sharing.
-  const bool a_streams = double(M) >= double(N);
-  const int64_t share = std::max<int64_t>(
-      1, std::min<int64_t>(a_streams ? ceil_div(N, bn) : ceil_div(M, dg::TC_BM), active));
-  const double streams = std::max(1.0, double(active) / double(share));
-  const double t_mem = bytes / std::min(md.stream_bw, md.sm_stream_bw * streams);
+  const double t_mem = bytes / std::min(md.stream_bw, md.panel_bw * double(streams));
   return std::max(makespan, t_mem) + t;
 }
 
@@ -168,18 +192,17 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
       force_bn = fn;
   }
   const int force_s = env_int("GEMM_FORCE_SPLITK", 0);
+  const int raster = env_int("GEMM_RASTER_GROUP", 16);
   const int64_t kb = ceil_div(K, dg::TC_BK);
   const int bns[3] = {256, 128, 64};
   for (int bn : bns) {
     if (force_bn && bn != force_bn) continue;
-    // A tile at least half outside C wastes its loads and MMAs (tile
-    // quantization, "Matrix Multiplication Background User's Guide", 3.1).
-    if (!force_bn && bn > 64 && ceil_div(N, bn) * bn - N >= bn / 2) continue;
     for (int s = 1; s <= 64; ++s) {
       if (force_s > 0 && s != force_s) continue;
       if (s > kb) break;
+      if (s > 1 && ceil_div(M, dg::TC_BM) * ceil_div(N, bn) * s > 4 * int64_t(sms)) break;
       int s_eff = 1;
-      const double t = estimate(M, N, K, bn, s, sms, c_es, beta, md, &s_eff);
+      const double t = estimate(M, N, K, bn, s, sms, c_es, beta, raster, md, &s_eff);
       if (s_eff != s) continue;
       // prefer wider tiles / fewer slices unless clearly faster (2%)
       if (t < best_t * 0.98) {
@@ -202,7 +225,7 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
   out->cta_per_tile = 1;
   out->stages = dg::tc_stages(best_bn);
   const int64_t mblocks = ceil_div(M, dg::TC_BM);
-  out->raster_group = int(std::max<int64_t>(1, std::min<int64_t>(env_int("GEMM_RASTER_GROUP", 16), mblocks)));
+  out->raster_group = int(std::max<int64_t>(1, std::min<int64_t>(raster, mblocks)));
   out->grid = int(std::min<int64_t>(out->units, sms));
 }
 

@@ -462,6 +462,8 @@ cudaError_t launch_splitk_reduce(const float* ws, int64_t ws_ld, int64_t ws_slic
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (const char* v = std::getenv("GEMM_PDL"))  // GEMM_PDL=0: ordinary launch, for comparison
+    if (v[0] == '0') cfg.numAttrs = 0;
   return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, ws, ws_ld, ws_slice, splits, M, N, C, ldc, e);
 }
 
