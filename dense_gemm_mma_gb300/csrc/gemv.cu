@@ -343,10 +343,49 @@ __global__ void __launch_bounds__(256)
       s.z += v.z;
       s.w += v.w;
     }
-    const float sv[4] = {s.x, s.y, s.z, s.w};
+    float sv[4] = {s.x, s.y, s.z, s.w};
     const int64_t base = static_cast<int64_t>(m) * ldc + n;
     const int nn = min(4, N - n);
-    for (int j = 0; j < nn; ++j) store_c(C, base + j, epilogue(sv[j], C, base + j, e), e.out_kind);
+    const int esz = e.out_kind == OUT_F32 ? 4 : 2;
+    const bool vec = nn == 4 && ((reinterpret_cast<uintptr_t>(C) + base * esz) & (4 * esz - 1)) == 0;
+    if (!vec) {
+      for (int j = 0; j < nn; ++j) store_c(C, base + j, epilogue(sv[j], C, base + j, e), e.out_kind);
+      continue;
+    }
+    // Four adjacent outputs with one 16-byte (fp32) or 8-byte (16-bit) access.
+    if (e.out_kind == OUT_F32) {
+      float4* cp = reinterpret_cast<float4*>(static_cast<float*>(C) + base);
+      float4 cv = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e.beta != 0.f) cv = *cp;
+      const float cin[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float v = e.alpha * sv[j];
+        if (e.beta != 0.f) v = fmaf(e.beta, cin[j], v);
+        if (e.act == 1 && v < 0.f) v *= e.slope;
+        sv[j] = v;
+      }
+      *cp = make_float4(sv[0], sv[1], sv[2], sv[3]);
+    } else {
+      uint2* cp = reinterpret_cast<uint2*>(static_cast<uint16_t*>(C) + base);
+      uint2 cv = make_uint2(0u, 0u);
+      if (e.beta != 0.f) cv = *cp;
+      const uint16_t cin[4] = {uint16_t(cv.x), uint16_t(cv.x >> 16), uint16_t(cv.y), uint16_t(cv.y >> 16)};
+      uint16_t o[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float v = e.alpha * sv[j];
+        if (e.beta != 0.f) {
+          const float c = e.out_kind == OUT_BF16 ? __bfloat162float(__ushort_as_bfloat16(cin[j]))
+                                                 : __half2float(__ushort_as_half(cin[j]));
+          v = fmaf(e.beta, c, v);
+        }
+        if (e.act == 1 && v < 0.f) v *= e.slope;
+        o[j] = e.out_kind == OUT_BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v))
+                                      : __half_as_ushort(__float2half_rn(v));
+      }
+      *cp = make_uint2(uint32_t(o[0]) | (uint32_t(o[1]) << 16), uint32_t(o[2]) | (uint32_t(o[3]) << 16));
+    }
   }
 }
 
