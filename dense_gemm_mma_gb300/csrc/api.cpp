@@ -98,8 +98,9 @@ void quantization(int64_t M, int64_t N, int tm, int tn, int splitk, int sms, int
 }
 
 // Cost model of the tensor-core path (seconds), calibrated on GB300 against
-// measured times of every tile width and split for 24 shapes (worst pick
-// within 9% of the best measured).  Persistent CTAs take units round-robin,
+// measured times of every tile shape (128 x {64,128,256} on one CTA, 256 x 256
+// on a CTA pair) and split for 24 shapes: 23 picks are the measured best, the
+// worst is within 9%.  Persistent CTAs take units round-robin,
 // so the busiest SM runs ceil(units/SMs) units ("Matrix Multiplication
 // Background User's Guide", section 3.2, wave quantization); every unit pays
 // for a full tile whatever part of it lies inside C (section 3.1, tile
@@ -115,13 +116,16 @@ struct Model {
   double feed = 8.0e10;         // B/s one SM's ring receives from DRAM
   double reuse_gain = 0.5;      // feed speed-up at full cross-wave L2 reuse
   double stream_bw = 4.9e12;    // B/s DRAM rate reachable by TMA box streams
-  double panel_bw = 6.0e10;     // B/s of one streamed panel
+  double panel_bw = 5.0e10;     // B/s of one streamed panel
   double hbm_bw = 6.8e12;       // B/s, copy bandwidth
   double fixed = 3.0e-6;        // launch, pipeline fill and last epilogue
   double reduce = 6.0e-6;       // split-K reduction launch and tail
 };
 
 double tile_efficiency(int bn) { return bn >= 256 ? 1.0 : (bn >= 128 ? 0.85 : 0.5); }
+
+// Extra fixed cost of a CTA-pair (cluster) launch, fitted on GB300.
+constexpr double kPairFixed = 8.0e-6;
 
 struct TileWalk {  // host copy of the kernel's unit order (gemm_tc.cuh: decode_unit)
   int64_t mb, nb, group;
@@ -136,17 +140,22 @@ struct TileWalk {  // host copy of the kernel's unit order (gemm_tc.cuh: decode_
   }
 };
 
-double estimate(int64_t M, int64_t N, int64_t K, int bn, int splitk, int sms, int c_es,
+double estimate(int64_t M, int64_t N, int64_t K, int bn, bool pair, int splitk, int sms, int c_es,
                 bool beta, int raster_group, const Model& md, int* splitk_eff) {
   const int64_t kb = ceil_div(K, dg::TC_BK);
   const int64_t kbps = ceil_div(kb, splitk);
   const int s_eff = int(ceil_div(kb, kbps));
   *splitk_eff = s_eff;
-  const TileWalk walk{ceil_div(M, dg::TC_BM), ceil_div(N, bn),
-                      std::max<int64_t>(1, std::min<int64_t>(raster_group, ceil_div(M, dg::TC_BM)))};
+  // A pair unit (256 x bn) runs on two SMs; each SM stages 128 rows of A and
+  // bn/2 columns of B per k-block and does the flops of a 128 x bn tile, so it
+  // needs a third less feed per flop than a one-CTA 128 x 256 tile.
+  const int tile_m = pair ? 2 * dg::TC_BM : dg::TC_BM;
+  const int slots = pair ? sms / 2 : sms;
+  const TileWalk walk{ceil_div(M, tile_m), ceil_div(N, bn),
+                      std::max<int64_t>(1, std::min<int64_t>(raster_group, ceil_div(M, tile_m)))};
   const int64_t units = walk.mb * walk.nb * s_eff;
-  const int64_t active = std::min<int64_t>(units, sms);
-  const double waves = double(ceil_div(units, sms));
+  const int64_t active = std::min<int64_t>(units, slots);
+  const double waves = double(ceil_div(units, slots));
   // distinct A and B panels the first wave streams
   std::vector<char> seen_a(size_t(walk.mb * s_eff), 0), seen_b(size_t(walk.nb * s_eff), 0);
   int64_t streams = 0;
@@ -156,13 +165,13 @@ double estimate(int64_t M, int64_t N, int64_t K, int bn, int splitk, int sms, in
     if (!seen_a[size_t(sp * walk.mb + m)]) { seen_a[size_t(sp * walk.mb + m)] = 1; ++streams; }
     if (!seen_b[size_t(sp * walk.nb + n)]) { seen_b[size_t(sp * walk.nb + n)] = 1; ++streams; }
   }
-  const double t_mma = 2.0 * dg::TC_BM * bn * double(kbps * dg::TC_BK) /
-                       (md.peak_flops / sms * tile_efficiency(bn));
-  const double unit_bytes = double(dg::TC_BM + bn) * double(kbps * dg::TC_BK) * 2.0;
+  const double t_mma = 2.0 * dg::TC_BM * bn * double(kbps * dg::TC_BK) / (md.peak_flops / sms * tile_efficiency(bn));
+  const double unit_bytes = double(dg::TC_BM + (pair ? bn / 2 : bn)) * double(kbps * dg::TC_BK) * 2.0;
   const double unique = double(M * K + K * N) * 2.0;
-  const double reuse = (1.0 - 1.0 / waves) * std::max(0.0, 1.0 - unique / (double(units) * unit_bytes));
+  const double reuse = (1.0 - 1.0 / waves) *
+                       std::max(0.0, 1.0 - unique / (double(units) * (pair ? 2 : 1) * unit_bytes));
   const double feed = md.feed * (1.0 + md.reuse_gain * reuse);
-  const double makespan = waves * std::max(t_mma, unit_bytes / feed) + md.fixed;
+  const double makespan = waves * std::max(t_mma, unit_bytes / feed) + md.fixed + (pair ? kPairFixed : 0.0);
   double bytes = unique + double(M) * N * c_es * (beta ? 2.0 : 1.0);
   double t = 0.0;
   if (s_eff > 1) {
@@ -170,6 +179,7 @@ double estimate(int64_t M, int64_t N, int64_t K, int bn, int splitk, int sms, in
     bytes += part;                           // partials written
     t += md.reduce + part / md.hbm_bw;       // and read back by the reduction
   }
+  if (pair) streams *= 2;  // each CTA of a pair streams its own half of A and of B
   const double t_mem = bytes / std::min(md.stream_bw, md.panel_bw * double(streams));
   return std::max(makespan, t_mem) + t;
 }
@@ -186,28 +196,41 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
   int best_bn = 256, best_s = 1;
   double best_t = 1e300;
   int force_bn = 0;
+  bool force_pair = false;
   if (const char* f = std::getenv("GEMM_FORCE_TILE")) {
     int fm = 0, fn = 0;
-    if (std::sscanf(f, "%dx%d", &fm, &fn) == 2 && fm == dg::TC_BM && (fn == 64 || fn == 128 || fn == 256))
-      force_bn = fn;
+    if (std::sscanf(f, "%dx%d", &fm, &fn) == 2 && (fn == 64 || fn == 128 || fn == 256)) {
+      if (fm == dg::TC_BM) force_bn = fn;
+      if (fm == 2 * dg::TC_BM && fn >= 128) {  // 256-row tile on a CTA pair
+        force_bn = fn;
+        force_pair = true;
+      }
+    }
   }
   const int force_s = env_int("GEMM_FORCE_SPLITK", 0);
   const int raster = env_int("GEMM_RASTER_GROUP", 16);
   const int64_t kb = ceil_div(K, dg::TC_BK);
-  const int bns[3] = {256, 128, 64};
-  for (int bn : bns) {
-    if (force_bn && bn != force_bn) continue;
+  // candidates: 128-row tiles of width 256/128/64 on one CTA, 256 x 256 on a CTA pair
+  struct Cand { int bn; bool pair; };
+  const Cand cands[4] = {{256, true}, {256, false}, {128, false}, {64, false}};
+  bool best_pair = false;
+  for (const Cand& c : cands) {
+    if (force_bn && (c.bn != force_bn || c.pair != force_pair)) continue;
+    const int tile_m = c.pair ? 2 * dg::TC_BM : dg::TC_BM;
+    const int slots = c.pair ? sms / 2 : sms;
+    if (c.pair && slots < 1) continue;
     for (int s = 1; s <= 64; ++s) {
       if (force_s > 0 && s != force_s) continue;
       if (s > kb) break;
-      if (s > 1 && ceil_div(M, dg::TC_BM) * ceil_div(N, bn) * s > 4 * int64_t(sms)) break;
+      if (s > 1 && ceil_div(M, tile_m) * ceil_div(N, c.bn) * s > 4 * int64_t(slots)) break;
       int s_eff = 1;
-      const double t = estimate(M, N, K, bn, s, sms, c_es, beta, raster, md, &s_eff);
+      const double t = estimate(M, N, K, c.bn, c.pair, s, sms, c_es, beta, raster, md, &s_eff);
       if (s_eff != s) continue;
-      // prefer wider tiles / fewer slices unless clearly faster (2%)
+      // prefer earlier candidates / fewer slices unless clearly faster (2%)
       if (t < best_t * 0.98) {
         best_t = t;
-        best_bn = bn;
+        best_bn = c.bn;
+        best_pair = c.pair;
         best_s = s;
       }
     }
@@ -215,18 +238,23 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
   if (force_s > 0 && best_t == 1e300) {  // forced split not reachable exactly: take nearest valid
     best_s = int(std::min<int64_t>(force_s, kb));
     best_bn = force_bn ? force_bn : 256;
+    best_pair = force_pair;
   }
   const int64_t kbps = ceil_div(kb, best_s);
   best_s = int(ceil_div(kb, kbps));
+  force_pair = best_pair;
+  const int tile_m = force_pair ? 2 * dg::TC_BM : dg::TC_BM;
+  const int pairs = sms / 2;
   std::memset(out, 0, sizeof(*out));
-  quantization(M, N, dg::TC_BM, best_bn, best_s, sms, 1, out);
+  quantization(M, N, tile_m, best_bn, best_s, force_pair ? pairs : sms, 1, out);
+  out->sms = sms;
   out->path = best_s > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
   out->tile_k = dg::TC_BK;
-  out->cta_per_tile = 1;
-  out->stages = dg::tc_stages(best_bn);
-  const int64_t mblocks = ceil_div(M, dg::TC_BM);
+  out->cta_per_tile = force_pair ? 2 : 1;
+  out->stages = dg::tc_stages(best_bn, force_pair);
+  const int64_t mblocks = ceil_div(M, tile_m);
   out->raster_group = int(std::max<int64_t>(1, std::min<int64_t>(raster, mblocks)));
-  out->grid = int(std::min<int64_t>(out->units, sms));
+  out->grid = force_pair ? int(2 * std::min<int64_t>(out->units, pairs)) : int(std::min<int64_t>(out->units, sms));
 }
 
 // ------------------------------------------------------------ tensor maps
@@ -386,6 +414,13 @@ gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const voi
   choose_tc(M, N, K, plan->sms, c_es, beta != 0.f, info);
   const int bn = info->tile_n;
   const int S = info->splitk;
+  const bool pair = info->cta_per_tile == 2;
+  const int tile_m = info->tile_m;
+  if (pair) {  // the grid holds whole clusters that fit at once
+    const int mp = dg::tc_max_pairs(bn);
+    if (mp <= 0) return GEMM_ERR_UNSUPPORTED;
+    info->grid = int(2 * std::min<int64_t>(info->units, mp));
+  }
   const bool f16 = in_is_f16(dtype);
   const CUtensorMapDataType in_t = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const bool a_mn = ta == GEMM_OP_T, b_mn = tb == GEMM_OP_N;
@@ -393,22 +428,22 @@ gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const voi
   bool ok = a_mn ? make_map(&ma, in_t, 2, A, M, K, lda, 64, 64)
                  : make_map(&ma, in_t, 2, A, K, M, lda, 64, dg::TC_BM);
   ok = ok && (b_mn ? make_map(&mb, in_t, 2, B, N, K, ldb, 64, 64)
-                   : make_map(&mb, in_t, 2, B, K, N, ldb, 64, bn));
+                   : make_map(&mb, in_t, 2, B, K, N, ldb, 64, pair ? bn / 2 : bn));
   dg::TcParams p{};
   p.M = int(M);
   p.N = int(N);
   p.K = int(K);
-  p.num_m_blocks = int(ceil_div(M, dg::TC_BM));
+  p.num_m_blocks = int(ceil_div(M, tile_m));
   p.num_n_blocks = int(ceil_div(N, bn));
   p.k_blocks = int(ceil_div(K, dg::TC_BK));
   p.splitk = S;
   p.kb_per_split = int(ceil_div(p.k_blocks, S));
   p.raster_group = info->raster_group;
   p.units = int(info->units);
-  p.ws_rows = p.num_m_blocks * dg::TC_BM;
+  p.ws_rows = p.num_m_blocks * tile_m;
   p.a_mn_major = a_mn;
   p.b_mn_major = b_mn;
-  p.idesc = make_idesc(f16, a_mn, b_mn, bn, dg::TC_BM);
+  p.idesc = make_idesc(f16, a_mn, b_mn, bn, tile_m);
   p.alpha = alpha;
   p.beta = beta;
   p.act = epi.act;
@@ -438,7 +473,7 @@ gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const voi
                         ws_ld, 32, 32);
   }
   if (!ok) return GEMM_ERR_CUDA;
-  if (dg::launch_gemm_tc(bn, ma, mb, mc, p, info->grid, s) != cudaSuccess) return GEMM_ERR_CUDA;
+  if (dg::launch_gemm_tc(bn, pair, ma, mb, mc, p, info->grid, s) != cudaSuccess) return GEMM_ERR_CUDA;
   info->launches = 1;
   if (S > 1) {
     const dg::EpiParams e{alpha, beta, epi.slope, epi.act, out_kind(dtype)};

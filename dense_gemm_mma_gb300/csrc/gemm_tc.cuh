@@ -49,11 +49,16 @@
 
 namespace dg {
 
-template <int BN>
+// PAIR: a cluster of two CTAs computes one 256-row tile with .cta_group::2
+// MMAs; each CTA stages its own 128 rows of A and half of the tile's BN columns
+// of B, and holds its 128 rows of the accumulator in its tensor memory.
+template <int BN, bool PAIR = false>
 struct TcCfg {
-  static constexpr int STAGES = BN == 256 ? 4 : (BN == 128 ? 6 : 8);
+  static constexpr int TILE_M = PAIR ? 2 * TC_BM : TC_BM;
+  static constexpr int BN_CTA = PAIR ? BN / 2 : BN;   // B columns staged by one CTA
   static constexpr int A_STAGE = TC_BM * TC_BK * 2;  // 16 KB
-  static constexpr int B_STAGE = BN * TC_BK * 2;
+  static constexpr int B_STAGE = BN_CTA * TC_BK * 2;
+  static constexpr int STAGES = (192 * 1024) / (A_STAGE + B_STAGE);
   static constexpr int STG_BYTES = 32 * 128;         // one 32-row x 128-byte epilogue box
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
@@ -66,6 +71,7 @@ struct TcCfg {
   static constexpr int TMEM_COLS = 2 * BN;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(TMEM_COLS <= 512, "tensor memory budget");
+  static_assert(BN_CTA % 64 == 0, "B is staged in 64-column pieces");
 };
 
 struct Unit {
@@ -116,12 +122,15 @@ __device__ __forceinline__ float2 unpack2(uint32_t w, int out_kind) {
   return __half22float2(h);
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ TcParams p) {
-  using Cfg = TcCfg<BN>;
+  using Cfg = TcCfg<BN, PAIR>;
   constexpr int S = Cfg::STAGES;
+  constexpr int BNC = Cfg::BN_CTA;
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // 0 = leader: issues the MMAs
+  const bool leader = rank == 0;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -143,7 +152,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull0 + 8 * b, 1);
-      mbar_init(tempty0 + 8 * b, TC_EPI_WARPS);
+      mbar_init(tempty0 + 8 * b, PAIR ? 2 * TC_EPI_WARPS : TC_EPI_WARPS);  // both CTAs' epilogues
     }
     for (int e = 0; e < TC_EPI_WARPS; ++e) mbar_init(cload0 + 8 * e, 1);
     mbar_init(drain_bar, 1);
@@ -156,17 +165,30 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     prefetch_tmap(&tmC);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), Cfg::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();  // both CTAs' barriers exist before either signals the other
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   // A dependent grid (the split-K reduction) may be scheduled now; it waits
   // for this grid's completion before it reads anything.
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const Watch w{abort_flag, p.err, p.timeout_ns};
+  // Bounded wait; cluster-scope acquire when the peer CTA of a pair signals.
+  auto wait = [&](uint32_t bar, uint32_t parity, int code) {
+    if constexpr (PAIR) return wait_bar_cluster(bar, parity, w, code);
+    return wait_bar(bar, parity, w, code);
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -175,30 +197,44 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      const int cta0 = PAIR ? int(blockIdx.x) / 2 : int(blockIdx.x);
+      const int ncta = PAIR ? int(gridDim.x) / 2 : int(gridDim.x);
+      for (int u = cta0; u < p.units && ok; u += ncta) {
         const Unit x = decode_unit(u, p);
-        const int m0 = x.m_blk * TC_BM, n0 = x.n_blk * BN;
+        // this CTA's rows of A and columns of B
+        const int m0 = x.m_blk * Cfg::TILE_M + int(rank) * TC_BM;
+        const int n0 = x.n_blk * BN + int(rank) * BNC;
         for (int kb = x.kb_begin; kb < x.kb_end; ++kb) {
-          if (!wait_bar(empty0 + 8 * stage, phase ^ 1u, w, WAIT_PRODUCER_EMPTY)) {
+          if (!wait(empty0 + 8 * stage, phase ^ 1u, WAIT_PRODUCER_EMPTY)) {
             ok = false;
             break;
           }
           const uint32_t fb = full0 + 8 * stage;
           const uint32_t sa = base + Cfg::OFF_A + stage * Cfg::A_STAGE;
           const uint32_t sb = base + Cfg::OFF_B + stage * Cfg::B_STAGE;
-          mbar_arrive_expect_tx(fb, Cfg::A_STAGE + Cfg::B_STAGE);
           const int k0 = kb * TC_BK;
+          // Pair: both CTAs' loads complete on the leader's barrier, which the
+          // leader arms with both CTAs' bytes.
+          uint32_t fbc = fb;
+          if constexpr (PAIR) fbc = mapa_shared(fb, 0);
+          if (leader) mbar_arrive_expect_tx(fb, (PAIR ? 2 : 1) * (Cfg::A_STAGE + Cfg::B_STAGE));
+          auto load = [&](uint32_t dst, const CUtensorMap* m, int cx, int cy) {
+            if constexpr (PAIR)
+              tma_load_2d_pair(dst, m, fbc, cx, cy);
+            else
+              tma_load_2d(dst, m, fb, cx, cy);
+          };
           if (!p.a_mn_major) {
-            tma_load_2d(sa, &tmA, fb, k0, m0);  // 128 rows x 64 K
+            load(sa, &tmA, k0, m0);  // 128 rows x 64 K
           } else {
-            tma_load_2d(sa, &tmA, fb, m0, k0);  // 64 K rows x 64 M, twice
-            tma_load_2d(sa + 64 * 128, &tmA, fb, m0 + 64, k0);
+            load(sa, &tmA, m0, k0);  // 64 K rows x 64 M, twice
+            load(sa + 64 * 128, &tmA, m0 + 64, k0);
           }
           if (!p.b_mn_major) {
-            tma_load_2d(sb, &tmB, fb, k0, n0);  // BN rows x 64 K
+            load(sb, &tmB, k0, n0);  // BNC rows x 64 K
           } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + j * 64 * 128, &tmB, fb, n0 + 64 * j, k0);
+            for (int j = 0; j < BNC / 64; ++j) load(sb + j * 64 * 128, &tmB, n0 + 64 * j, k0);
           }
           ++issued;
           if (++stage == S) {
@@ -211,13 +247,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         // Let the loads already in flight land before the CTA can exit.
         for (int s = 0; s < S; ++s) {
           const int n_s = issued > s ? (issued - s + S - 1) / S : 0;
-          if (n_s > 0) wait_bar(full0 + 8 * s, (uint32_t)((n_s - 1) & 1), Watch{abort_flag, p.err, p.timeout_ns}, 0);
+          if (n_s > 0 && leader) wait(full0 + 8 * s, (uint32_t)((n_s - 1) & 1), 0);
         }
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       const uint32_t lbo_a = p.a_mn_major ? 64 * 128 : 16;
       const uint32_t lbo_b = p.b_mn_major ? 64 * 128 : 16;
       const uint32_t kstep_a = p.a_mn_major ? 16 * 128 : 32;
@@ -227,13 +263,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      const int cta0 = PAIR ? int(blockIdx.x) / 2 : int(blockIdx.x);
+      const int ncta = PAIR ? int(gridDim.x) / 2 : int(gridDim.x);
+      for (int u = cta0; u < p.units && ok; u += ncta) {
         const Unit x = decode_unit(u, p);
-        if (!wait_bar(tempty0 + 8 * acc, acc_phase ^ 1u, w, WAIT_MMA_TMEM_EMPTY)) break;
+        if (!wait(tempty0 + 8 * acc, acc_phase ^ 1u, WAIT_MMA_TMEM_EMPTY)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = x.kb_begin; kb < x.kb_end; ++kb) {
-          if (!wait_bar(full0 + 8 * stage, phase, w, WAIT_MMA_FULL)) {
+          if (!wait(full0 + 8 * stage, phase, WAIT_MMA_FULL)) {
             ok = false;
             break;
           }
@@ -244,22 +282,36 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           for (int kk = 0; kk < TC_BK / 16; ++kk) {
             const uint64_t ad = smem_desc_sw128(sa + kk * kstep_a, lbo_a, 1024);
             const uint64_t bd = smem_desc_sw128(sb + kk * kstep_b, lbo_b, 1024);
-            tc_mma_f16(d_tmem, ad, bd, p.idesc, (kb > x.kb_begin || kk > 0) ? 1u : 0u);
+            if constexpr (PAIR)
+              tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, (kb > x.kb_begin || kk > 0) ? 1u : 0u);
+            else
+              tc_mma_f16(d_tmem, ad, bd, p.idesc, (kb > x.kb_begin || kk > 0) ? 1u : 0u);
           }
-          tc_commit(empty0 + 8 * stage);  // stage free once these MMAs finish
+          // stage free (in both CTAs of a pair) once these MMAs finish
+          if constexpr (PAIR)
+            tc_commit_pair_multicast(empty0 + 8 * stage, 0x3);
+          else
+            tc_commit(empty0 + 8 * stage);
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        tc_commit(tfull0 + 8 * acc);  // accumulator ready for the epilogue
+        // accumulator ready for the epilogue (of both CTAs of a pair)
+        if constexpr (PAIR)
+          tc_commit_pair_multicast(tfull0 + 8 * acc, 0x3);
+        else
+          tc_commit(tfull0 + 8 * acc);
         acc ^= 1;
         if (acc == 0) acc_phase ^= 1u;
       }
       // Every MMA issued by this thread completes before tensor memory is freed.
-      tc_commit(drain_bar);
-      wait_bar(drain_bar, 0, Watch{abort_flag, p.err, p.timeout_ns}, WAIT_DRAIN);
+      if constexpr (PAIR)
+        tc_commit_pair_multicast(drain_bar, 0x1);
+      else
+        tc_commit(drain_bar);
+      wait(drain_bar, 0, WAIT_DRAIN);
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -276,15 +328,17 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     int sbuf = 0;
     uint32_t cphase = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+    const int cta0 = PAIR ? int(blockIdx.x) / 2 : int(blockIdx.x);
+    const int ncta = PAIR ? int(gridDim.x) / 2 : int(gridDim.x);
+    for (int u = cta0; u < p.units && ok; u += ncta) {
       const Unit x = decode_unit(u, p);
       // All lanes wait; the warp leaves together if any lane gave up, because the
       // tcgen05.ld below must be executed by the whole warp.
-      if (!__all_sync(0xffffffffu, wait_bar(tfull0 + 8 * acc, acc_phase, w, WAIT_EPI_TMEM_FULL)))
+      if (!__all_sync(0xffffffffu, wait(tfull0 + 8 * acc, acc_phase, WAIT_EPI_TMEM_FULL)))
         break;
       tc_fence_after();
       const int n0 = x.n_blk * BN;
-      const int row0 = x.m_blk * TC_BM + 32 * q;
+      const int row0 = x.m_blk * Cfg::TILE_M + int(rank) * TC_BM + 32 * q;
       const int y0 = partial ? x.split * p.ws_rows + row0 : row0;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc * BN);
@@ -306,7 +360,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_arrive_expect_tx(cload0 + 8 * e, Cfg::STG_BYTES);
             tma_load_2d(stg, &tmC, cload0 + 8 * e, x0, y0);
           }
-          if (!__all_sync(0xffffffffu, wait_bar(cload0 + 8 * e, cphase, w, WAIT_EPI_C_LOAD))) {
+          if (!__all_sync(0xffffffffu, wait(cload0 + 8 * e, cphase, WAIT_EPI_C_LOAD))) {
             ok = false;
             break;
           }
@@ -390,10 +444,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         sbuf ^= 1;
       }
-      // This warp's reads of the accumulator are complete: release it.
+      // This warp's reads of the accumulator are complete: release it (to the
+      // leader, whose MMA warp waits for both CTAs of a pair).
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      if (lane == 0) {
+        if constexpr (PAIR)
+          mbar_arrive_cluster(mapa_shared(tempty0 + 8 * acc, 0));
+        else
+          mbar_arrive(tempty0 + 8 * acc);
+      }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -401,24 +461,69 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
 
   // ------------------------------------------------------------- teardown
+  // A pair's CTAs stay until both are done: the leader's MMAs read the peer's
+  // shared memory and write its tensor memory.
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    if constexpr (PAIR)
+      tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
   }
 }
 
-template <int BN>
+template <int BN, bool PAIR>
 cudaError_t launch_gemm_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                               const TcParams& p, int grid, cudaStream_t s) {
-  constexpr int smem = TcCfg<BN>::SMEM_BYTES;
-  cudaError_t err =
-      cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  constexpr int smem = TcCfg<BN, PAIR>::SMEM_BYTES;
+  auto kern = gemm_tc_kernel<BN, PAIR>;
+  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  gemm_tc_kernel<BN><<<grid, TC_THREADS, smem, s>>>(a, b, c, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = PAIR ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, a, b, c, p);
+}
+
+// Clusters of two that can be resident at once (the grid of a pair kernel is
+// twice this, at most).
+template <int BN>
+int max_pairs() {
+  constexpr int smem = TcCfg<BN, true>::SMEM_BYTES;
+  auto kern = gemm_tc_kernel<BN, true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(TC_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
 }
 
 }  // namespace dg

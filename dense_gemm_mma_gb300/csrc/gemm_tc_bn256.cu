@@ -2,6 +2,9 @@
 #include "gemm_tc.cuh"
 
 namespace dg {
-template cudaError_t launch_gemm_tc_bn<256>(const CUtensorMap&, const CUtensorMap&,
-                                           const CUtensorMap&, const TcParams&, int, cudaStream_t);
+template cudaError_t launch_gemm_tc_bn<256, false>(const CUtensorMap&, const CUtensorMap&,
+                                                  const CUtensorMap&, const TcParams&, int, cudaStream_t);
+template cudaError_t launch_gemm_tc_bn<256, true>(const CUtensorMap&, const CUtensorMap&,
+                                                 const CUtensorMap&, const TcParams&, int, cudaStream_t);
+template int max_pairs<256>();
 }  // namespace dg

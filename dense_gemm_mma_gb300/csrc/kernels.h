@@ -54,11 +54,14 @@ struct TcParams {
   uint64_t timeout_ns;
 };
 
-// Shared-memory footprint of the tensor-core kernel for a tile width.
-int tc_smem_bytes(int bn);
-int tc_stages(int bn);
+// Shared-memory footprint and ring depth of the tensor-core kernel for a tile
+// width; pair = 256-row tiles computed by a cluster of two CTAs (bn 128, 256).
+int tc_smem_bytes(int bn, bool pair);
+int tc_stages(int bn, bool pair);
+// Clusters of two CTAs of the pair kernel that fit on the device at once.
+int tc_max_pairs(int bn);
 
-cudaError_t launch_gemm_tc(int bn, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t launch_gemm_tc(int bn, bool pair, const CUtensorMap& a, const CUtensorMap& b,
                            const CUtensorMap& c, const TcParams& p, int grid, cudaStream_t s);
 
 struct EpiParams {

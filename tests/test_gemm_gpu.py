@@ -122,6 +122,36 @@ def test_unaligned_row_tail_of_c(plan, out_fmt, N):
              seed=N + 1, pad=(0, 0, 8))
 
 
+# ------------------------------------------------------------------- CTA pair
+
+@pytest.mark.parametrize("shape", [(256, 256, 64), (300, 520, 200), (129, 257, 1000), (640, 384, 77),
+                                   (513, 129, 300), (2, 3, 5)])
+def test_cta_pair_ragged(plan, shape):
+    r = run_case(plan, *shape, env={"GEMM_FORCE_TILE": "256x256"}, seed=sum(shape) + 1)
+    assert r.info["tile_m"] == 256 and r.info["cta_per_tile"] == 2 and r.info["grid"] % 2 == 0
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+@pytest.mark.parametrize("ta,tb", [(False, False), (False, True), (True, False), (True, True)])
+def test_cta_pair_transposes(plan, fmt, ta, tb):
+    run_case(plan, 300, 384, 200, in_fmt=fmt, ta=ta, tb=tb, env={"GEMM_FORCE_TILE": "256x256"}, seed=11)
+
+
+@pytest.mark.parametrize("out_fmt", ["f32", "bf16", "f16"])
+def test_cta_pair_epilogues_and_tails(plan, out_fmt):
+    in_fmt = "f16" if out_fmt == "f16" else "bf16"
+    env = {"GEMM_FORCE_TILE": "256x256"}
+    run_case(plan, 257, 300, 513, in_fmt=in_fmt, out_fmt=out_fmt, beta=0.5, act=1, slope=0.1, env=env, seed=12)
+    run_case(plan, 260, 257, 129, in_fmt=in_fmt, out_fmt=out_fmt, alpha=-2.0, env=env, seed=13, pad=(0, 0, 8))
+
+
+def test_cta_pair_splitk_deterministic(plan):
+    r = run_case(plan, 512, 512, 4096, env={"GEMM_FORCE_TILE": "256x256", "GEMM_FORCE_SPLITK": "3"},
+                 repeat=2, seed=14)
+    assert r.info["splitk"] == 3 and r.info["cta_per_tile"] == 2
+    assert np.array_equal(r.outputs[0].view(np.uint8), r.outputs[1].view(np.uint8))
+
+
 # -------------------------------------------------------------------- split-K
 
 @pytest.mark.parametrize("splits", [2, 3, 7])
@@ -196,7 +226,7 @@ def test_full_config2_skinny_both_b_layouts(plan):
 
 def test_full_config3_square_bf16_out(plan):
     r = run_case(plan, 8192, 8192, 8192, out_fmt="bf16", seed=1236, sample=SAMPLE)
-    assert r.info["path"] == "tc"
+    assert r.info["path"] == "tc" and r.info["cta_per_tile"] == 2
 
 
 def test_full_config3_beta_leaky_relu(plan):

@@ -196,8 +196,10 @@ def test_planner_invariants(M, N, K):
     for sms in (108, 148, 152):
         c = g.gemm_choose_config(M, N, K, g.GEMM_BF16_F32, 0, 0, sms)
         assert c.path in (1, 2)
-        assert c.tile_m == 128 and c.tile_n in (64, 128, 256) and c.tile_k == 64
-        assert 1 <= c.grid <= sms and c.grid <= c.units
+        assert (c.tile_m, c.cta_per_tile) in ((128, 1), (256, 2))
+        assert c.tile_n in (64, 128, 256) and c.tile_k == 64
+        assert 1 <= c.grid <= sms and c.grid <= c.units * c.cta_per_tile
+        assert c.grid % c.cta_per_tile == 0
         assert c.units == c.tiles * c.splitk
         kb = -(-K // 64)
         assert 1 <= c.splitk <= kb
@@ -211,7 +213,7 @@ def test_planner_splits_small_output_with_long_k():
     c = g.gemm_choose_config(256, 256, 65536, g.GEMM_F16_F32, 0, 0, 152)
     assert c.splitk > 1 and c.units >= 64
     big = g.gemm_choose_config(8192, 8192, 8192, g.GEMM_BF16_BF16, 0, 0, 152)
-    assert big.splitk == 1 and big.tile_n == 256
+    assert big.splitk == 1 and big.tile_n == 256 and big.tile_m == 256 and big.cta_per_tile == 2
 
 
 def test_planner_gemv_paths():
@@ -221,6 +223,13 @@ def test_planner_gemv_paths():
     assert g.PATH_NAMES[g.gemm_choose_config(8192, 1, 8192, 0, 1, 0, 152).path] == "gemv_colstream"
     assert g.PATH_NAMES[g.gemm_choose_config(0, 5, 5, 0, 0, 0, 152).path] == "none"
     assert g.PATH_NAMES[g.gemm_choose_config(5, 5, 0, 0, 0, 0, 152).path] == "scale"
+
+
+def test_planner_forced_pair(monkeypatch):
+    monkeypatch.setenv("GEMM_FORCE_TILE", "256x256")
+    c = g.gemm_choose_config(1000, 1000, 1000, 0, 0, 0, 152)
+    assert c.tile_m == 256 and c.tile_n == 256 and c.cta_per_tile == 2
+    assert c.tiles == 4 * 4 and c.grid == 2 * c.units
 
 
 def test_planner_env_overrides(monkeypatch):
