@@ -14,9 +14,47 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <unordered_map>
 #include <vector>
 
 #include "kernels.h"
+
+namespace {
+
+// A tensor-core call as far as planning and descriptors are concerned.
+struct TcKey {
+  int64_t M, N, K, lda, ldb, ldc;
+  uintptr_t A, B, C;
+  int32_t dtype, ta, tb, beta_nz;
+  bool operator==(const TcKey& o) const {
+    return M == o.M && N == o.N && K == o.K && lda == o.lda && ldb == o.ldb && ldc == o.ldc &&
+           A == o.A && B == o.B && C == o.C && dtype == o.dtype && ta == o.ta && tb == o.tb &&
+           beta_nz == o.beta_nz;
+  }
+};
+
+struct TcKeyHash {
+  size_t operator()(const TcKey& k) const {
+    uint64_t h = 1469598103934665603ull;
+    auto mix = [&](uint64_t v) { h = (h ^ v) * 1099511628211ull; };
+    mix(uint64_t(k.M)); mix(uint64_t(k.N)); mix(uint64_t(k.K)); mix(uint64_t(k.lda));
+    mix(uint64_t(k.ldb)); mix(uint64_t(k.ldc)); mix(k.A); mix(k.B); mix(k.C);
+    mix(uint64_t(k.dtype) | (uint64_t(k.ta) << 8) | (uint64_t(k.tb) << 16) | (uint64_t(k.beta_nz) << 24));
+    return size_t(h);
+  }
+};
+
+// Planner decision, encoded tensor maps and kernel parameters of one call.
+struct TcEntry {
+  gemm_config_info_t info;
+  CUtensorMap ma, mb, mc;
+  dg::TcParams p;
+  int64_t ws_ld, ws_slice;
+  size_t ws_bytes;
+  void* ws_ptr;  // workspace the partial map was encoded for (split-K)
+};
+
+}  // namespace
 
 struct gemm_plan {
   int device = 0;
@@ -28,6 +66,10 @@ struct gemm_plan {
   size_t counter_count = 0;
   uint64_t watchdog_ns = 2000000000ull;
   gemm_config_info_t last{};
+  // Repeated calls with the same shapes, pointers and flags skip planning and
+  // descriptor encoding (host time that would otherwise sit in front of the
+  // kernels on the stream).
+  std::unordered_map<TcKey, TcEntry, TcKeyHash> tc_cache;
 };
 
 namespace {
@@ -127,18 +169,27 @@ double tile_efficiency(int bn) { return bn >= 256 ? 1.0 : (bn >= 128 ? 0.85 : 0.
 // Extra fixed cost of a CTA-pair (cluster) launch, fitted on GB300.
 constexpr double kPairFixed = 8.0e-6;
 
-struct TileWalk {  // host copy of the kernel's unit order (gemm_tc.cuh: decode_unit)
-  int64_t mb, nb, group;
-  void unit(int64_t u, int64_t* m, int64_t* n, int64_t* split) const {
-    const int64_t tiles = mb * nb;
-    *split = u / tiles;
-    const int64_t t = u - *split * tiles;
-    const int64_t per = group * nb, g = t / per, first = g * group;
-    const int64_t rows = std::min(mb - first, group), r = t - g * per;
-    *m = first + r % rows;
-    *n = r / rows;
+// Distinct A row-panels and B column-panels among the first `count` units of
+// the kernel's unit order (gemm_tc.cuh: decode_unit): slice-major, then groups
+// of `group` tile rows walked column by column.
+void distinct_panels(int64_t mb, int64_t nb, int64_t group, int64_t count, int64_t* da, int64_t* db) {
+  const int64_t tiles = mb * nb;
+  const int64_t full_slices = count / tiles, r = count % tiles;
+  *da = full_slices * mb;
+  *db = full_slices * nb;
+  if (r == 0) return;
+  const int64_t per = group * nb;
+  const int64_t full_groups = r / per, rem = r % per;
+  int64_t dm = std::min(full_groups * group, mb);
+  int64_t dn = full_groups > 0 ? nb : 0;
+  if (rem > 0) {
+    const int64_t rows = std::min(mb - full_groups * group, group);
+    dm += std::min(rows, rem);
+    dn = std::max(dn, ceil_div(rem, rows));
   }
-};
+  *da += dm;
+  *db += dn;
+}
 
 double estimate(int64_t M, int64_t N, int64_t K, int bn, bool pair, int splitk, int sms, int c_es,
                 bool beta, int raster_group, const Model& md, int* splitk_eff) {
@@ -151,20 +202,15 @@ double estimate(int64_t M, int64_t N, int64_t K, int bn, bool pair, int splitk, 
   // needs a third less feed per flop than a one-CTA 128 x 256 tile.
   const int tile_m = pair ? 2 * dg::TC_BM : dg::TC_BM;
   const int slots = pair ? sms / 2 : sms;
-  const TileWalk walk{ceil_div(M, tile_m), ceil_div(N, bn),
-                      std::max<int64_t>(1, std::min<int64_t>(raster_group, ceil_div(M, tile_m)))};
-  const int64_t units = walk.mb * walk.nb * s_eff;
+  const int64_t mb = ceil_div(M, tile_m), nb = ceil_div(N, bn);
+  const int64_t group = std::max<int64_t>(1, std::min<int64_t>(raster_group, mb));
+  const int64_t units = mb * nb * s_eff;
   const int64_t active = std::min<int64_t>(units, slots);
   const double waves = double(ceil_div(units, slots));
   // distinct A and B panels the first wave streams
-  std::vector<char> seen_a(size_t(walk.mb * s_eff), 0), seen_b(size_t(walk.nb * s_eff), 0);
-  int64_t streams = 0;
-  for (int64_t u = 0; u < active; ++u) {
-    int64_t m, n, sp;
-    walk.unit(u, &m, &n, &sp);
-    if (!seen_a[size_t(sp * walk.mb + m)]) { seen_a[size_t(sp * walk.mb + m)] = 1; ++streams; }
-    if (!seen_b[size_t(sp * walk.nb + n)]) { seen_b[size_t(sp * walk.nb + n)] = 1; ++streams; }
-  }
+  int64_t da = 0, db = 0;
+  distinct_panels(mb, nb, group, active, &da, &db);
+  int64_t streams = da + db;
   const double t_mma = 2.0 * dg::TC_BM * bn * double(kbps * dg::TC_BK) / (md.peak_flops / sms * tile_efficiency(bn));
   const double unit_bytes = double(dg::TC_BM + (pair ? bn / 2 : bn)) * double(kbps * dg::TC_BK) * 2.0;
   const double unique = double(M * K + K * N) * 2.0;
@@ -175,7 +221,7 @@ double estimate(int64_t M, int64_t N, int64_t K, int bn, bool pair, int splitk, 
   double bytes = unique + double(M) * N * c_es * (beta ? 2.0 : 1.0);
   double t = 0.0;
   if (s_eff > 1) {
-    const double part = double(s_eff) * double(walk.mb * dg::TC_BM) * double(N) * 4.0;
+    const double part = double(s_eff) * double(mb * tile_m) * double(N) * 4.0;
     bytes += part;                           // partials written
     t += md.reduce + part / md.hbm_bw;       // and read back by the reduction
   }
@@ -406,12 +452,23 @@ gemm_status_t run_gemv(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const v
   return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-                     const void* B, int64_t ldb, void* C, int64_t ldc, float alpha, float beta,
-                     gemm_dtype_t dtype, gemm_op_t ta, gemm_op_t tb, gemm_epilogue_t epi,
-                     cudaStream_t s, gemm_config_info_t* info) {
+bool planner_overridden() {
+  static const char* vars[] = {"GEMM_FORCE_TILE", "GEMM_FORCE_SPLITK", "GEMM_RASTER_GROUP"};
+  for (const char* v : vars) {
+    const char* x = std::getenv(v);
+    if (x && *x) return true;
+  }
+  return false;
+}
+
+// Plan a tensor-core call and encode its descriptors (cache miss).
+gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* A,
+                             int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
+                             bool beta_nz, gemm_dtype_t dtype, gemm_op_t ta, gemm_op_t tb,
+                             TcEntry* e) {
+  gemm_config_info_t* info = &e->info;
   const int c_es = out_is_f32(dtype) ? 4 : 2;
-  choose_tc(M, N, K, plan->sms, c_es, beta != 0.f, info);
+  choose_tc(M, N, K, plan->sms, c_es, beta_nz, info);
   const int bn = info->tile_n;
   const int S = info->splitk;
   const bool pair = info->cta_per_tile == 2;
@@ -424,12 +481,12 @@ gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const voi
   const bool f16 = in_is_f16(dtype);
   const CUtensorMapDataType in_t = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const bool a_mn = ta == GEMM_OP_T, b_mn = tb == GEMM_OP_N;
-  CUtensorMap ma, mb, mc;
-  bool ok = a_mn ? make_map(&ma, in_t, 2, A, M, K, lda, 64, 64)
-                 : make_map(&ma, in_t, 2, A, K, M, lda, 64, dg::TC_BM);
-  ok = ok && (b_mn ? make_map(&mb, in_t, 2, B, N, K, ldb, 64, 64)
-                   : make_map(&mb, in_t, 2, B, K, N, ldb, 64, pair ? bn / 2 : bn));
-  dg::TcParams p{};
+  bool ok = a_mn ? make_map(&e->ma, in_t, 2, A, M, K, lda, 64, 64)
+                 : make_map(&e->ma, in_t, 2, A, K, M, lda, 64, dg::TC_BM);
+  ok = ok && (b_mn ? make_map(&e->mb, in_t, 2, B, N, K, ldb, 64, 64)
+                   : make_map(&e->mb, in_t, 2, B, K, N, ldb, 64, pair ? bn / 2 : bn));
+  dg::TcParams& p = e->p;
+  p = dg::TcParams{};
   p.M = int(M);
   p.N = int(N);
   p.K = int(K);
@@ -444,43 +501,82 @@ gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const voi
   p.a_mn_major = a_mn;
   p.b_mn_major = b_mn;
   p.idesc = make_idesc(f16, a_mn, b_mn, bn, tile_m);
-  p.alpha = alpha;
-  p.beta = beta;
-  p.act = epi.act;
-  p.slope = epi.slope;
-  p.err = plan->err;
-  p.timeout_ns = plan->watchdog_ns;
   p.c_ptr = C;
   p.ldc = ldc;
-  int64_t ws_ld = 0, ws_slice = 0;
+  p.err = plan->err;
+  e->ws_ld = e->ws_slice = 0;
+  e->ws_bytes = 0;
+  e->ws_ptr = nullptr;
   if (S == 1) {
     p.out_kind = out_kind(dtype);
     // TMA stores write whole 16-byte pieces of a row: the map covers only the
     // 16-byte-aligned prefix of each row of C; the kernel writes the rest.
     p.n_tma = int((N * c_es) / 16 * 16 / c_es);
     const CUtensorMapDataType ct = out_is_f32(dtype) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : in_t;
-    ok = ok && make_map(&mc, ct, c_es, C, std::max<int64_t>(p.n_tma, 1), M, ldc, 128 / c_es, 32);
+    ok = ok && make_map(&e->mc, ct, c_es, C, std::max<int64_t>(p.n_tma, 1), M, ldc, 128 / c_es, 32);
   } else {
     p.out_kind = dg::OUT_PARTIAL;
     p.n_tma = int(N);  // the workspace rows are padded to 16 bytes: no tail
-    ws_ld = (N + 3) & ~int64_t(3);
-    ws_slice = int64_t(p.ws_rows) * ws_ld;
-    const size_t bytes = size_t(S) * size_t(ws_slice) * 4;
-    const gemm_status_t st = ensure_ws(plan, bytes, s);
-    if (st != GEMM_OK) return st;
-    info->workspace_bytes = int64_t(bytes);
-    ok = ok && make_map(&mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, plan->ws, N, int64_t(S) * p.ws_rows,
-                        ws_ld, 32, 32);
+    e->ws_ld = (N + 3) & ~int64_t(3);
+    e->ws_slice = int64_t(p.ws_rows) * e->ws_ld;
+    e->ws_bytes = size_t(S) * size_t(e->ws_slice) * 4;
+    info->workspace_bytes = int64_t(e->ws_bytes);
   }
-  if (!ok) return GEMM_ERR_CUDA;
-  if (dg::launch_gemm_tc(bn, pair, ma, mb, mc, p, info->grid, s) != cudaSuccess) return GEMM_ERR_CUDA;
-  info->launches = 1;
+  info->launches = S > 1 ? 2 : 1;
+  return ok ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                     const void* B, int64_t ldb, void* C, int64_t ldc, float alpha, float beta,
+                     gemm_dtype_t dtype, gemm_op_t ta, gemm_op_t tb, gemm_epilogue_t epi,
+                     cudaStream_t s, gemm_config_info_t* info) {
+  const TcKey key{M, N, K, lda, ldb, ldc, reinterpret_cast<uintptr_t>(A), reinterpret_cast<uintptr_t>(B),
+                  reinterpret_cast<uintptr_t>(C), int32_t(dtype), int32_t(ta), int32_t(tb),
+                  int32_t(beta != 0.f)};
+  const bool use_cache = !planner_overridden();
+  TcEntry local;
+  TcEntry* e = nullptr;
+  if (use_cache) {
+    auto it = plan->tc_cache.find(key);
+    if (it != plan->tc_cache.end()) e = &it->second;
+  }
+  if (e == nullptr) {
+    const gemm_status_t st = build_tc_entry(plan, M, N, K, A, lda, B, ldb, C, ldc, beta != 0.f, dtype,
+                                            ta, tb, &local);
+    if (st != GEMM_OK) return st;
+    if (use_cache) {
+      if (plan->tc_cache.size() >= 256) plan->tc_cache.clear();
+      e = &plan->tc_cache.emplace(key, local).first->second;
+    } else {
+      e = &local;
+    }
+  }
+  dg::TcParams p = e->p;  // per-call fields below
+  p.alpha = alpha;
+  p.beta = beta;
+  p.act = epi.act;
+  p.slope = epi.slope;
+  p.timeout_ns = plan->watchdog_ns;
+  const int S = e->info.splitk;
   if (S > 1) {
-    const dg::EpiParams e{alpha, beta, epi.slope, epi.act, out_kind(dtype)};
-    if (dg::launch_splitk_reduce(static_cast<const float*>(plan->ws), ws_ld, ws_slice, S, int(M),
-                                 int(N), C, ldc, e, s, plan->sms) != cudaSuccess)
+    const gemm_status_t st = ensure_ws(plan, e->ws_bytes, s);
+    if (st != GEMM_OK) return st;
+    if (e->ws_ptr != plan->ws) {  // (re-)encode the partial map for the current workspace
+      if (!make_map(&e->mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, plan->ws, N,
+                    int64_t(S) * e->p.ws_rows, e->ws_ld, 32, 32))
+        return GEMM_ERR_CUDA;
+      e->ws_ptr = plan->ws;
+    }
+  }
+  *info = e->info;
+  const bool pair = e->info.cta_per_tile == 2;
+  if (dg::launch_gemm_tc(e->info.tile_n, pair, e->ma, e->mb, e->mc, p, e->info.grid, s) != cudaSuccess)
+    return GEMM_ERR_CUDA;
+  if (S > 1) {
+    const dg::EpiParams ep{alpha, beta, epi.slope, epi.act, out_kind(dtype)};
+    if (dg::launch_splitk_reduce(static_cast<const float*>(plan->ws), e->ws_ld, e->ws_slice, S, int(M),
+                                 int(N), C, ldc, ep, s, plan->sms) != cudaSuccess)
       return GEMM_ERR_CUDA;
-    info->launches = 2;
   }
   return GEMM_OK;
 }
