@@ -190,6 +190,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside), "note": note}
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """Largest `value` over all ranks (the slowest replica sets the job time)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, steps: int, step_bytes: float, max_ms: float) -> float:
+    """Whole-job GB/s: the bytes every replica processed over the slowest replica's time."""
+    return world * steps * step_bytes / (max_ms / 1e3) / 1e9
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -420,14 +435,10 @@ def main():
     call_ms = np.array([[ev[s][i][0].elapsed_time(ev[s][i][1]) for i in range(n)]
                         for s in range(args.steps)])
     step_ms = call_ms.sum(axis=1)
-    total_ms = float(step_ms.sum())
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(float(step_ms.sum()), dist, dev)
     step_bytes = sum(c.bytes for c in calls)
     step_flops = sum(c.flops for c in calls)
-    value = ws * args.steps * step_bytes / (total_ms / 1e3) / 1e9
+    value = job_throughput(ws, args.steps, step_bytes, total_ms)
 
     peaks, peak_src = load_peaks()
     mean_call = call_ms.mean(axis=0)
@@ -567,12 +578,8 @@ def measure_e2e(args, calls, host, devbuf, launch, stream, dev, torch, step_byte
         if s > 0:
             e1[s - 1].record(stream)
     torch.cuda.synchronize(dev)
-    ms = float(sum(a.elapsed_time(b) for a, b in zip(e0, e1)))
-    if dist is not None:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": round(ws * steps * step_bytes / (ms / 1e3) / 1e9, 1), "unit": "GB/s",
+    ms = max_over_ranks(float(sum(a.elapsed_time(b) for a, b in zip(e0, e1))), dist, dev)
+    return {"value": round(job_throughput(ws, steps, step_bytes, ms), 1), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(ms / steps, 4)}
 

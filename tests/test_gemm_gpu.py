@@ -167,6 +167,55 @@ def test_splitk_ragged_with_beta(plan):
     assert r.info["splitk"] == 5
 
 
+def test_plan_cache_survives_workspace_growth(plan):
+    """A repeated call reuses its cached plan and descriptors; when another
+    call grows (reallocates) the plan's workspace in between, the cached
+    split-K call re-targets the new workspace and gives the same bits."""
+    import torch
+    from dense_gemm_mma_gb300 import gemm, inputs
+    from tests.gemm_case import decode, to_device
+    import oracle
+    M, N, K = 256, 256, 16384
+    A = inputs.matrix(M, K, 301, inputs.TENSOR_A, "bf16")
+    B = inputs.matrix(K, N, 301, inputs.TENSOR_B, "bf16")
+    Ad, Bd = to_device(A, "bf16"), to_device(B, "bf16")
+    C1 = torch.zeros(M, N, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+
+    def call(c):
+        assert gemm.gemm_run(plan.handle, M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), N, c.data_ptr(), N,
+                             1.0, 0.0, gemm.GEMM_BF16_F32, 0, 0, 0, 0.0, st) == gemm.GEMM_OK
+        torch.cuda.synchronize()
+        return plan.last_config()
+
+    info1 = call(C1)
+    assert info1["path"] == "tc_splitk"
+    first = C1.cpu().numpy().copy()
+    # a larger split-K problem grows the workspace
+    M2, N2, K2 = 1024, 1024, 65536
+    A2 = torch.zeros(M2, K2, device="cuda", dtype=torch.bfloat16)
+    B2 = torch.zeros(K2, N2, device="cuda", dtype=torch.bfloat16)
+    C2 = torch.zeros(M2, N2, device="cuda")
+    assert gemm.gemm_run(plan.handle, M2, N2, K2, A2.data_ptr(), K2, B2.data_ptr(), N2, C2.data_ptr(), N2,
+                         1.0, 0.0, gemm.GEMM_BF16_F32, 0, 0, 0, 0.0, st) == gemm.GEMM_OK
+    torch.cuda.synchronize()
+    info2 = plan.last_config()
+    assert info2["workspace_bytes"] > info1["workspace_bytes"]
+    C1.zero_()
+    info3 = call(C1)
+    assert info3["splitk"] == info1["splitk"]
+    assert np.array_equal(C1.cpu().numpy().view(np.uint32), first.view(np.uint32))
+    # and it is right: sampled against the oracle
+    rows = np.arange(0, M, 17)
+    cols = (rows * 7) % N
+    exact, _ = oracle.sample(rows, cols, K, A, B)
+    assert np.all(np.abs(first[rows, cols] - exact) <= 1e-5 * K + 2.0 ** -21 * np.abs(exact))
+    # a different output pointer with the same shape is a different entry
+    C3 = torch.zeros(M, N, device="cuda")
+    call(C3)
+    assert np.array_equal(C3.cpu().numpy().view(np.uint32), first.view(np.uint32))
+
+
 # ----------------------------------------------------------------------- GEMV
 
 @pytest.mark.parametrize("tb", [False, True])
