@@ -168,6 +168,10 @@ double tile_efficiency(int bn) { return bn >= 256 ? 1.0 : (bn >= 128 ? 0.85 : 0.
 
 // Extra fixed cost of a CTA-pair (cluster) launch, fitted on GB300.
 constexpr double kPairFixed = 8.0e-6;
+// Cost of a K pair's on-chip exchange per 64-column round (bn/128 rounds):
+// 32 KB of fp32 partials each way between two SMs, measured on GB300 at
+// ~2 us (distributed shared memory moves ~15-27 GB/s per SM each way).
+constexpr double kKPairRound = 2.0e-6;
 
 // Distinct A row-panels and B column-panels among the first `count` units of
 // the kernel's unit order (gemm_tc.cuh: decode_unit): slice-major, then groups
@@ -191,15 +195,17 @@ void distinct_panels(int64_t mb, int64_t nb, int64_t group, int64_t count, int64
   *db += dn;
 }
 
-double estimate(int64_t M, int64_t N, int64_t K, int bn, bool pair, int splitk, int sms, int c_es,
+double estimate(int64_t M, int64_t N, int64_t K, int bn, int mode, int splitk, int sms, int c_es,
                 bool beta, int raster_group, const Model& md, int* splitk_eff) {
+  const bool pair = mode == dg::TC_PAIR, kpair = mode == dg::TC_KPAIR;
   const int64_t kb = ceil_div(K, dg::TC_BK);
   const int64_t kbps = ceil_div(kb, splitk);
   const int s_eff = int(ceil_div(kb, kbps));
   *splitk_eff = s_eff;
   // A pair unit (256 x bn) runs on two SMs; each SM stages 128 rows of A and
   // bn/2 columns of B per k-block and does the flops of a 128 x bn tile, so it
-  // needs a third less feed per flop than a one-CTA 128 x 256 tile.
+  // needs a third less feed per flop than a one-CTA 128 x 256 tile.  A K-pair
+  // tile is two CTA units (its K halves) that run side by side.
   const int tile_m = pair ? 2 * dg::TC_BM : dg::TC_BM;
   const int slots = pair ? sms / 2 : sms;
   const int64_t mb = ceil_div(M, tile_m), nb = ceil_div(N, bn);
@@ -209,7 +215,13 @@ double estimate(int64_t M, int64_t N, int64_t K, int bn, bool pair, int splitk, 
   const double waves = double(ceil_div(units, slots));
   // distinct A and B panels the first wave streams
   int64_t da = 0, db = 0;
-  distinct_panels(mb, nb, group, active, &da, &db);
+  if (kpair) {
+    distinct_panels(mb, nb, group, active / 2, &da, &db);
+    da *= 2;  // both K halves of each panel stream at once
+    db *= 2;
+  } else {
+    distinct_panels(mb, nb, group, active, &da, &db);
+  }
   int64_t streams = da + db;
   const double t_mma = 2.0 * dg::TC_BM * bn * double(kbps * dg::TC_BK) / (md.peak_flops / sms * tile_efficiency(bn));
   const double unit_bytes = double(dg::TC_BM + (pair ? bn / 2 : bn)) * double(kbps * dg::TC_BK) * 2.0;
@@ -217,10 +229,11 @@ double estimate(int64_t M, int64_t N, int64_t K, int bn, bool pair, int splitk, 
   const double reuse = (1.0 - 1.0 / waves) *
                        std::max(0.0, 1.0 - unique / (double(units) * (pair ? 2 : 1) * unit_bytes));
   const double feed = md.feed * (1.0 + md.reuse_gain * reuse);
-  const double makespan = waves * std::max(t_mma, unit_bytes / feed) + md.fixed + (pair ? kPairFixed : 0.0);
+  const double makespan = waves * std::max(t_mma, unit_bytes / feed) + md.fixed +
+                          (pair ? kPairFixed : 0.0) + (kpair ? kKPairRound * (bn / 128) : 0.0);
   double bytes = unique + double(M) * N * c_es * (beta ? 2.0 : 1.0);
   double t = 0.0;
-  if (s_eff > 1) {
+  if (s_eff > 1 && !kpair) {
     const double part = double(s_eff) * double(mb * tile_m) * double(N) * 4.0;
     bytes += part;                           // partials written
     t += md.reduce + part / md.hbm_bw;       // and read back by the reduction
@@ -239,7 +252,7 @@ int env_int(const char* name, int dflt) {
 void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
                gemm_config_info_t* out) {
   const Model md;
-  int best_bn = 256, best_s = 1;
+  int best_bn = 256, best_s = 1, best_mode = dg::TC_SOLO;
   double best_t = 1e300;
   int force_bn = 0;
   bool force_pair = false;
@@ -254,53 +267,72 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
     }
   }
   const int force_s = env_int("GEMM_FORCE_SPLITK", 0);
+  // GEMM_SPLITK_CLUSTER: 0 never reduces K halves on chip, 1 only does (where
+  // a two-slice split on a K pair exists), unset lets the model choose.
+  const int kpair_env = env_int("GEMM_SPLITK_CLUSTER", -1);
   const int raster = env_int("GEMM_RASTER_GROUP", 16);
   const int64_t kb = ceil_div(K, dg::TC_BK);
-  // candidates: 128-row tiles of width 256/128/64 on one CTA, 256 x 256 on a CTA pair
-  struct Cand { int bn; bool pair; };
-  const Cand cands[4] = {{256, true}, {256, false}, {128, false}, {64, false}};
-  bool best_pair = false;
+  // candidates: 128-row tiles of width 256/128/64 on one CTA, 256 x 256 on a
+  // CTA pair, 128 x 128 with K halves on a K pair.  The 128 x 256 K pair
+  // (two exchange rounds, and a third of each ring stage for A instead of
+  // half) measured no faster than the 256 x 256 CTA pair on any shape: it
+  // runs only when that tile is forced.
+  struct Cand { int bn; int mode; };
+  const Cand cands[6] = {{256, dg::TC_PAIR}, {256, dg::TC_SOLO}, {128, dg::TC_SOLO}, {64, dg::TC_SOLO},
+                         {256, dg::TC_KPAIR}, {128, dg::TC_KPAIR}};
   for (const Cand& c : cands) {
-    if (force_bn && (c.bn != force_bn || c.pair != force_pair)) continue;
-    const int tile_m = c.pair ? 2 * dg::TC_BM : dg::TC_BM;
-    const int slots = c.pair ? sms / 2 : sms;
-    if (c.pair && slots < 1) continue;
-    for (int s = 1; s <= 64; ++s) {
+    const bool kpair = c.mode == dg::TC_KPAIR;
+    if (force_bn && (c.bn != force_bn || (c.mode == dg::TC_PAIR) != force_pair)) continue;
+    if (kpair ? kpair_env == 0 : kpair_env == 1) continue;
+    if (kpair && c.bn == 256 && force_bn != 256) continue;
+    // A K pair pays its exchange on every tile; it measured faster only where
+    // the tiles fit one wave of clusters (then it replaces a reduction launch).
+    if (kpair && kpair_env != 1 && ceil_div(M, dg::TC_BM) * ceil_div(N, c.bn) > sms / 2) continue;
+    const int tile_m = c.mode == dg::TC_PAIR ? 2 * dg::TC_BM : dg::TC_BM;
+    const int slots = c.mode == dg::TC_PAIR ? sms / 2 : sms;
+    if (c.mode != dg::TC_SOLO && sms < 2) continue;
+    for (int s = kpair ? 2 : 1; s <= (kpair ? 2 : 64); ++s) {
       if (force_s > 0 && s != force_s) continue;
       if (s > kb) break;
       if (s > 1 && ceil_div(M, tile_m) * ceil_div(N, c.bn) * s > 4 * int64_t(slots)) break;
       int s_eff = 1;
-      const double t = estimate(M, N, K, c.bn, c.pair, s, sms, c_es, beta, raster, md, &s_eff);
+      const double t = estimate(M, N, K, c.bn, c.mode, s, sms, c_es, beta, raster, md, &s_eff);
       if (s_eff != s) continue;
       // prefer earlier candidates / fewer slices unless clearly faster (2%)
       if (t < best_t * 0.98) {
         best_t = t;
         best_bn = c.bn;
-        best_pair = c.pair;
+        best_mode = c.mode;
         best_s = s;
       }
     }
   }
-  if (force_s > 0 && best_t == 1e300) {  // forced split not reachable exactly: take nearest valid
-    best_s = int(std::min<int64_t>(force_s, kb));
+  if (best_t == 1e300) {  // forced choices not reachable exactly: take the nearest valid
+    best_s = force_s > 0 ? int(std::min<int64_t>(force_s, kb)) : 1;
     best_bn = force_bn ? force_bn : 256;
-    best_pair = force_pair;
+    best_mode = force_pair ? dg::TC_PAIR : dg::TC_SOLO;
   }
   const int64_t kbps = ceil_div(kb, best_s);
   best_s = int(ceil_div(kb, kbps));
-  force_pair = best_pair;
-  const int tile_m = force_pair ? 2 * dg::TC_BM : dg::TC_BM;
+  const bool pair = best_mode == dg::TC_PAIR, kpair = best_mode == dg::TC_KPAIR;
+  const int tile_m = pair ? 2 * dg::TC_BM : dg::TC_BM;
   const int pairs = sms / 2;
   std::memset(out, 0, sizeof(*out));
-  quantization(M, N, tile_m, best_bn, best_s, force_pair ? pairs : sms, 1, out);
+  quantization(M, N, tile_m, best_bn, best_s, pair ? pairs : sms, 1, out);
   out->sms = sms;
-  out->path = best_s > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC;
+  out->path = kpair ? GEMM_PATH_TC_SPLITK_CLUSTER : (best_s > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC);
   out->tile_k = dg::TC_BK;
-  out->cta_per_tile = force_pair ? 2 : 1;
-  out->stages = dg::tc_stages(best_bn, force_pair);
+  out->cta_per_tile = best_mode == dg::TC_SOLO ? 1 : 2;
+  out->stages = dg::tc_stages(best_bn, best_mode);
   const int64_t mblocks = ceil_div(M, tile_m);
   out->raster_group = int(std::max<int64_t>(1, std::min<int64_t>(raster, mblocks)));
-  out->grid = force_pair ? int(2 * std::min<int64_t>(out->units, pairs)) : int(std::min<int64_t>(out->units, sms));
+  if (pair)
+    out->grid = int(2 * std::min<int64_t>(out->units, pairs));
+  else if (kpair)
+    out->grid = int(2 * std::min<int64_t>(out->tiles, pairs));
+  else
+    out->grid = int(std::min<int64_t>(out->units, sms));
+  out->launches = best_s > 1 && !kpair ? 2 : 1;
 }
 
 // ------------------------------------------------------------ tensor maps
@@ -452,8 +484,15 @@ gemm_status_t run_gemv(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const v
   return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
+// Kernel variant of a tensor-core plan.
+int tc_mode(const gemm_config_info_t& info) {
+  if (info.path == GEMM_PATH_TC_SPLITK_CLUSTER) return dg::TC_KPAIR;
+  return info.cta_per_tile == 2 ? dg::TC_PAIR : dg::TC_SOLO;
+}
+
 bool planner_overridden() {
-  static const char* vars[] = {"GEMM_FORCE_TILE", "GEMM_FORCE_SPLITK", "GEMM_RASTER_GROUP"};
+  static const char* vars[] = {"GEMM_FORCE_TILE", "GEMM_FORCE_SPLITK", "GEMM_RASTER_GROUP",
+                               "GEMM_SPLITK_CLUSTER"};
   for (const char* v : vars) {
     const char* x = std::getenv(v);
     if (x && *x) return true;
@@ -471,12 +510,13 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
   choose_tc(M, N, K, plan->sms, c_es, beta_nz, info);
   const int bn = info->tile_n;
   const int S = info->splitk;
-  const bool pair = info->cta_per_tile == 2;
+  const int mode = tc_mode(*info);
+  const bool pair = mode == dg::TC_PAIR, kpair = mode == dg::TC_KPAIR;
   const int tile_m = info->tile_m;
-  if (pair) {  // the grid holds whole clusters that fit at once
-    const int mp = dg::tc_max_pairs(bn);
-    if (mp <= 0) return GEMM_ERR_UNSUPPORTED;
-    info->grid = int(2 * std::min<int64_t>(info->units, mp));
+  if (mode != dg::TC_SOLO) {  // the grid holds whole clusters that fit at once
+    const int mc = dg::tc_max_clusters(bn, mode);
+    if (mc <= 0) return GEMM_ERR_UNSUPPORTED;
+    info->grid = int(2 * std::min<int64_t>(pair ? info->units : info->tiles, mc));
   }
   const bool f16 = in_is_f16(dtype);
   const CUtensorMapDataType in_t = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -496,7 +536,7 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
   p.splitk = S;
   p.kb_per_split = int(ceil_div(p.k_blocks, S));
   p.raster_group = info->raster_group;
-  p.units = int(info->units);
+  p.units = int(kpair ? info->tiles : info->units);  // a K pair's cluster takes whole tiles
   p.ws_rows = p.num_m_blocks * tile_m;
   p.a_mn_major = a_mn;
   p.b_mn_major = b_mn;
@@ -507,7 +547,7 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
   e->ws_ld = e->ws_slice = 0;
   e->ws_bytes = 0;
   e->ws_ptr = nullptr;
-  if (S == 1) {
+  if (S == 1 || kpair) {
     p.out_kind = out_kind(dtype);
     // TMA stores write whole 16-byte pieces of a row: the map covers only the
     // 16-byte-aligned prefix of each row of C; the kernel writes the rest.
@@ -522,7 +562,7 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
     e->ws_bytes = size_t(S) * size_t(e->ws_slice) * 4;
     info->workspace_bytes = int64_t(e->ws_bytes);
   }
-  info->launches = S > 1 ? 2 : 1;
+  info->launches = S > 1 && !kpair ? 2 : 1;
   return ok ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -557,7 +597,8 @@ gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const voi
   p.act = epi.act;
   p.slope = epi.slope;
   p.timeout_ns = plan->watchdog_ns;
-  const int S = e->info.splitk;
+  const int mode = tc_mode(e->info);
+  const int S = mode == dg::TC_KPAIR ? 1 : e->info.splitk;  // slices reduced by a second launch
   if (S > 1) {
     const gemm_status_t st = ensure_ws(plan, e->ws_bytes, s);
     if (st != GEMM_OK) return st;
@@ -569,8 +610,7 @@ gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const voi
     }
   }
   *info = e->info;
-  const bool pair = e->info.cta_per_tile == 2;
-  if (dg::launch_gemm_tc(e->info.tile_n, pair, e->ma, e->mb, e->mc, p, e->info.grid, s) != cudaSuccess)
+  if (dg::launch_gemm_tc(e->info.tile_n, mode, e->ma, e->mb, e->mc, p, e->info.grid, s) != cudaSuccess)
     return GEMM_ERR_CUDA;
   if (S > 1) {
     const dg::EpiParams ep{alpha, beta, epi.slope, epi.act, out_kind(dtype)};
@@ -760,7 +800,6 @@ gemm_status_t gemm_choose_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t d
     return GEMM_OK;
   }
   choose_tc(M, N, K, sms, out_is_f32(dtype) ? 4 : 2, false, out);
-  out->launches = out->splitk > 1 ? 2 : 1;
   return GEMM_OK;
 }
 

@@ -39,6 +39,15 @@
 //    fp32 partials to the workspace and a separate kernel sums the slices in a
 //    fixed order ("Matrix Multiplication Background User's Guide", section 2.3:
 //    splitting along K needs a final reduction).
+//  - K pair (TC_KPAIR): the same reduction done on chip for two slices.  A
+//    cluster of two CTAs takes one tile; CTA r runs the r-th half of the K
+//    loop into its own tensor memory.  In the epilogue each CTA sends its
+//    partial sums of the other CTA's half of the columns straight into that
+//    CTA's staging buffers (st.async into distributed shared memory, counted
+//    on the receiver's mbarrier), adds the partials it receives to its own
+//    and finishes its half of the columns.  fp32 addition is commutative, so
+//    both halves are summed in the same, fixed way, and the result equals the
+//    two-slice reduction kernel's.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -49,11 +58,15 @@
 
 namespace dg {
 
-// PAIR: a cluster of two CTAs computes one 256-row tile with .cta_group::2
+// TC_PAIR: a cluster of two CTAs computes one 256-row tile with .cta_group::2
 // MMAs; each CTA stages its own 128 rows of A and half of the tile's BN columns
 // of B, and holds its 128 rows of the accumulator in its tensor memory.
-template <int BN, bool PAIR = false>
+// TC_KPAIR: each CTA of a cluster of two stages whole 128 x BN tiles' blocks of
+// one half of K; the exchange of partials goes through the staging buffers.
+template <int BN, int MODE = TC_SOLO>
 struct TcCfg {
+  static constexpr bool PAIR = MODE == TC_PAIR;
+  static constexpr bool KPAIR = MODE == TC_KPAIR;
   static constexpr int TILE_M = PAIR ? 2 * TC_BM : TC_BM;
   static constexpr int BN_CTA = PAIR ? BN / 2 : BN;   // B columns staged by one CTA
   static constexpr int A_STAGE = TC_BM * TC_BK * 2;  // 16 KB
@@ -64,14 +77,20 @@ struct TcCfg {
   static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
   static constexpr int OFF_STG = OFF_B + STAGES * B_STAGE;
   static constexpr int OFF_BAR = OFF_STG + TC_EPI_WARPS * 2 * STG_BYTES;
-  // full[S], empty[S], tmem_full[2], tmem_empty[2], c_load[4], drain[1]
-  static constexpr int NUM_BARS = 2 * STAGES + 4 + TC_EPI_WARPS + 1;
+  // full[S], empty[S], tmem_full[2], tmem_empty[2], c_load[4], drain[1],
+  // K pair: xfull[4] (the peer's partials have landed), xfree[4] (the peer's
+  // staging buffers may be written)
+  static constexpr int NUM_BARS = 2 * STAGES + 4 + TC_EPI_WARPS + 1 + 2 * TC_EPI_WARPS;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;  // tmem address, abort flag
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1024-B alignment
   static constexpr int TMEM_COLS = 2 * BN;
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(TMEM_COLS <= 512, "tensor memory budget");
   static_assert(BN_CTA % 64 == 0, "B is staged in 64-column pieces");
+  // K pair: each CTA finishes BN/2 columns, 64 per exchange round (the two
+  // staging buffers of a warp hold 32 rows x 64 fp32 partials).
+  static constexpr int KP_ROUNDS = BN / 128;
+  static_assert(!KPAIR || BN >= 128, "a K pair finishes 64-column pieces");
 };
 
 struct Unit {
@@ -122,15 +141,40 @@ __device__ __forceinline__ float2 unpack2(uint32_t w, int out_kind) {
   return __half22float2(h);
 }
 
-template <int BN, bool PAIR>
+// 16 bytes of C starting at (row, col), col a multiple of 16 / esize; zero
+// outside the matrix.  C and ldc * esize are 16-byte multiples on this path.
+__device__ __forceinline__ uint4 load_c16(const TcParams& p, int row, int col, int esize) {
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (row >= p.M || col >= p.N) return v;
+  const int per = 16 / esize;
+  const uint8_t* src = static_cast<const uint8_t*>(p.c_ptr) + (int64_t(row) * p.ldc + col) * esize;
+  if (col + per <= p.N) return *reinterpret_cast<const uint4*>(src);
+  // ragged end of the row
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (i < per && col + i < p.N) {
+      if (esize == 4)
+        w[i & 3] = reinterpret_cast<const uint32_t*>(src)[i];
+      else
+        w[i >> 1] |= uint32_t(reinterpret_cast<const uint16_t*>(src)[i]) << (16 * (i & 1));
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <int BN, int MODE>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ TcParams p) {
-  using Cfg = TcCfg<BN, PAIR>;
+  using Cfg = TcCfg<BN, MODE>;
+  constexpr bool PAIR = Cfg::PAIR;
+  constexpr bool KPAIR = Cfg::KPAIR;
+  constexpr bool CLUSTER = MODE != TC_SOLO;
   constexpr int S = Cfg::STAGES;
   constexpr int BNC = Cfg::BN_CTA;
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;  // 0 = leader: issues the MMAs
-  const bool leader = rank == 0;
+  const uint32_t rank = CLUSTER ? cluster_ctarank() : 0u;
+  const bool leader = !PAIR || rank == 0;  // issues MMAs (only CTA 0 of a 256-row pair)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -142,6 +186,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   const uint32_t full0 = bar0, empty0 = bar0 + 8 * S;
   const uint32_t tfull0 = bar0 + 16 * S, tempty0 = tfull0 + 16;
   const uint32_t cload0 = tempty0 + 16, drain_bar = cload0 + 8 * TC_EPI_WARPS;
+  const uint32_t xfull0 = drain_bar + 8, xfree0 = xfull0 + 8 * TC_EPI_WARPS;
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + Cfg::OFF_MISC);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(sbase + Cfg::OFF_MISC + 4);
 
@@ -154,7 +199,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       mbar_init(tfull0 + 8 * b, 1);
       mbar_init(tempty0 + 8 * b, PAIR ? 2 * TC_EPI_WARPS : TC_EPI_WARPS);  // both CTAs' epilogues
     }
-    for (int e = 0; e < TC_EPI_WARPS; ++e) mbar_init(cload0 + 8 * e, 1);
+    for (int e = 0; e < TC_EPI_WARPS; ++e) {
+      mbar_init(cload0 + 8 * e, 1);
+      mbar_init(xfull0 + 8 * e, 1);  // own arrive.expect_tx; the peer's bytes complete it
+      mbar_init(xfree0 + 8 * e, 1);  // one arrival from the peer per exchange round
+    }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -174,7 +223,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     }
   }
   tc_fence_before();
-  if constexpr (PAIR)
+  if constexpr (CLUSTER)
     cluster_sync();  // both CTAs' barriers exist before either signals the other
   else
     __syncthreads();
@@ -184,10 +233,27 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   // for this grid's completion before it reads anything.
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const Watch w{abort_flag, p.err, p.timeout_ns};
-  // Bounded wait; cluster-scope acquire when the peer CTA of a pair signals.
+  // Bounded wait; cluster-scope acquire when the peer CTA signals (a pair's
+  // shared pipeline).  A K pair's pipeline is its own; only its exchange
+  // barriers hear from the peer.
   auto wait = [&](uint32_t bar, uint32_t parity, int code) {
     if constexpr (PAIR) return wait_bar_cluster(bar, parity, w, code);
     return wait_bar(bar, parity, w, code);
+  };
+  auto wait_peer = [&](uint32_t bar, uint32_t parity, int code) {
+    return wait_bar_cluster(bar, parity, w, code);
+  };
+  // Units: a cluster walks tiles; a K pair's CTA r takes the r-th K half.
+  const int cta0 = CLUSTER ? int(blockIdx.x) / 2 : int(blockIdx.x);
+  const int ncta = CLUSTER ? int(gridDim.x) / 2 : int(gridDim.x);
+  auto unit_of = [&](int u) {
+    Unit x = decode_unit(u, p);
+    if constexpr (KPAIR) {
+      x.split = int(rank);
+      x.kb_begin = int(rank) * p.kb_per_split;
+      x.kb_end = min(p.k_blocks, x.kb_begin + p.kb_per_split);
+    }
+    return x;
   };
 
   if (warp == 0) {
@@ -197,13 +263,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
-      const int cta0 = PAIR ? int(blockIdx.x) / 2 : int(blockIdx.x);
-      const int ncta = PAIR ? int(gridDim.x) / 2 : int(gridDim.x);
       for (int u = cta0; u < p.units && ok; u += ncta) {
-        const Unit x = decode_unit(u, p);
+        const Unit x = unit_of(u);
         // this CTA's rows of A and columns of B
-        const int m0 = x.m_blk * Cfg::TILE_M + int(rank) * TC_BM;
-        const int n0 = x.n_blk * BN + int(rank) * BNC;
+        const int m0 = x.m_blk * Cfg::TILE_M + (PAIR ? int(rank) * TC_BM : 0);
+        const int n0 = x.n_blk * BN + (PAIR ? int(rank) * BNC : 0);
         for (int kb = x.kb_begin; kb < x.kb_end; ++kb) {
           if (!wait(empty0 + 8 * stage, phase ^ 1u, WAIT_PRODUCER_EMPTY)) {
             ok = false;
@@ -263,10 +327,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       bool ok = true;
-      const int cta0 = PAIR ? int(blockIdx.x) / 2 : int(blockIdx.x);
-      const int ncta = PAIR ? int(gridDim.x) / 2 : int(gridDim.x);
       for (int u = cta0; u < p.units && ok; u += ncta) {
-        const Unit x = decode_unit(u, p);
+        const Unit x = unit_of(u);
         if (!wait(tempty0 + 8 * acc, acc_phase ^ 1u, WAIT_MMA_TMEM_EMPTY)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
@@ -313,6 +375,171 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         tc_commit(drain_bar);
       wait(drain_bar, 0, WAIT_DRAIN);
     }
+  } else if constexpr (KPAIR) {
+    // ------------------------------------------------- epilogue of a K pair
+    // Warp e of each CTA reads tensor-memory lanes 32q..32q+31 (tile rows) and
+    // trades with warp e of the peer.  Per round: my two staging buffers are
+    // free (my stores from them are done) -> tell the peer and arm my receive;
+    // send my partials of the peer's 64 columns into the peer's buffers once
+    // the peer says they are free; wait for the peer's partials of my 64
+    // columns, add, apply the epilogue in place and store with TMA.
+    const int e = warp - 2;
+    const int q = warp & 3;
+    const uint32_t peer = rank ^ 1u;
+    const bool has_beta = p.beta != 0.f;
+    const int esize = p.out_kind == OUT_F32 ? 4 : 2;
+    const uint32_t stg0 = base + Cfg::OFF_STG + e * 2 * Cfg::STG_BYTES;
+    uint8_t* const stg_p0 = sbase + Cfg::OFF_STG + e * 2 * Cfg::STG_BYTES;
+    const uint32_t xfull = xfull0 + 8 * e, xfree = xfree0 + 8 * e;
+    const uint32_t peer_stg = mapa_shared(stg0, peer) + lane * 128;
+    const uint32_t peer_xfull = mapa_shared(xfull, peer);
+    const uint32_t peer_xfree = mapa_shared(xfree, peer);
+    const int sw = lane & 7;  // 128-byte swizzle: 16-byte chunk j of row r lives at j ^ (r % 8)
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    uint32_t xphase = 0;
+    bool ok = true;
+    for (int u = cta0; u < p.units && ok; u += ncta) {
+      const Unit x = unit_of(u);
+      if (!__all_sync(0xffffffffu, wait(tfull0 + 8 * acc, acc_phase, WAIT_EPI_TMEM_FULL))) break;
+      tc_fence_after();
+      const int y0 = x.m_blk * TC_BM + 32 * q;
+      const int row = y0 + lane;
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
+                             static_cast<uint32_t>(acc * BN);
+      for (int rd = 0; rd < Cfg::KP_ROUNDS; ++rd) {
+        const int own_c = int(rank) * (BN / 2) + rd * 64;  // tile columns finished here
+        const int peer_c = int(peer) * (BN / 2) + rd * 64;
+        if (lane == 0) {
+          bulk_wait_read<0>();
+          mbar_arrive_cluster(peer_xfree);
+          mbar_arrive_expect_tx(xfull, 2 * Cfg::STG_BYTES);
+        }
+        __syncwarp();
+        {
+          uint32_t r0[32], r1[32];
+          tmem_ld_32x32b_x32(t_row + peer_c, r0);
+          tmem_ld_32x32b_x32(t_row + peer_c + 32, r1);
+          tmem_ld_wait(r0);
+          tmem_ld_wait(r1);
+          if (!__all_sync(0xffffffffu, wait_peer(xfree, xphase, WAIT_EPI_EXCHANGE))) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint32_t off = uint32_t((j ^ sw) << 4);
+            st_async_v4(peer_stg + off, r0[4 * j], r0[4 * j + 1], r0[4 * j + 2], r0[4 * j + 3], peer_xfull);
+            st_async_v4(peer_stg + Cfg::STG_BYTES + off, r1[4 * j], r1[4 * j + 1], r1[4 * j + 2],
+                        r1[4 * j + 3], peer_xfull);
+          }
+        }
+        if (!__all_sync(0xffffffffu, wait_peer(xfull, xphase, WAIT_EPI_EXCHANGE))) {
+          ok = false;
+          break;
+        }
+        xphase ^= 1u;
+        if (esize == 4) {
+          for (int c = 0; c < 2; ++c) {
+            const int x0 = x.n_blk * BN + own_c + 32 * c;
+            uint8_t* const row_p = stg_p0 + c * Cfg::STG_BYTES + lane * 128;
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(t_row + own_c + 32 * c, r);
+            tmem_ld_wait(r);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float4* slot = reinterpret_cast<float4*>(row_p + ((j ^ sw) << 4));
+              const float4 pv = *slot;
+              float4 cv = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (has_beta) {
+                const uint4 cw = load_c16(p, row, x0 + 4 * j, 4);
+                cv = make_float4(__uint_as_float(cw.x), __uint_as_float(cw.y), __uint_as_float(cw.z),
+                                 __uint_as_float(cw.w));
+              }
+              float4 o;
+              o.x = epi_value(__uint_as_float(r[4 * j + 0]) + pv.x, cv.x, p, has_beta);
+              o.y = epi_value(__uint_as_float(r[4 * j + 1]) + pv.y, cv.y, p, has_beta);
+              o.z = epi_value(__uint_as_float(r[4 * j + 2]) + pv.z, cv.z, p, has_beta);
+              o.w = epi_value(__uint_as_float(r[4 * j + 3]) + pv.w, cv.w, p, has_beta);
+              *slot = o;
+            }
+            const int tail_lo = max(x0, p.n_tma), tail_hi = min(x0 + 32, p.N);
+            if (tail_lo < tail_hi && row < p.M) {
+              for (int col = tail_lo; col < tail_hi; ++col) {
+                const int b = (col - x0) * 4;
+                *reinterpret_cast<float*>(static_cast<uint8_t*>(p.c_ptr) + (int64_t(row) * p.ldc + col) * 4) =
+                    *reinterpret_cast<const float*>(row_p + (((b >> 4) ^ sw) << 4) + (b & 15));
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              if (x0 < p.n_tma) tma_store_2d(&tmC, stg0 + c * Cfg::STG_BYTES, x0, y0);
+              bulk_commit();
+            }
+          }
+        } else {
+          const int x0 = x.n_blk * BN + own_c;
+          uint32_t r0[32], r1[32];
+          tmem_ld_32x32b_x32(t_row + own_c, r0);
+          tmem_ld_32x32b_x32(t_row + own_c + 32, r1);
+          tmem_ld_wait(r0);
+          tmem_ld_wait(r1);
+          // the peer's partials of my 64 columns, whole row first (the bf16 /
+          // fp16 result is then written over the first buffer)
+          float pv[64];
+          uint8_t* const row_p = stg_p0 + lane * 128;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float4 v = *reinterpret_cast<const float4*>(row_p + (j >> 3) * Cfg::STG_BYTES +
+                                                              (((j & 7) ^ sw) << 4));
+            pv[4 * j] = v.x;
+            pv[4 * j + 1] = v.y;
+            pv[4 * j + 2] = v.z;
+            pv[4 * j + 3] = v.w;
+          }
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint4 cv = make_uint4(0u, 0u, 0u, 0u);
+            if (has_beta) cv = load_c16(p, row, x0 + 8 * j, 2);
+            const uint32_t* src = j < 4 ? &r0[8 * j] : &r1[8 * (j - 4)];
+            const uint32_t cw4[4] = {cv.x, cv.y, cv.z, cv.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              const float2 cc = unpack2(cw4[t], p.out_kind);
+              const float a = epi_value(__uint_as_float(src[2 * t]) + pv[8 * j + 2 * t], cc.x, p, has_beta);
+              const float b = epi_value(__uint_as_float(src[2 * t + 1]) + pv[8 * j + 2 * t + 1], cc.y, p,
+                                        has_beta);
+              o[t] = pack2(a, b, p.out_kind);
+            }
+            *reinterpret_cast<uint4*>(row_p + ((j ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+          const int tail_lo = max(x0, p.n_tma), tail_hi = min(x0 + 64, p.N);
+          if (tail_lo < tail_hi && row < p.M) {
+            for (int col = tail_lo; col < tail_hi; ++col) {
+              const int b = (col - x0) * 2;
+              *reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(p.c_ptr) + (int64_t(row) * p.ldc + col) * 2) =
+                  *reinterpret_cast<const uint16_t*>(row_p + (((b >> 4) ^ sw) << 4) + (b & 15));
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (x0 < p.n_tma) tma_store_2d(&tmC, stg0, x0, y0);
+            bulk_commit();
+          }
+        }
+      }
+      if (!ok) break;
+      // this warp's reads of the accumulator are complete: release it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (lane == 0) bulk_wait<0>();
   } else {
     // ------------------------------------------------------------ epilogue
     const int e = warp - 2;  // staging buffers / C-load barrier of this warp
@@ -328,10 +555,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     int sbuf = 0;
     uint32_t cphase = 0;
     bool ok = true;
-    const int cta0 = PAIR ? int(blockIdx.x) / 2 : int(blockIdx.x);
-    const int ncta = PAIR ? int(gridDim.x) / 2 : int(gridDim.x);
     for (int u = cta0; u < p.units && ok; u += ncta) {
-      const Unit x = decode_unit(u, p);
+      const Unit x = unit_of(u);
       // All lanes wait; the warp leaves together if any lane gave up, because the
       // tcgen05.ld below must be executed by the whole warp.
       if (!__all_sync(0xffffffffu, wait(tfull0 + 8 * acc, acc_phase, WAIT_EPI_TMEM_FULL)))
@@ -461,10 +686,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
 
   // ------------------------------------------------------------- teardown
-  // A pair's CTAs stay until both are done: the leader's MMAs read the peer's
-  // shared memory and write its tensor memory.
+  // A cluster's CTAs stay until both are done: a pair leader's MMAs read the
+  // peer's shared memory and write its tensor memory; a K pair writes partial
+  // sums into the peer's shared memory and arrives on its barriers.
   tc_fence_before();
-  if constexpr (PAIR)
+  if constexpr (CLUSTER)
     cluster_sync();
   else
     __syncthreads();
@@ -478,11 +704,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
 }
 
-template <int BN, bool PAIR>
+template <int BN, int MODE>
 cudaError_t launch_gemm_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                               const TcParams& p, int grid, cudaStream_t s) {
-  constexpr int smem = TcCfg<BN, PAIR>::SMEM_BYTES;
-  auto kern = gemm_tc_kernel<BN, PAIR>;
+  constexpr int smem = TcCfg<BN, MODE>::SMEM_BYTES;
+  auto kern = gemm_tc_kernel<BN, MODE>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};
@@ -492,20 +718,20 @@ cudaError_t launch_gemm_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const 
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = PAIR ? 2 : 1;
+  attr[0].val.clusterDim.x = MODE != TC_SOLO ? 2 : 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = PAIR ? 1 : 0;
+  cfg.numAttrs = MODE != TC_SOLO ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kern, a, b, c, p);
 }
 
-// Clusters of two that can be resident at once (the grid of a pair kernel is
-// twice this, at most).
-template <int BN>
-int max_pairs() {
-  constexpr int smem = TcCfg<BN, true>::SMEM_BYTES;
-  auto kern = gemm_tc_kernel<BN, true>;
+// Clusters of two that can be resident at once (the grid of a cluster kernel
+// is twice this, at most).
+template <int BN, int MODE>
+int max_clusters() {
+  constexpr int smem = TcCfg<BN, MODE>::SMEM_BYTES;
+  auto kern = gemm_tc_kernel<BN, MODE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);

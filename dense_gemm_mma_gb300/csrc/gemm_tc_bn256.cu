@@ -1,10 +1,15 @@
-// Tensor-core GEMM kernel instantiated for 256-column output tiles.
+// Tensor-core GEMM kernel instantiated for 256-column output tiles: one CTA per
+// tile, a CTA pair per 256-row tile, and a K pair.
 #include "gemm_tc.cuh"
 
 namespace dg {
-template cudaError_t launch_gemm_tc_bn<256, false>(const CUtensorMap&, const CUtensorMap&,
-                                                  const CUtensorMap&, const TcParams&, int, cudaStream_t);
-template cudaError_t launch_gemm_tc_bn<256, true>(const CUtensorMap&, const CUtensorMap&,
-                                                 const CUtensorMap&, const TcParams&, int, cudaStream_t);
-template int max_pairs<256>();
+#define DG_INST(MODE)                                                                              \
+  template cudaError_t launch_gemm_tc_bn<256, MODE>(const CUtensorMap&, const CUtensorMap&,        \
+                                                   const CUtensorMap&, const TcParams&, int, cudaStream_t);
+DG_INST(TC_SOLO)
+DG_INST(TC_PAIR)
+DG_INST(TC_KPAIR)
+#undef DG_INST
+template int max_clusters<256, TC_PAIR>();
+template int max_clusters<256, TC_KPAIR>();
 }  // namespace dg

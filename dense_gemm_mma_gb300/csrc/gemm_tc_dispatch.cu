@@ -1,58 +1,70 @@
-// Selects the tensor-core kernel instantiation for a tile shape.
+// Selects the tensor-core kernel instantiation for a tile shape and mode.
 #include "gemm_tc.cuh"
 
 namespace dg {
 
-#define DG_EXTERN(BN, PAIR)                                                                   \
-  extern template cudaError_t launch_gemm_tc_bn<BN, PAIR>(const CUtensorMap&, const CUtensorMap&, \
+#define DG_EXTERN(BN, MODE)                                                                        \
+  extern template cudaError_t launch_gemm_tc_bn<BN, MODE>(const CUtensorMap&, const CUtensorMap&, \
                                                           const CUtensorMap&, const TcParams&, int, \
                                                           cudaStream_t);
-DG_EXTERN(64, false)
-DG_EXTERN(128, false)
-DG_EXTERN(256, false)
-DG_EXTERN(128, true)
-DG_EXTERN(256, true)
+DG_EXTERN(64, TC_SOLO)
+DG_EXTERN(128, TC_SOLO)
+DG_EXTERN(256, TC_SOLO)
+DG_EXTERN(128, TC_PAIR)
+DG_EXTERN(256, TC_PAIR)
+DG_EXTERN(128, TC_KPAIR)
+DG_EXTERN(256, TC_KPAIR)
 #undef DG_EXTERN
-extern template int max_pairs<128>();
-extern template int max_pairs<256>();
+extern template int max_clusters<128, TC_PAIR>();
+extern template int max_clusters<256, TC_PAIR>();
+extern template int max_clusters<128, TC_KPAIR>();
+extern template int max_clusters<256, TC_KPAIR>();
 
-int tc_smem_bytes(int bn, bool pair) {
-  if (pair) return bn == 256 ? TcCfg<256, true>::SMEM_BYTES : (bn == 128 ? TcCfg<128, true>::SMEM_BYTES : -1);
-  switch (bn) {
-    case 64: return TcCfg<64>::SMEM_BYTES;
-    case 128: return TcCfg<128>::SMEM_BYTES;
-    case 256: return TcCfg<256>::SMEM_BYTES;
+namespace {
+template <int MODE>
+int cfg_value(int bn, bool stages) {
+  if (bn == 128) return stages ? TcCfg<128, MODE>::STAGES : TcCfg<128, MODE>::SMEM_BYTES;
+  if (bn == 256) return stages ? TcCfg<256, MODE>::STAGES : TcCfg<256, MODE>::SMEM_BYTES;
+  if (bn == 64 && MODE == TC_SOLO) return stages ? TcCfg<64>::STAGES : TcCfg<64>::SMEM_BYTES;
+  return -1;
+}
+
+int cfg_of(int bn, int mode, bool stages) {
+  switch (mode) {
+    case TC_SOLO: return cfg_value<TC_SOLO>(bn, stages);
+    case TC_PAIR: return cfg_value<TC_PAIR>(bn, stages);
+    case TC_KPAIR: return cfg_value<TC_KPAIR>(bn, stages);
     default: return -1;
   }
 }
+}  // namespace
 
-int tc_stages(int bn, bool pair) {
-  if (pair) return bn == 256 ? TcCfg<256, true>::STAGES : (bn == 128 ? TcCfg<128, true>::STAGES : -1);
-  switch (bn) {
-    case 64: return TcCfg<64>::STAGES;
-    case 128: return TcCfg<128>::STAGES;
-    case 256: return TcCfg<256>::STAGES;
-    default: return -1;
-  }
-}
+int tc_smem_bytes(int bn, int mode) { return cfg_of(bn, mode, false); }
+int tc_stages(int bn, int mode) { return cfg_of(bn, mode, true); }
 
-int tc_max_pairs(int bn) {
-  if (bn == 256) return max_pairs<256>();
-  if (bn == 128) return max_pairs<128>();
+int tc_max_clusters(int bn, int mode) {
+  if (mode == TC_PAIR) return bn == 256 ? max_clusters<256, TC_PAIR>() : (bn == 128 ? max_clusters<128, TC_PAIR>() : 0);
+  if (mode == TC_KPAIR)
+    return bn == 256 ? max_clusters<256, TC_KPAIR>() : (bn == 128 ? max_clusters<128, TC_KPAIR>() : 0);
   return 0;
 }
 
-cudaError_t launch_gemm_tc(int bn, bool pair, const CUtensorMap& a, const CUtensorMap& b,
+cudaError_t launch_gemm_tc(int bn, int mode, const CUtensorMap& a, const CUtensorMap& b,
                            const CUtensorMap& c, const TcParams& p, int grid, cudaStream_t s) {
-  if (pair) {
-    if (bn == 256) return launch_gemm_tc_bn<256, true>(a, b, c, p, grid, s);
-    if (bn == 128) return launch_gemm_tc_bn<128, true>(a, b, c, p, grid, s);
+  if (mode == TC_PAIR) {
+    if (bn == 256) return launch_gemm_tc_bn<256, TC_PAIR>(a, b, c, p, grid, s);
+    if (bn == 128) return launch_gemm_tc_bn<128, TC_PAIR>(a, b, c, p, grid, s);
+    return cudaErrorInvalidValue;
+  }
+  if (mode == TC_KPAIR) {
+    if (bn == 256) return launch_gemm_tc_bn<256, TC_KPAIR>(a, b, c, p, grid, s);
+    if (bn == 128) return launch_gemm_tc_bn<128, TC_KPAIR>(a, b, c, p, grid, s);
     return cudaErrorInvalidValue;
   }
   switch (bn) {
-    case 64: return launch_gemm_tc_bn<64, false>(a, b, c, p, grid, s);
-    case 128: return launch_gemm_tc_bn<128, false>(a, b, c, p, grid, s);
-    case 256: return launch_gemm_tc_bn<256, false>(a, b, c, p, grid, s);
+    case 64: return launch_gemm_tc_bn<64, TC_SOLO>(a, b, c, p, grid, s);
+    case 128: return launch_gemm_tc_bn<128, TC_SOLO>(a, b, c, p, grid, s);
+    case 256: return launch_gemm_tc_bn<256, TC_SOLO>(a, b, c, p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

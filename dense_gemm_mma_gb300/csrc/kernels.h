@@ -24,7 +24,17 @@ enum WaitCode : int {
   WAIT_EPI_TMEM_FULL = 8,
   WAIT_EPI_C_LOAD = 16,
   WAIT_DRAIN = 32,
-  WAIT_SELFTEST = 64
+  WAIT_SELFTEST = 64,
+  WAIT_EPI_EXCHANGE = 128  // K pair: the peer CTA's partial sums or its free buffers
+};
+
+// Variants of the tensor-core kernel.
+enum TcMode : int {
+  TC_SOLO = 0,  // one CTA per 128-row tile (K optionally split over units + reduction kernel)
+  TC_PAIR = 1,  // a cluster of two CTAs computes one 256-row tile with .cta_group::2 MMAs
+  TC_KPAIR = 2  // a cluster of two CTAs splits the K loop of one 128-row tile in halves;
+                // the halves' partial sums are exchanged through distributed shared
+                // memory and each CTA finishes half of the tile's columns
 };
 
 constexpr int TC_BM = 128;       // output rows per tile (one tcgen05.mma M=128)
@@ -55,13 +65,15 @@ struct TcParams {
 };
 
 // Shared-memory footprint and ring depth of the tensor-core kernel for a tile
-// width; pair = 256-row tiles computed by a cluster of two CTAs (bn 128, 256).
-int tc_smem_bytes(int bn, bool pair);
-int tc_stages(int bn, bool pair);
-// Clusters of two CTAs of the pair kernel that fit on the device at once.
-int tc_max_pairs(int bn);
+// width and TcMode (TC_PAIR and TC_KPAIR exist for bn 128 and 256); -1 if none.
+int tc_smem_bytes(int bn, int mode);
+int tc_stages(int bn, int mode);
+// Clusters of two CTAs of a TC_PAIR / TC_KPAIR kernel that fit on the device at once.
+int tc_max_clusters(int bn, int mode);
 
-cudaError_t launch_gemm_tc(int bn, bool pair, const CUtensorMap& a, const CUtensorMap& b,
+// TC_KPAIR: p.units counts tiles (one per cluster), p.kb_per_split is half the
+// k-blocks (rounded up), the output kind is final (not OUT_PARTIAL).
+cudaError_t launch_gemm_tc(int bn, int mode, const CUtensorMap& a, const CUtensorMap& b,
                            const CUtensorMap& c, const TcParams& p, int grid, cudaStream_t s);
 
 struct EpiParams {

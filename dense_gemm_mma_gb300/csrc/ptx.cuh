@@ -321,6 +321,17 @@ __device__ __forceinline__ void tc_commit_pair_multicast(uint32_t bar, uint16_t 
       : "memory");
 }
 
+// 16-byte store into the shared memory of a CTA of this cluster (cluster
+// address) whose completion is counted, in bytes, on a barrier of that CTA.
+__device__ __forceinline__ void st_async_v4(uint32_t dst_cluster, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d, uint32_t bar_cluster) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          dst_cluster),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar_cluster)
+      : "memory");
+}
+
 static __device__ __noinline__ bool wait_bar_slow_cluster(uint32_t bar, uint32_t parity, const Watch w,
                                                           int code) {
   const uint64_t t0 = global_timer_ns();

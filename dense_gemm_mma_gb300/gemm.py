@@ -27,7 +27,7 @@ GEMM_BF16_F32, GEMM_BF16_BF16, GEMM_F16_F32, GEMM_F16_F16 = 0, 1, 2, 3
 GEMM_ACT_NONE, GEMM_ACT_LEAKY_RELU = 0, 1
 
 PATH_NAMES = {0: "none", 1: "tc", 2: "tc_splitk", 3: "gemv_rowdot", 4: "gemv_colstream",
-              5: "gemv_generic", 6: "scale"}
+              5: "gemv_generic", 6: "scale", 7: "tc_splitk_cluster"}
 
 DTYPES = {("bf16", "f32"): GEMM_BF16_F32, ("bf16", "bf16"): GEMM_BF16_BF16,
           ("f16", "f32"): GEMM_F16_F32, ("f16", "f16"): GEMM_F16_F16}

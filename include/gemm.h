@@ -87,7 +87,10 @@ typedef enum {
   GEMM_PATH_GEMV_ROWDOT = 3,   /* GEMV: one warp per contiguous row                      */
   GEMM_PATH_GEMV_COLSTREAM = 4,/* GEMV: threads own 8 contiguous columns, K split       */
   GEMM_PATH_GEMV_GENERIC = 5,  /* GEMV with strided operands (no 128-bit loads)          */
-  GEMM_PATH_SCALE = 6          /* K == 0 or alpha == 0: C <- act(beta*C)                 */
+  GEMM_PATH_SCALE = 6,         /* K == 0 or alpha == 0: C <- act(beta*C)                 */
+  GEMM_PATH_TC_SPLITK_CLUSTER = 7 /* tcgen05 GEMM, K in two halves on a cluster of two CTAs
+                                  whose partial sums are added on chip: one launch, no
+                                  workspace (the reduction of section 2.3 done in place) */
 } gemm_path_t;
 
 /* Plan decisions and the tile/wave quantization they imply ("Matrix
@@ -98,14 +101,16 @@ typedef struct {
   int32_t tile_m;          /* output tile rows (tensor-core paths)                     */
   int32_t tile_n;          /* output tile columns                                      */
   int32_t tile_k;          /* K elements per pipeline stage                            */
-  int32_t cta_per_tile;    /* CTAs that share one tile's MMA (1; 2 = CTA pair)         */
+  int32_t cta_per_tile;    /* CTAs that work on one tile (1; 2 = a cluster of two: a    */
+                           /* 256-row CTA pair, or the K halves of a split-K cluster)  */
   int32_t splitk;          /* K slices (1 = none)                                      */
   int32_t stages;          /* shared-memory pipeline depth                             */
   int32_t raster_group;    /* output-tile rows per rasterisation group                 */
   int32_t grid;            /* CTAs launched for the main kernel                        */
   int32_t sms;             /* streaming multiprocessors used for the wave size         */
   int64_t tiles;           /* output tiles = ceil(M/tile_m) * ceil(N/tile_n)           */
-  int64_t units;           /* work units = tiles * splitk                              */
+  int64_t units;           /* work units = tiles * splitk (CTA-sized: a 256-row pair   */
+                           /* tile is one unit of two CTAs)                            */
   double waves;            /* units / wave size                                        */
   double tail_fraction;    /* (units mod wave) / wave: SMs busy in the last wave, 0=full */
   double useful_fraction;  /* M*N / (tiles*tile_m*tile_n): share of tile area in C     */

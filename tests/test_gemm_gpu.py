@@ -156,9 +156,67 @@ def test_cta_pair_splitk_deterministic(plan):
 
 @pytest.mark.parametrize("splits", [2, 3, 7])
 def test_splitk_forced_and_deterministic(plan, splits):
-    r = run_case(plan, 256, 256, 4096, env={"GEMM_FORCE_SPLITK": str(splits)}, repeat=2, seed=60)
+    r = run_case(plan, 256, 256, 4096, env={"GEMM_FORCE_SPLITK": str(splits), "GEMM_SPLITK_CLUSTER": "0"},
+                 repeat=2, seed=60)
     assert r.info["path"] == "tc_splitk" and r.info["splitk"] == splits
     assert np.array_equal(r.outputs[0].view(np.uint8), r.outputs[1].view(np.uint8))
+
+
+# ------------------------------------------- split-K reduced on chip (K pair)
+
+KPAIR = {"GEMM_SPLITK_CLUSTER": "1", "GEMM_FORCE_SPLITK": "2"}
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("shape", [(300, 520, 1000), (129, 257, 130), (640, 384, 65), (128, 128, 128)])
+def test_kpair_ragged(plan, bn, shape):
+    r = run_case(plan, *shape, env={**KPAIR, "GEMM_FORCE_TILE": f"128x{bn}"}, seed=sum(shape) + bn + 1)
+    assert r.info["path"] == "tc_splitk_cluster" and r.info["tile_n"] == bn
+    assert r.info["splitk"] == 2 and r.info["cta_per_tile"] == 2 and r.info["launches"] == 1
+    assert r.info["workspace_bytes"] == 0
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+@pytest.mark.parametrize("out_fmt", ["f32", "bf16", "f16"])
+def test_kpair_epilogues_transposes_and_tails(plan, bn, out_fmt):
+    in_fmt = "f16" if out_fmt == "f16" else "bf16"
+    env = {**KPAIR, "GEMM_FORCE_TILE": f"128x{bn}"}
+    # beta and LeakyReLU; N not a multiple of 16 bytes of C (thread-written tail)
+    run_case(plan, 257, 300, 513, in_fmt=in_fmt, out_fmt=out_fmt, beta=0.5, act=1, slope=0.1, env=env,
+             seed=70 + bn)
+    run_case(plan, 260, 203, 777, in_fmt=in_fmt, out_fmt=out_fmt, alpha=-2.0, beta=-1.0, ta=True, tb=True,
+             env=env, seed=71 + bn, pad=(8, 16, 8))
+    run_case(plan, 130, 129, 200, in_fmt=in_fmt, out_fmt=out_fmt, ta=True, env=env, seed=72 + bn)
+    run_case(plan, 200, 136, 300, in_fmt=in_fmt, out_fmt=out_fmt, tb=True, env=env, seed=73 + bn)
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+def test_kpair_many_tiles_per_cluster(plan, bn):
+    """More tiles than resident clusters: each cluster walks several tiles, so
+    both tensor-memory accumulators and every exchange-barrier phase turn over."""
+    r = run_case(plan, 4100, 1030, 700, env={**KPAIR, "GEMM_FORCE_TILE": f"128x{bn}"}, seed=74 + bn,
+                 sample=4096, out_fmt="bf16", beta=0.25)
+    assert r.info["tiles"] > r.info["grid"]
+
+
+@pytest.mark.parametrize("bn", [128, 256])
+def test_kpair_bitwise_equals_two_slice_reduction(plan, bn):
+    """Both forms add the same two fp32 slices once and apply the same
+    epilogue, so their outputs agree bit for bit, and repeat bit for bit."""
+    env = {"GEMM_FORCE_SPLITK": "2", "GEMM_FORCE_TILE": f"128x{bn}"}
+    a = run_case(plan, 384, 520, 3000, env={**env, "GEMM_SPLITK_CLUSTER": "1"}, beta=0.5, act=1, slope=0.2,
+                 repeat=2, seed=75)
+    b = run_case(plan, 384, 520, 3000, env={**env, "GEMM_SPLITK_CLUSTER": "0"}, beta=0.5, act=1, slope=0.2,
+                 seed=75)
+    assert a.info["path"] == "tc_splitk_cluster" and b.info["path"] == "tc_splitk"
+    assert np.array_equal(a.outputs[0].view(np.uint8), a.outputs[1].view(np.uint8))
+    assert np.array_equal(a.outputs[0].view(np.uint8), b.outputs[0].view(np.uint8))
+
+
+def test_kpair_plan_cache_and_watchdog_clear(plan):
+    r = run_case(plan, 1024, 128, 8192, env=KPAIR, repeat=3, seed=76)
+    assert r.info["path"] == "tc_splitk_cluster"
+    assert plan.poll_error() == 0
 
 
 def test_splitk_ragged_with_beta(plan):

@@ -195,8 +195,9 @@ def test_roofline_bound():
 def test_planner_invariants(M, N, K):
     for sms in (108, 148, 152):
         c = g.gemm_choose_config(M, N, K, g.GEMM_BF16_F32, 0, 0, sms)
-        assert c.path in (1, 2)
-        assert (c.tile_m, c.cta_per_tile) in ((128, 1), (256, 2))
+        assert c.path in (1, 2, 7)
+        assert (c.tile_m, c.cta_per_tile) in ((128, 1), (256, 2), (128, 2))
+        assert (c.tile_m, c.cta_per_tile) != (128, 2) or (c.path == 7 and c.splitk == 2)
         assert c.tile_n in (64, 128, 256) and c.tile_k == 64
         assert 1 <= c.grid <= sms and c.grid <= c.units * c.cta_per_tile
         assert c.grid % c.cta_per_tile == 0
@@ -205,8 +206,8 @@ def test_planner_invariants(M, N, K):
         assert 1 <= c.splitk <= kb
         per = -(-kb // c.splitk)
         assert -(-kb // per) == c.splitk                  # no empty K slice
-        assert (c.path == 2) == (c.splitk > 1)
-        assert c.launches == (2 if c.splitk > 1 else 1)
+        assert (c.path in (2, 7)) == (c.splitk > 1)
+        assert c.launches == (2 if c.path == 2 else 1)
 
 
 def test_planner_splits_small_output_with_long_k():
@@ -230,6 +231,23 @@ def test_planner_forced_pair(monkeypatch):
     c = g.gemm_choose_config(1000, 1000, 1000, 0, 0, 0, 152)
     assert c.tile_m == 256 and c.tile_n == 256 and c.cta_per_tile == 2
     assert c.tiles == 4 * 4 and c.grid == 2 * c.units
+
+
+def test_planner_kpair_switch(monkeypatch):
+    """GEMM_SPLITK_CLUSTER=1 takes the on-chip two-slice reduction (a cluster
+    of two CTAs per 128-row tile, one launch); =0 never does."""
+    monkeypatch.setenv("GEMM_SPLITK_CLUSTER", "1")
+    c = g.gemm_choose_config(1024, 1024, 4096, 0, 0, 0, 152)
+    assert g.PATH_NAMES[c.path] == "tc_splitk_cluster"
+    assert (c.tile_m, c.cta_per_tile, c.splitk, c.launches) == (128, 2, 2, 1)
+    assert c.units == 2 * c.tiles and c.grid == 2 * min(c.tiles, 76)
+    monkeypatch.setenv("GEMM_SPLITK_CLUSTER", "0")
+    for shape in [(8192, 128, 8192), (8192, 256, 8192), (1024, 1024, 4096)]:
+        assert g.gemm_choose_config(*shape, 0, 0, 0, 152).path in (1, 2)
+    # K of one k-block cannot be halved: the switch is ignored
+    monkeypatch.setenv("GEMM_SPLITK_CLUSTER", "1")
+    c = g.gemm_choose_config(1024, 1024, 64, 0, 0, 0, 152)
+    assert c.path in (1, 2) and c.splitk == 1
 
 
 def test_planner_env_overrides(monkeypatch):
