@@ -122,7 +122,7 @@ def load_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 100 ms."""
+    """nvidia-smi clocks / throttle reasons sampled every 20 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -138,7 +138,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -177,7 +177,7 @@ class ClockSampler:
         note = "samples inside the timed region"
         if not inside:  # timed region shorter than the sampling period: nearest samples
             inside = [min(rows, key=lambda tr: min(abs(tr[0] - t0), abs(tr[0] - t1)))[1]]
-            note = "timed region shorter than the 100 ms sampling period; nearest sample"
+            note = "timed region shorter than the 20 ms sampling period; nearest sample"
         reasons = set()
         for r in inside:
             for key, name in (("hw_slowdown", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
@@ -188,6 +188,18 @@ class ClockSampler:
                 "sm_max_mhz": max(r["max"] for r in inside),
                 "power_w_max": max(r["power"] for r in inside),
                 "reasons": sorted(reasons), "samples": len(inside), "note": note}
+
+
+def ref_tiling(c, sms: int):
+    """Tile and wave quantization of the call under a fixed 256 x 128 tiling, one
+    tile per SM ("Matrix Multiplication Background User's Guide", section 3.2,
+    quotes its tail-wave example for 256 x 128 tiles on 108 SMs), for comparison
+    with the tiling the planner chose.  None for GEMV shapes."""
+    from dense_gemm_mma_gb300 import gemm
+    if c.M < 2 or c.N < 2 or sms <= 0:
+        return None
+    q = gemm.gemm_quantization(c.M, c.N, 256, 128, 1, sms, 1)
+    return {"tiles": q.tiles, "waves": round(q.waves, 3), "tail_fraction": round(q.tail_fraction, 4)}
 
 
 def max_over_ranks(value: float, dist, device) -> float:
@@ -441,6 +453,7 @@ def main():
     value = job_throughput(ws, args.steps, step_bytes, total_ms)
 
     peaks, peak_src = load_peaks()
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     mean_call = call_ms.mean(axis=0)
     parts = []
     for i, c in enumerate(calls):
@@ -451,13 +464,15 @@ def main():
         parts.append({
             "name": c.name, "us": round(mean_call[i] * 1e3, 2),
             "us_median": round(float(np.median(call_ms[:, i])) * 1e3, 2),
+            "us_iqr": round(float(np.subtract(*np.percentile(call_ms[:, i], [75, 25]))) * 1e3, 2),
             "tflops": round(c.flops / sec / 1e12, 2), "gbs": round(c.bytes / sec / 1e9, 1),
             "intensity": round(ai, 1), "bound": rl.bound(ai, peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9),
             "frac_of_roofline": round(c.flops / sec / att, 3),
             "frac_of_nominal_roofline": round(c.flops / sec / rl.attainable(ai, 2.25e15, 8e12), 3),
             "path": info["path"], "tile": f"{info['tile_m']}x{info['tile_n']}", "splitk": info["splitk"],
             "grid": info["grid"], "units": info["units"], "waves": round(info["waves"], 3),
-            "tail_fraction": round(info["tail_fraction"], 4), "launches": info["launches"]})
+            "tail_fraction": round(info["tail_fraction"], 4), "launches": info["launches"],
+            "ref_256x128": ref_tiling(c, n_sms)})
     dom = int(np.argmax(mean_call))
     dc = calls[dom]
     dom_sec = mean_call[dom] / 1e3
@@ -480,7 +495,7 @@ def main():
     # ---- CPU oracle baseline (rank 0, N == 1 only)
     cpu = None
     if not args.no_cpu and rank == 0 and ws == 1:
-        frac = args.cpu_fraction or {"skinny": 1 / 16, "square": 1 / 8192, "small": 1 / 8,
+        frac = args.cpu_fraction or {"skinny": 1 / 4, "square": 1 / 8192, "small": 1 / 8,
                                      "tile": 1 / 4096, "wave": 1 / 2048}[args.workload]
         secs, byts, desc = oracle_sample(calls, host, frac)
         cpu = {"value": round(byts / secs / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",

@@ -64,3 +64,17 @@ def test_replicas_take_the_slowest_rank_gloo():
     for rank, worst, gbs in out:
         assert worst == 20.0                      # max over ranks
         assert gbs == pytest.approx(2 * 10 * 1e8 / 0.020 / 1e9)
+
+
+def test_reference_tiling_matches_the_guides_tail_wave_example():
+    """The guide's section 3.2 example: 2304 x 1536 x 4096 with 256 x 128 tiles
+    fills 108 SMs exactly (108 tiles); N = 1544 needs 117 tiles, a second wave
+    with 9 of 108 SMs busy (8.33%)."""
+    import bench
+    import __graft_entry__
+    __graft_entry__.build_library()
+    full = bench.ref_tiling(bench.Call("x", 2304, 1536, 4096), 108)
+    assert full == {"tiles": 108, "waves": 1.0, "tail_fraction": 0.0}
+    tail = bench.ref_tiling(bench.Call("x", 2304, 1544, 4096), 108)
+    assert tail["tiles"] == 117 and tail["tail_fraction"] == round(9 / 108, 4)
+    assert bench.ref_tiling(bench.Call("gemv", 1, 8192, 8192), 152) is None
