@@ -47,9 +47,8 @@ struct TcKeyHash {
 // Planner decision, encoded tensor maps and kernel parameters of one call.
 struct TcEntry {
   gemm_config_info_t info;
-  CUtensorMap ma, mb, mc;
+  CUtensorMap ma, mb, mc, mw;  // A, B, C, split-K partial workspace
   dg::TcParams p;
-  int64_t ws_ld, ws_slice;
   size_t ws_bytes;
   void* ws_ptr;  // workspace the partial map was encoded for (split-K)
 };
@@ -243,6 +242,45 @@ double estimate(int64_t M, int64_t N, int64_t K, int bn, int mode, int splitk, i
   return std::max(makespan, t_mem) + t;
 }
 
+// Extra cost of a tail split's reduction over the model's split-K reduction,
+// fitted on GB300 against the tail split on and off for the 673 shapes of the
+// 2304 x N x 4096 sweep and 8192^3: with it, 250 shapes take the tail split
+// and measure faster (up to 20%), 6 take it and measure at most 1.1% slower.
+constexpr double kTailExtra = 1.0e-6;
+
+// Whole tiles for the W = tiles / slots full waves, then the T remaining
+// tiles in S K slices each (one more wave, T*S <= slots), whose partials a
+// reduction launch sums.  Same ingredients as estimate().
+double estimate_tail(int64_t M, int64_t N, int64_t K, int bn, int mode, int S, int sms, int c_es,
+                     bool beta, int raster_group, const Model& md) {
+  const bool pair = mode == dg::TC_PAIR;
+  const int tile_m = pair ? 2 * dg::TC_BM : dg::TC_BM;
+  const int slots = pair ? sms / 2 : sms;
+  const int64_t mb = ceil_div(M, tile_m), nb = ceil_div(N, bn), tiles = mb * nb;
+  const int64_t W = tiles / slots, T = tiles - W * slots;
+  const int64_t kb = ceil_div(K, dg::TC_BK), kbps = ceil_div(kb, S);
+  const int64_t group = std::max<int64_t>(1, std::min<int64_t>(raster_group, mb));
+  int64_t da = 0, db = 0;
+  distinct_panels(mb, nb, group, std::min<int64_t>(tiles, slots), &da, &db);
+  const int64_t streams = (da + db) * (pair ? 2 : 1);
+  const double rate = md.peak_flops / sms * tile_efficiency(bn);
+  const double t_mma_full = 2.0 * dg::TC_BM * bn * double(kb * dg::TC_BK) / rate;
+  const double t_mma_tail = 2.0 * dg::TC_BM * bn * double(kbps * dg::TC_BK) / rate;
+  const double row_bytes = double(dg::TC_BM + (pair ? bn / 2 : bn)) * dg::TC_BK * 2.0;
+  const double ub_full = row_bytes * double(kb), ub_tail = row_bytes * double(kbps);
+  const double unique = double(M * K + K * N) * 2.0;
+  const double waves = double(W + 1);
+  const double all_units = (double(W * slots) * ub_full + double(T * S) * ub_tail) * (pair ? 2 : 1);
+  const double reuse = (1.0 - 1.0 / waves) * std::max(0.0, 1.0 - unique / all_units);
+  const double feed = md.feed * (1.0 + md.reuse_gain * reuse);
+  const double makespan = double(W) * std::max(t_mma_full, ub_full / feed) +
+                          std::max(t_mma_tail, ub_tail / feed) + md.fixed + (pair ? kPairFixed : 0.0);
+  const double part = double(S) * double(T) * tile_m * bn * 4.0;
+  const double bytes = unique + double(M) * N * c_es * (beta ? 2.0 : 1.0) + part;
+  const double t_mem = bytes / std::min(md.stream_bw, md.panel_bw * double(streams));
+  return std::max(makespan, t_mem) + md.reduce + kTailExtra + part / md.hbm_bw;
+}
+
 int env_int(const char* name, int dflt) {
   const char* v = std::getenv(name);
   if (!v || !*v) return dflt;
@@ -253,6 +291,7 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
                gemm_config_info_t* out) {
   const Model md;
   int best_bn = 256, best_s = 1, best_mode = dg::TC_SOLO;
+  bool best_tail = false;  // split only the tiles of the last, partly filled wave
   double best_t = 1e300;
   int force_bn = 0;
   bool force_pair = false;
@@ -270,6 +309,11 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
   // GEMM_SPLITK_CLUSTER: 0 never reduces K halves on chip, 1 only does (where
   // a two-slice split on a K pair exists), unset lets the model choose.
   const int kpair_env = env_int("GEMM_SPLITK_CLUSTER", -1);
+  // GEMM_TAIL_SPLIT: 0 never splits only the tail wave; 1 only does (where a
+  // partly filled last wave exists), with the slices the planner picks; S >= 2
+  // only does, with S slices; unset lets the model choose.
+  const int tail_env = env_int("GEMM_TAIL_SPLIT", -1);
+  const bool only_tail = tail_env >= 1;
   const int raster = env_int("GEMM_RASTER_GROUP", 16);
   const int64_t kb = ceil_div(K, dg::TC_BK);
   // candidates: 128-row tiles of width 256/128/64 on one CTA, 256 x 256 on a
@@ -280,30 +324,62 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
   struct Cand { int bn; int mode; };
   const Cand cands[6] = {{256, dg::TC_PAIR}, {256, dg::TC_SOLO}, {128, dg::TC_SOLO}, {64, dg::TC_SOLO},
                          {256, dg::TC_KPAIR}, {128, dg::TC_KPAIR}};
+  // GEMM_PLAN_DEBUG=1 prints every candidate's estimate to stderr.
+  const bool debug = env_int("GEMM_PLAN_DEBUG", 0) != 0;
+  auto take = [&](double t, int bn, int mode, int s, bool tail) {
+    if (debug)
+      std::fprintf(stderr, "gemm plan %lldx%lldx%lld: bn %d mode %d split %d tail %d -> %.2f us\n",
+                   (long long)M, (long long)N, (long long)K, bn, mode, s, int(tail), t * 1e6);
+    // prefer earlier candidates / fewer slices unless clearly faster (2%)
+    if (t < best_t * 0.98) {
+      best_t = t;
+      best_bn = bn;
+      best_mode = mode;
+      best_s = s;
+      best_tail = tail;
+    }
+  };
   for (const Cand& c : cands) {
     const bool kpair = c.mode == dg::TC_KPAIR;
     if (force_bn && (c.bn != force_bn || (c.mode == dg::TC_PAIR) != force_pair)) continue;
     if (kpair ? kpair_env == 0 : kpair_env == 1) continue;
-    if (kpair && c.bn == 256 && force_bn != 256) continue;
+    if (kpair && (only_tail || (c.bn == 256 && force_bn != 256))) continue;
     // A K pair pays its exchange on every tile; it measured faster only where
     // the tiles fit one wave of clusters (then it replaces a reduction launch).
     if (kpair && kpair_env != 1 && ceil_div(M, dg::TC_BM) * ceil_div(N, c.bn) > sms / 2) continue;
     const int tile_m = c.mode == dg::TC_PAIR ? 2 * dg::TC_BM : dg::TC_BM;
     const int slots = c.mode == dg::TC_PAIR ? sms / 2 : sms;
     if (c.mode != dg::TC_SOLO && sms < 2) continue;
-    for (int s = kpair ? 2 : 1; s <= (kpair ? 2 : 64); ++s) {
+    const int64_t tiles = ceil_div(M, tile_m) * ceil_div(N, c.bn);
+    for (int s = kpair ? 2 : 1; s <= (kpair ? 2 : 64) && !only_tail; ++s) {
       if (force_s > 0 && s != force_s) continue;
       if (s > kb) break;
-      if (s > 1 && ceil_div(M, tile_m) * ceil_div(N, c.bn) * s > 4 * int64_t(slots)) break;
+      if (s > 1 && tiles * s > 4 * int64_t(slots)) break;
       int s_eff = 1;
       const double t = estimate(M, N, K, c.bn, c.mode, s, sms, c_es, beta, raster, md, &s_eff);
       if (s_eff != s) continue;
-      // prefer earlier candidates / fewer slices unless clearly faster (2%)
-      if (t < best_t * 0.98) {
-        best_t = t;
-        best_bn = c.bn;
-        best_mode = c.mode;
-        best_s = s;
+      take(t, c.bn, c.mode, s, false);
+    }
+    // Tail split: whole tiles for the full waves, the last wave's tiles in
+    // K slices that fill one more wave ("Matrix Multiplication Background
+    // User's Guide", section 3.2: the tail wave is what a tile choice alone
+    // cannot fill).
+    if (!kpair && tail_env != 0 && (force_s <= 0 || only_tail)) {
+      const int64_t W = tiles / slots, T = tiles - W * slots;
+      if (W >= 1 && T > 0) {
+        // slices: as many as fill the wave at most, fewer when the partials'
+        // traffic and reduction cost more than the shorter slices save
+        static const int kTry[] = {2, 3, 4, 6, 8, 12, 16, 24, 32, 48, 64};
+        for (int st0 : kTry) {
+          if (tail_env >= 2 && st0 != 2) break;
+          int64_t st = tail_env >= 2 ? tail_env : st0;
+          if (tail_env < 2 && st * T > slots) break;
+          st = std::min<int64_t>(st, kb);
+          if (st >= 2) st = ceil_div(kb, ceil_div(kb, st));  // no empty slice
+          if (st < 2) break;
+          const double t = estimate_tail(M, N, K, c.bn, c.mode, int(st), sms, c_es, beta, raster, md);
+          take(t, c.bn, c.mode, int(st), true);
+        }
       }
     }
   }
@@ -311,16 +387,31 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
     best_s = force_s > 0 ? int(std::min<int64_t>(force_s, kb)) : 1;
     best_bn = force_bn ? force_bn : 256;
     best_mode = force_pair ? dg::TC_PAIR : dg::TC_SOLO;
+    best_tail = false;
   }
   const int64_t kbps = ceil_div(kb, best_s);
   best_s = int(ceil_div(kb, kbps));
   const bool pair = best_mode == dg::TC_PAIR, kpair = best_mode == dg::TC_KPAIR;
   const int tile_m = pair ? 2 * dg::TC_BM : dg::TC_BM;
   const int pairs = sms / 2;
+  const int slots = pair ? pairs : sms;
   std::memset(out, 0, sizeof(*out));
-  quantization(M, N, tile_m, best_bn, best_s, pair ? pairs : sms, 1, out);
+  quantization(M, N, tile_m, best_bn, best_s, slots, 1, out);
   out->sms = sms;
-  out->path = kpair ? GEMM_PATH_TC_SPLITK_CLUSTER : (best_s > 1 ? GEMM_PATH_TC_SPLITK : GEMM_PATH_TC);
+  if (kpair) {
+    out->path = GEMM_PATH_TC_SPLITK_CLUSTER;
+  } else if (best_tail) {
+    out->path = GEMM_PATH_TC_TAIL_SPLIT;
+    out->tail_tiles = int32_t(out->tiles % slots);
+    out->units = (out->tiles - out->tail_tiles) + int64_t(out->tail_tiles) * best_s;
+    out->waves = double(out->units) / double(slots);
+    out->tail_fraction = double(out->units % slots) / double(slots);
+  } else if (best_s > 1) {
+    out->path = GEMM_PATH_TC_SPLITK;
+    out->tail_tiles = int32_t(out->tiles);
+  } else {
+    out->path = GEMM_PATH_TC;
+  }
   out->tile_k = dg::TC_BK;
   out->cta_per_tile = best_mode == dg::TC_SOLO ? 1 : 2;
   out->stages = dg::tc_stages(best_bn, best_mode);
@@ -332,7 +423,8 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
     out->grid = int(2 * std::min<int64_t>(out->tiles, pairs));
   else
     out->grid = int(std::min<int64_t>(out->units, sms));
-  out->launches = best_s > 1 && !kpair ? 2 : 1;
+  out->launches = out->tail_tiles > 0 ? 2 : 1;
+  out->workspace_bytes = int64_t(out->tail_tiles) * best_s * tile_m * best_bn * 4;
 }
 
 // ------------------------------------------------------------ tensor maps
@@ -492,7 +584,7 @@ int tc_mode(const gemm_config_info_t& info) {
 
 bool planner_overridden() {
   static const char* vars[] = {"GEMM_FORCE_TILE", "GEMM_FORCE_SPLITK", "GEMM_RASTER_GROUP",
-                               "GEMM_SPLITK_CLUSTER"};
+                               "GEMM_SPLITK_CLUSTER", "GEMM_TAIL_SPLIT"};
   for (const char* v : vars) {
     const char* x = std::getenv(v);
     if (x && *x) return true;
@@ -533,36 +625,34 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
   p.num_m_blocks = int(ceil_div(M, tile_m));
   p.num_n_blocks = int(ceil_div(N, bn));
   p.k_blocks = int(ceil_div(K, dg::TC_BK));
+  p.raster_group = info->raster_group;
+  // units: whole tiles first, then the K slices of the tail tiles (all tiles
+  // for split-K, the last wave's for a tail split, none otherwise)
+  const int64_t tiles = int64_t(p.num_m_blocks) * p.num_n_blocks;
+  const int tail = kpair ? 0 : info->tail_tiles;
+  p.dp_units = int(tiles - tail);
+  p.tail_tiles = tail;
   p.splitk = S;
   p.kb_per_split = int(ceil_div(p.k_blocks, S));
-  p.raster_group = info->raster_group;
-  p.units = int(kpair ? info->tiles : info->units);  // a K pair's cluster takes whole tiles
-  p.ws_rows = p.num_m_blocks * tile_m;
+  p.units = kpair ? int(tiles) : p.dp_units + tail * S;
+  p.out_kind = out_kind(dtype);
   p.a_mn_major = a_mn;
   p.b_mn_major = b_mn;
   p.idesc = make_idesc(f16, a_mn, b_mn, bn, tile_m);
   p.c_ptr = C;
   p.ldc = ldc;
   p.err = plan->err;
-  e->ws_ld = e->ws_slice = 0;
-  e->ws_bytes = 0;
+  // TMA stores write whole 16-byte pieces of a row: the map covers only the
+  // 16-byte-aligned prefix of each row of C; the kernel writes the rest.
+  p.n_tma = int((N * c_es) / 16 * 16 / c_es);
+  const CUtensorMapDataType ct = out_is_f32(dtype) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : in_t;
+  ok = ok && make_map(&e->mc, ct, c_es, C, std::max<int64_t>(p.n_tma, 1), M, ldc, 128 / c_es, 32);
+  e->mw = e->mc;  // replaced by the workspace map before a launch that has tail tiles
   e->ws_ptr = nullptr;
-  if (S == 1 || kpair) {
-    p.out_kind = out_kind(dtype);
-    // TMA stores write whole 16-byte pieces of a row: the map covers only the
-    // 16-byte-aligned prefix of each row of C; the kernel writes the rest.
-    p.n_tma = int((N * c_es) / 16 * 16 / c_es);
-    const CUtensorMapDataType ct = out_is_f32(dtype) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : in_t;
-    ok = ok && make_map(&e->mc, ct, c_es, C, std::max<int64_t>(p.n_tma, 1), M, ldc, 128 / c_es, 32);
-  } else {
-    p.out_kind = dg::OUT_PARTIAL;
-    p.n_tma = int(N);  // the workspace rows are padded to 16 bytes: no tail
-    e->ws_ld = (N + 3) & ~int64_t(3);
-    e->ws_slice = int64_t(p.ws_rows) * e->ws_ld;
-    e->ws_bytes = size_t(S) * size_t(e->ws_slice) * 4;
-    info->workspace_bytes = int64_t(e->ws_bytes);
-  }
-  info->launches = S > 1 && !kpair ? 2 : 1;
+  // fp32 partials, tile-major: [slice][tail tile][tile_m rows][bn columns]
+  e->ws_bytes = size_t(tail) * size_t(S) * size_t(tile_m) * size_t(bn) * 4;
+  info->workspace_bytes = int64_t(e->ws_bytes);
+  info->launches = tail > 0 ? 2 : 1;
   return ok ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -598,25 +688,39 @@ gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const voi
   p.slope = epi.slope;
   p.timeout_ns = plan->watchdog_ns;
   const int mode = tc_mode(e->info);
-  const int S = mode == dg::TC_KPAIR ? 1 : e->info.splitk;  // slices reduced by a second launch
-  if (S > 1) {
+  const int tail = e->p.tail_tiles;  // tiles whose K slices a second launch reduces
+  if (tail > 0) {
     const gemm_status_t st = ensure_ws(plan, e->ws_bytes, s);
     if (st != GEMM_OK) return st;
     if (e->ws_ptr != plan->ws) {  // (re-)encode the partial map for the current workspace
-      if (!make_map(&e->mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, plan->ws, N,
-                    int64_t(S) * e->p.ws_rows, e->ws_ld, 32, 32))
+      const int64_t rows = int64_t(e->p.splitk) * tail * e->info.tile_m;
+      if (!make_map(&e->mw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, plan->ws, e->info.tile_n, rows,
+                    e->info.tile_n, 32, 32))
         return GEMM_ERR_CUDA;
       e->ws_ptr = plan->ws;
     }
   }
   *info = e->info;
-  if (dg::launch_gemm_tc(e->info.tile_n, mode, e->ma, e->mb, e->mc, p, e->info.grid, s) != cudaSuccess)
+  if (dg::launch_gemm_tc(e->info.tile_n, mode, e->ma, e->mb, e->mc, e->mw, p, e->info.grid, s) !=
+      cudaSuccess)
     return GEMM_ERR_CUDA;
-  if (S > 1) {
-    const dg::EpiParams ep{alpha, beta, epi.slope, epi.act, out_kind(dtype)};
-    if (dg::launch_splitk_reduce(static_cast<const float*>(plan->ws), e->ws_ld, e->ws_slice, S, int(M),
-                                 int(N), C, ldc, ep, s, plan->sms) != cudaSuccess)
-      return GEMM_ERR_CUDA;
+  if (tail > 0) {
+    dg::TileReduceArgs r{};
+    r.ws = static_cast<const float*>(plan->ws);
+    r.tail_tiles = tail;
+    r.splits = e->p.splitk;
+    r.tile0 = e->p.dp_units;
+    r.tile_m = e->info.tile_m;
+    r.tile_n = e->info.tile_n;
+    r.num_m_blocks = e->p.num_m_blocks;
+    r.num_n_blocks = e->p.num_n_blocks;
+    r.raster_group = e->p.raster_group;
+    r.M = int(M);
+    r.N = int(N);
+    r.C = C;
+    r.ldc = ldc;
+    r.e = dg::EpiParams{alpha, beta, epi.slope, epi.act, out_kind(dtype)};
+    if (dg::launch_tile_reduce(r, s, plan->sms) != cudaSuccess) return GEMM_ERR_CUDA;
   }
   return GEMM_OK;
 }

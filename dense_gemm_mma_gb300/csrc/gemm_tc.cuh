@@ -35,10 +35,13 @@
 //    stay there; here the queue is explicit).  Units are ordered slice-major,
 //    then in groups of `raster_group` tile rows so that concurrently running
 //    tiles share A and B blocks in L2.
-//  - split-K: a unit may cover only a K slice; then the epilogue writes raw
-//    fp32 partials to the workspace and a separate kernel sums the slices in a
-//    fixed order ("Matrix Multiplication Background User's Guide", section 2.3:
-//    splitting along K needs a final reduction).
+//  - split-K: a unit may cover only a K slice of a tile; then the epilogue
+//    writes raw fp32 partials to the workspace and a separate kernel sums the
+//    slices in a fixed order ("Matrix Multiplication Background User's Guide",
+//    section 2.3: splitting along K needs a final reduction).  The split may
+//    cover every tile, or only the tiles of the last, partly filled wave: the
+//    first whole waves then run whole tiles, and the tail tiles' slices fill
+//    one more wave (section 3.2: a partial last wave leaves SMs idle).
 //  - K pair (TC_KPAIR): the same reduction done on chip for two slices.  A
 //    cluster of two CTAs takes one tile; CTA r runs the r-th half of the K
 //    loop into its own tensor memory.  In the epilogue each CTA sends its
@@ -95,24 +98,32 @@ struct TcCfg {
 
 struct Unit {
   int m_blk, n_blk, split, kb_begin, kb_end;
+  int ws_tile;   // tail tile index (partial units)
+  bool partial;  // a K slice of a tail tile: raw fp32 partials to the workspace
 };
 
-// Work unit u -> (tile, K slice).  Slice-major; inside a slice, groups of
-// raster_group tile rows, each group walked column by column.
+// Work unit u -> (tile, K range).  Units [0, dp_units) are whole tiles in
+// raster order; the rest are K slices of the tail tiles, slice-major.
 __device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
-  const int tiles = p.num_m_blocks * p.num_n_blocks;
   Unit x;
-  x.split = u / tiles;
-  const int t = u - x.split * tiles;
-  const int per_group = p.raster_group * p.num_n_blocks;
-  const int g = t / per_group;
-  const int first_m = g * p.raster_group;
-  const int rows_in_group = min(p.num_m_blocks - first_m, p.raster_group);
-  const int r = t - g * per_group;
-  x.m_blk = first_m + r % rows_in_group;
-  x.n_blk = r / rows_in_group;
-  x.kb_begin = x.split * p.kb_per_split;
-  x.kb_end = min(p.k_blocks, x.kb_begin + p.kb_per_split);
+  int t;
+  if (u < p.dp_units) {
+    t = u;
+    x.split = 0;
+    x.ws_tile = 0;
+    x.partial = false;
+    x.kb_begin = 0;
+    x.kb_end = p.k_blocks;
+  } else {
+    const int v = u - p.dp_units;
+    x.split = v / p.tail_tiles;
+    x.ws_tile = v - x.split * p.tail_tiles;
+    x.partial = true;
+    t = p.dp_units + x.ws_tile;
+    x.kb_begin = x.split * p.kb_per_split;
+    x.kb_end = min(p.k_blocks, x.kb_begin + p.kb_per_split);
+  }
+  tile_coords(t, p.num_m_blocks, p.num_n_blocks, p.raster_group, &x.m_blk, &x.n_blk);
   return x;
 }
 
@@ -166,7 +177,8 @@ __device__ __forceinline__ uint4 load_c16(const TcParams& p, int row, int col, i
 template <int BN, int MODE>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ TcParams p) {
+                   const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
+                   const __grid_constant__ TcParams p) {
   using Cfg = TcCfg<BN, MODE>;
   constexpr bool PAIR = Cfg::PAIR;
   constexpr bool KPAIR = Cfg::KPAIR;
@@ -212,6 +224,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
     prefetch_tmap(&tmC);
+    if (p.tail_tiles > 0) prefetch_tmap(&tmW);
   }
   if (warp == 1) {
     if constexpr (PAIR) {
@@ -544,10 +557,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int e = warp - 2;  // staging buffers / C-load barrier of this warp
     const int q = warp & 3;  // tensor-memory lane quarter this warp may read
-    const bool partial = p.out_kind == OUT_PARTIAL;
-    const bool has_beta = !partial && p.beta != 0.f;
-    const int esize = (p.out_kind == OUT_F32 || partial) ? 4 : 2;
-    const int cw = 128 / esize;  // columns per 128-byte box row
     const uint32_t stg0 = base + Cfg::OFF_STG + e * 2 * Cfg::STG_BYTES;
     uint8_t* const stg_p0 = sbase + Cfg::OFF_STG + e * 2 * Cfg::STG_BYTES;
     int acc = 0;
@@ -562,9 +571,18 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       if (!__all_sync(0xffffffffu, wait(tfull0 + 8 * acc, acc_phase, WAIT_EPI_TMEM_FULL)))
         break;
       tc_fence_after();
-      const int n0 = x.n_blk * BN;
-      const int row0 = x.m_blk * Cfg::TILE_M + int(rank) * TC_BM + 32 * q;
-      const int y0 = partial ? x.split * p.ws_rows + row0 : row0;
+      // A partial unit stores raw fp32 sums into its slice's copy of the tile
+      // in the workspace (BN columns wide, no ragged edge); a whole tile
+      // stores the epilogue's result into C.
+      const bool partial = x.partial;
+      const bool has_beta = !partial && p.beta != 0.f;
+      const int esize = (partial || p.out_kind == OUT_F32) ? 4 : 2;
+      const int cw = 128 / esize;  // columns per 128-byte box row
+      const CUtensorMap* const out_map = partial ? &tmW : &tmC;
+      const int n0 = partial ? 0 : x.n_blk * BN;
+      const int row0 = x.m_blk * Cfg::TILE_M + int(rank) * TC_BM + 32 * q;  // rows of C
+      const int y0 = partial ? (x.split * p.tail_tiles + x.ws_tile) * Cfg::TILE_M + int(rank) * TC_BM + 32 * q
+                             : row0;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc * BN);
       const int chunks = BN / cw;
@@ -574,9 +592,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int x0 = n0 + c * cw;
         // A TMA store writes whole 16-byte pieces of a row, so columns past the
         // last 16-byte boundary inside C, [n_tma, N), are written by the threads.
-        const bool tma_cols = x0 < p.n_tma;
+        const bool tma_cols = partial || x0 < p.n_tma;
         const int tail_lo = max(x0, p.n_tma), tail_hi = min(x0 + cw, p.N);
-        const int row = y0 + lane;
+        const int row = row0 + lane;
         const bool has_tail = !partial && tail_lo < tail_hi && row < p.M;
         if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
         __syncwarp();
@@ -664,7 +682,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          if (tma_cols) tma_store_2d(&tmC, stg, x0, y0);
+          if (tma_cols) tma_store_2d(out_map, stg, x0, y0);
           bulk_commit();  // one group per chunk (possibly empty) keeps the buffer accounting exact
         }
         sbuf ^= 1;
@@ -706,7 +724,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
 
 template <int BN, int MODE>
 cudaError_t launch_gemm_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                              const TcParams& p, int grid, cudaStream_t s) {
+                              const CUtensorMap& ws, const TcParams& p, int grid, cudaStream_t s) {
   constexpr int smem = TcCfg<BN, MODE>::SMEM_BYTES;
   auto kern = gemm_tc_kernel<BN, MODE>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -723,7 +741,7 @@ cudaError_t launch_gemm_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const 
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = MODE != TC_SOLO ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kern, a, b, c, p);
+  return cudaLaunchKernelEx(&cfg, kern, a, b, c, ws, p);
 }
 
 // Clusters of two that can be resident at once (the grid of a cluster kernel

@@ -5,7 +5,7 @@
 namespace dg {
 #define DG_INST(MODE)                                                                              \
   template cudaError_t launch_gemm_tc_bn<128, MODE>(const CUtensorMap&, const CUtensorMap&,        \
-                                                   const CUtensorMap&, const TcParams&, int, cudaStream_t);
+                                                   const CUtensorMap&, const CUtensorMap&, const TcParams&, int, cudaStream_t);
 DG_INST(TC_SOLO)
 DG_INST(TC_PAIR)
 DG_INST(TC_KPAIR)

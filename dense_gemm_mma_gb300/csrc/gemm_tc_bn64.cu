@@ -3,5 +3,5 @@
 
 namespace dg {
 template cudaError_t launch_gemm_tc_bn<64, TC_SOLO>(const CUtensorMap&, const CUtensorMap&,
-                                                   const CUtensorMap&, const TcParams&, int, cudaStream_t);
+                                                   const CUtensorMap&, const CUtensorMap&, const TcParams&, int, cudaStream_t);
 }  // namespace dg

@@ -5,8 +5,8 @@ namespace dg {
 
 #define DG_EXTERN(BN, MODE)                                                                        \
   extern template cudaError_t launch_gemm_tc_bn<BN, MODE>(const CUtensorMap&, const CUtensorMap&, \
-                                                          const CUtensorMap&, const TcParams&, int, \
-                                                          cudaStream_t);
+                                                          const CUtensorMap&, const CUtensorMap&, \
+                                                          const TcParams&, int, cudaStream_t);
 DG_EXTERN(64, TC_SOLO)
 DG_EXTERN(128, TC_SOLO)
 DG_EXTERN(256, TC_SOLO)
@@ -50,21 +50,22 @@ int tc_max_clusters(int bn, int mode) {
 }
 
 cudaError_t launch_gemm_tc(int bn, int mode, const CUtensorMap& a, const CUtensorMap& b,
-                           const CUtensorMap& c, const TcParams& p, int grid, cudaStream_t s) {
+                           const CUtensorMap& c, const CUtensorMap& ws, const TcParams& p, int grid,
+                           cudaStream_t s) {
   if (mode == TC_PAIR) {
-    if (bn == 256) return launch_gemm_tc_bn<256, TC_PAIR>(a, b, c, p, grid, s);
-    if (bn == 128) return launch_gemm_tc_bn<128, TC_PAIR>(a, b, c, p, grid, s);
+    if (bn == 256) return launch_gemm_tc_bn<256, TC_PAIR>(a, b, c, ws, p, grid, s);
+    if (bn == 128) return launch_gemm_tc_bn<128, TC_PAIR>(a, b, c, ws, p, grid, s);
     return cudaErrorInvalidValue;
   }
   if (mode == TC_KPAIR) {
-    if (bn == 256) return launch_gemm_tc_bn<256, TC_KPAIR>(a, b, c, p, grid, s);
-    if (bn == 128) return launch_gemm_tc_bn<128, TC_KPAIR>(a, b, c, p, grid, s);
+    if (bn == 256) return launch_gemm_tc_bn<256, TC_KPAIR>(a, b, c, ws, p, grid, s);
+    if (bn == 128) return launch_gemm_tc_bn<128, TC_KPAIR>(a, b, c, ws, p, grid, s);
     return cudaErrorInvalidValue;
   }
   switch (bn) {
-    case 64: return launch_gemm_tc_bn<64, TC_SOLO>(a, b, c, p, grid, s);
-    case 128: return launch_gemm_tc_bn<128, TC_SOLO>(a, b, c, p, grid, s);
-    case 256: return launch_gemm_tc_bn<256, TC_SOLO>(a, b, c, p, grid, s);
+    case 64: return launch_gemm_tc_bn<64, TC_SOLO>(a, b, c, ws, p, grid, s);
+    case 128: return launch_gemm_tc_bn<128, TC_SOLO>(a, b, c, ws, p, grid, s);
+    case 256: return launch_gemm_tc_bn<256, TC_SOLO>(a, b, c, ws, p, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

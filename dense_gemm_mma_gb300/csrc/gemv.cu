@@ -319,32 +319,42 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvArgs g) {
 }
 
 // ------------------------------------------------------------ split-K reduce
-// One thread per 4 adjacent columns of a row: sums the slices s = 0..S-1 in
-// order (16-byte loads; the workspace row stride is a multiple of 4 floats),
-// applies the epilogue and stores 4 outputs.
-__global__ void __launch_bounds__(256)
-    splitk_reduce_kernel(const float* __restrict__ ws, int64_t ws_ld, int64_t ws_slice, int splits,
-                         int M, int N, void* C, int64_t ldc, const EpiParams e) {
+// One thread per 4 adjacent columns of a row of a tail tile: sums the tile's
+// slices s = 0..S-1 in order (16-byte loads from the tile-major workspace),
+// applies the epilogue and stores the outputs that lie inside C.
+__global__ void __launch_bounds__(256) tile_reduce_kernel(const TileReduceArgs a) {
   // Launched as a programmatic dependent of the GEMM that writes the partials:
   // this CTA may start before that grid ends, so wait for its results here.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int gpr = (N + 3) >> 2;
-  const int64_t total = static_cast<int64_t>(M) * gpr;
+  const EpiParams& e = a.e;
+  const int gpr = a.tile_n >> 2;
+  const int64_t per_tile = static_cast<int64_t>(a.tile_m) * gpr;
+  const int64_t total = per_tile * a.tail_tiles;
+  const int64_t slice = static_cast<int64_t>(a.tail_tiles) * a.tile_m * a.tile_n;
+  void* const C = a.C;
+  const int N = a.N;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int m = static_cast<int>(i / gpr);
-    const int n = static_cast<int>(i - static_cast<int64_t>(m) * gpr) * 4;
-    const float* src = ws + static_cast<int64_t>(m) * ws_ld + n;
+    const int t = static_cast<int>(i / per_tile);
+    const int rem = static_cast<int>(i - static_cast<int64_t>(t) * per_tile);
+    const int r = rem / gpr;
+    const int c4 = rem - r * gpr;
+    int m_blk, n_blk;
+    tile_coords(a.tile0 + t, a.num_m_blocks, a.num_n_blocks, a.raster_group, &m_blk, &n_blk);
+    const int m = m_blk * a.tile_m + r;
+    const int n = n_blk * a.tile_n + c4 * 4;
+    if (m >= a.M || n >= N) continue;
+    const float* src = a.ws + (static_cast<int64_t>(t) * a.tile_m + r) * a.tile_n + c4 * 4;
     float4 s = __ldcs(reinterpret_cast<const float4*>(src));
-    for (int sp = 1; sp < splits; ++sp) {
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(src + sp * ws_slice));
+    for (int sp = 1; sp < a.splits; ++sp) {
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(src + sp * slice));
       s.x += v.x;
       s.y += v.y;
       s.z += v.z;
       s.w += v.w;
     }
     float sv[4] = {s.x, s.y, s.z, s.w};
-    const int64_t base = static_cast<int64_t>(m) * ldc + n;
+    const int64_t base = static_cast<int64_t>(m) * a.ldc + n;
     const int nn = min(4, N - n);
     const int esz = e.out_kind == OUT_F32 ? 4 : 2;
     const bool vec = nn == 4 && ((reinterpret_cast<uintptr_t>(C) + base * esz) & (4 * esz - 1)) == 0;
@@ -485,10 +495,8 @@ cudaError_t launch_gemv_generic(const GemvArgs& g, cudaStream_t s, int sms) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_splitk_reduce(const float* ws, int64_t ws_ld, int64_t ws_slice, int splits,
-                                 int M, int N, void* C, int64_t ldc, EpiParams e, cudaStream_t s,
-                                 int sms) {
-  const int64_t items = static_cast<int64_t>(M) * ((N + 3) / 4);
+cudaError_t launch_tile_reduce(const TileReduceArgs& a, cudaStream_t s, int sms) {
+  const int64_t items = static_cast<int64_t>(a.tail_tiles) * a.tile_m * (a.tile_n / 4);
   // Programmatic dependent launch: the reduction's launch overlaps the tail of
   // the GEMM; its griddepcontrol.wait orders it after the GEMM's writes.
   cudaLaunchConfig_t cfg = {};
@@ -503,7 +511,7 @@ cudaError_t launch_splitk_reduce(const float* ws, int64_t ws_ld, int64_t ws_slic
   cfg.numAttrs = 1;
   if (const char* v = std::getenv("GEMM_PDL"))  // GEMM_PDL=0: ordinary launch, for comparison
     if (v[0] == '0') cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, ws, ws_ld, ws_slice, splits, M, N, C, ldc, e);
+  return cudaLaunchKernelEx(&cfg, tile_reduce_kernel, a);
 }
 
 cudaError_t launch_scale(int M, int N, void* C, int64_t ldc, EpiParams e, cudaStream_t s, int sms) {

@@ -12,8 +12,7 @@ namespace dg {
 enum OutKind : int {
   OUT_F32 = 0,
   OUT_BF16 = 1,
-  OUT_F16 = 2,
-  OUT_PARTIAL = 3  // raw fp32 partial sums of one K slice into the workspace
+  OUT_F16 = 2
 };
 
 // Codes OR-ed into the plan's error word by a wait that ran out.
@@ -42,16 +41,37 @@ constexpr int TC_BK = 64;        // K elements per stage: 64 x 2 B = one 128-B s
 constexpr int TC_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int TC_EPI_WARPS = 4;
 
+// Output tile t (raster order) -> (m_blk, n_blk): groups of `group` tile rows,
+// each group walked column by column, so that tiles running at the same time
+// share A row-panels and B column-panels in L2.
+__host__ __device__ inline void tile_coords(int t, int num_m_blocks, int num_n_blocks, int group,
+                                            int* m_blk, int* n_blk) {
+  const int per_group = group * num_n_blocks;
+  const int g = t / per_group;
+  const int first_m = g * group;
+  const int rows = num_m_blocks - first_m < group ? num_m_blocks - first_m : group;
+  const int r = t - g * per_group;
+  *m_blk = first_m + r % rows;
+  *n_blk = r / rows;
+}
+
 struct TcParams {
   int M, N, K;
   int num_m_blocks, num_n_blocks;
   int k_blocks;      // ceil(K / TC_BK)
-  int splitk;        // K slices (1 = plain GEMM)
-  int kb_per_split;  // k-blocks per slice (the last one may be shorter)
   int raster_group;  // output-tile rows per rasterisation group
-  int units;         // num_m_blocks * num_n_blocks * splitk
-  int ws_rows;       // workspace rows per slice (num_m_blocks * TC_BM), OUT_PARTIAL only
-  int out_kind;      // OutKind
+  // Work units, in this order: dp_units whole tiles (raster positions
+  // 0 .. dp_units-1, all of K, final output); then `splitk` K slices of each of
+  // the tail_tiles remaining tiles, slice-major, written as raw fp32 partial
+  // sums to the workspace, tile-major [slice][tail tile][TILE_M rows][BN
+  // columns], and summed in slice order by the tile reduction kernel.  Plain
+  // split-K is dp_units = 0; no split is tail_tiles = 0.
+  int dp_units;
+  int tail_tiles;
+  int splitk;        // K slices of a tail tile
+  int kb_per_split;  // k-blocks per slice (the last one may be shorter); a K pair: per half
+  int units;         // dp_units + tail_tiles * splitk (a K pair: tiles)
+  int out_kind;      // OutKind of C
   int n_tma;         // columns [0, n_tma) of C go through TMA (a 16-byte multiple per row)
   void* c_ptr;       // C, for the columns [n_tma, N) written directly
   int64_t ldc;
@@ -72,9 +92,14 @@ int tc_stages(int bn, int mode);
 int tc_max_clusters(int bn, int mode);
 
 // TC_KPAIR: p.units counts tiles (one per cluster), p.kb_per_split is half the
-// k-blocks (rounded up), the output kind is final (not OUT_PARTIAL).
+// k-blocks (rounded up), and no unit is a tail slice (tail_tiles = 0).
+// c: C (box 32 rows x 128 bytes); ws: the fp32 partial workspace (box 32 x 32),
+// used only when p.tail_tiles > 0.
 cudaError_t launch_gemm_tc(int bn, int mode, const CUtensorMap& a, const CUtensorMap& b,
-                           const CUtensorMap& c, const TcParams& p, int grid, cudaStream_t s);
+                           const CUtensorMap& c, const CUtensorMap& ws, const TcParams& p, int grid,
+                           cudaStream_t s);
+
+
 
 struct EpiParams {
   float alpha, beta, slope;
@@ -82,10 +107,20 @@ struct EpiParams {
   int out_kind;  // OUT_F32 / OUT_BF16 / OUT_F16
 };
 
-// Fixed-order sum of `splits` fp32 partial slices, then the epilogue into C.
-cudaError_t launch_splitk_reduce(const float* ws, int64_t ws_ld, int64_t ws_slice, int splits,
-                                 int M, int N, void* C, int64_t ldc, EpiParams e,
-                                 cudaStream_t s, int sms);
+// Fixed-order sum of the K slices of the tail tiles of a tensor-core call
+// (workspace layout: see TcParams), then the epilogue into C.
+struct TileReduceArgs {
+  const float* ws;
+  int tail_tiles, splits;
+  int tile0;  // raster position of the first tail tile (= dp_units)
+  int tile_m, tile_n;
+  int num_m_blocks, num_n_blocks, raster_group;
+  int M, N;
+  void* C;
+  int64_t ldc;
+  EpiParams e;
+};
+cudaError_t launch_tile_reduce(const TileReduceArgs& a, cudaStream_t s, int sms);
 
 // C <- act(beta * C) (K == 0 or alpha == 0).
 cudaError_t launch_scale(int M, int N, void* C, int64_t ldc, EpiParams e, cudaStream_t s,

@@ -27,7 +27,7 @@ GEMM_BF16_F32, GEMM_BF16_BF16, GEMM_F16_F32, GEMM_F16_F16 = 0, 1, 2, 3
 GEMM_ACT_NONE, GEMM_ACT_LEAKY_RELU = 0, 1
 
 PATH_NAMES = {0: "none", 1: "tc", 2: "tc_splitk", 3: "gemv_rowdot", 4: "gemv_colstream",
-              5: "gemv_generic", 6: "scale", 7: "tc_splitk_cluster"}
+              5: "gemv_generic", 6: "scale", 7: "tc_splitk_cluster", 8: "tc_tail_split"}
 
 DTYPES = {("bf16", "f32"): GEMM_BF16_F32, ("bf16", "bf16"): GEMM_BF16_BF16,
           ("f16", "f32"): GEMM_F16_F32, ("f16", "f16"): GEMM_F16_F16}
@@ -45,11 +45,11 @@ class gemm_config_info_t(ctypes.Structure):
         ("sms", ctypes.c_int32), ("tiles", ctypes.c_int64), ("units", ctypes.c_int64),
         ("waves", ctypes.c_double), ("tail_fraction", ctypes.c_double),
         ("useful_fraction", ctypes.c_double), ("launches", ctypes.c_int32),
-        ("reserved", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
+        ("tail_tiles", ctypes.c_int32), ("workspace_bytes", ctypes.c_int64),
     ]
 
     def as_dict(self) -> dict:
-        d = {name: getattr(self, name) for name, _ in self._fields_ if name != "reserved"}
+        d = {name: getattr(self, name) for name, _ in self._fields_}
         d["path"] = PATH_NAMES.get(self.path, str(self.path))
         return d
 

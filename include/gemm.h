@@ -88,9 +88,12 @@ typedef enum {
   GEMM_PATH_GEMV_COLSTREAM = 4,/* GEMV: threads own 8 contiguous columns, K split       */
   GEMM_PATH_GEMV_GENERIC = 5,  /* GEMV with strided operands (no 128-bit loads)          */
   GEMM_PATH_SCALE = 6,         /* K == 0 or alpha == 0: C <- act(beta*C)                 */
-  GEMM_PATH_TC_SPLITK_CLUSTER = 7 /* tcgen05 GEMM, K in two halves on a cluster of two CTAs
+  GEMM_PATH_TC_SPLITK_CLUSTER = 7, /* tcgen05 GEMM, K in two halves on a cluster of two CTAs
                                   whose partial sums are added on chip: one launch, no
                                   workspace (the reduction of section 2.3 done in place) */
+  GEMM_PATH_TC_TAIL_SPLIT = 8  /* tcgen05 GEMM: whole tiles for the full waves; only the
+                                  tiles of the last, partly filled wave are split along K
+                                  (section 3.2's tail wave), + reduction of those tiles  */
 } gemm_path_t;
 
 /* Plan decisions and the tile/wave quantization they imply ("Matrix
@@ -109,13 +112,15 @@ typedef struct {
   int32_t grid;            /* CTAs launched for the main kernel                        */
   int32_t sms;             /* streaming multiprocessors used for the wave size         */
   int64_t tiles;           /* output tiles = ceil(M/tile_m) * ceil(N/tile_n)           */
-  int64_t units;           /* work units = tiles * splitk (CTA-sized: a 256-row pair   */
-                           /* tile is one unit of two CTAs)                            */
+  int64_t units;           /* work units = tiles - tail_tiles + tail_tiles * splitk    */
+                           /* (a 256-row pair tile is one unit of two CTAs; a K pair  */
+                           /* tile is two units, its halves)                          */
   double waves;            /* units / wave size                                        */
   double tail_fraction;    /* (units mod wave) / wave: SMs busy in the last wave, 0=full */
   double useful_fraction;  /* M*N / (tiles*tile_m*tile_n): share of tile area in C     */
   int32_t launches;        /* kernels the call launched                                */
-  int32_t reserved;
+  int32_t tail_tiles;      /* tiles split along K and reduced by a second launch:      */
+                           /* all tiles (split-K), the last wave's (tail split) or 0   */
   int64_t workspace_bytes; /* plan workspace the call used                             */
 } gemm_config_info_t;
 

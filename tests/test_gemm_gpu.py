@@ -219,6 +219,41 @@ def test_kpair_plan_cache_and_watchdog_clear(plan):
     assert plan.poll_error() == 0
 
 
+# ------------------------------------------------ tail-wave split (hybrid)
+
+@pytest.mark.parametrize("tile,shape", [("128x64", (1300, 1000, 300)), ("128x128", (1300, 2000, 333)),
+                                        ("128x256", (2600, 2000, 330)), ("256x256", (2600, 2000, 260))])
+def test_tail_split_ragged(plan, tile, shape):
+    """More tiles than one wave, the last wave partly filled: whole tiles for
+    the first wave, K slices for the rest, reduced by the tile reduction."""
+    r = run_case(plan, *shape, env={"GEMM_TAIL_SPLIT": "3", "GEMM_FORCE_TILE": tile}, seed=80 + len(tile))
+    i = r.info
+    assert i["path"] == "tc_tail_split" and i["splitk"] == 3 and 0 < i["tail_tiles"] < i["tiles"]
+    assert i["units"] == i["tiles"] - i["tail_tiles"] + 3 * i["tail_tiles"] and i["launches"] == 2
+
+
+@pytest.mark.parametrize("out_fmt", ["f32", "bf16", "f16"])
+def test_tail_split_epilogues_and_transposes(plan, out_fmt):
+    in_fmt = "f16" if out_fmt == "f16" else "bf16"
+    env = {"GEMM_TAIL_SPLIT": "2", "GEMM_FORCE_TILE": "128x128"}
+    run_case(plan, 1290, 2003, 515, in_fmt=in_fmt, out_fmt=out_fmt, beta=0.5, act=1, slope=0.1,
+             ta=True, env=env, seed=82, pad=(8, 0, 8))
+    run_case(plan, 1301, 1930, 200, in_fmt=in_fmt, out_fmt=out_fmt, alpha=-1.5, tb=True, env=env, seed=83)
+
+
+def test_tail_split_deterministic_and_pair(plan):
+    r = run_case(plan, 2600, 2000, 640, env={"GEMM_TAIL_SPLIT": "5", "GEMM_FORCE_TILE": "256x256"},
+                 repeat=2, seed=84, beta=1.0, out_fmt="bf16")
+    assert r.info["path"] == "tc_tail_split" and r.info["cta_per_tile"] == 2
+    assert np.array_equal(r.outputs[0].view(np.uint8), r.outputs[1].view(np.uint8))
+
+
+def test_tail_split_planner_choice_wave_shape(plan):
+    """2304 x 2176 x 4096 fp16: 81 pair tiles on 76 pairs; the planner splits the 5 tail tiles."""
+    r = run_case(plan, 2304, 2176, 4096, in_fmt="f16", sample=4096, seed=1238)
+    assert r.info["path"] == "tc_tail_split" and r.info["tail_tiles"] == 5
+
+
 def test_splitk_ragged_with_beta(plan):
     r = run_case(plan, 200, 150, 3000, out_fmt="bf16", beta=0.5, act=1, slope=0.1,
                  env={"GEMM_FORCE_SPLITK": "5", "GEMM_FORCE_TILE": "128x64"}, seed=61)
@@ -333,7 +368,7 @@ def test_full_config2_skinny_both_b_layouts(plan):
 
 def test_full_config3_square_bf16_out(plan):
     r = run_case(plan, 8192, 8192, 8192, out_fmt="bf16", seed=1236, sample=SAMPLE)
-    assert r.info["path"] == "tc" and r.info["cta_per_tile"] == 2
+    assert r.info["path"] in ("tc", "tc_tail_split") and r.info["cta_per_tile"] == 2
 
 
 def test_full_config3_beta_leaky_relu(plan):

@@ -195,26 +195,37 @@ def test_roofline_bound():
 def test_planner_invariants(M, N, K):
     for sms in (108, 148, 152):
         c = g.gemm_choose_config(M, N, K, g.GEMM_BF16_F32, 0, 0, sms)
-        assert c.path in (1, 2, 7)
+        assert c.path in (1, 2, 7, 8)
         assert (c.tile_m, c.cta_per_tile) in ((128, 1), (256, 2), (128, 2))
         assert (c.tile_m, c.cta_per_tile) != (128, 2) or (c.path == 7 and c.splitk == 2)
         assert c.tile_n in (64, 128, 256) and c.tile_k == 64
         assert 1 <= c.grid <= sms and c.grid <= c.units * c.cta_per_tile
         assert c.grid % c.cta_per_tile == 0
-        assert c.units == c.tiles * c.splitk
+        slots = sms // 2 if c.tile_m == 256 else sms
+        if c.path == 8:       # whole tiles for the full waves, K slices for the last wave's tiles
+            assert 0 < c.tail_tiles < slots and c.tiles >= slots
+            assert c.tail_tiles == c.tiles % slots
+            assert c.units == c.tiles - c.tail_tiles + c.tail_tiles * c.splitk
+            assert c.tail_tiles * c.splitk <= slots
+        elif c.path == 2:     # every tile split
+            assert c.tail_tiles == c.tiles and c.units == c.tiles * c.splitk
+        else:
+            assert c.tail_tiles == 0 and c.units == c.tiles * c.splitk
         kb = -(-K // 64)
         assert 1 <= c.splitk <= kb
         per = -(-kb // c.splitk)
         assert -(-kb // per) == c.splitk                  # no empty K slice
-        assert (c.path in (2, 7)) == (c.splitk > 1)
-        assert c.launches == (2 if c.path == 2 else 1)
+        assert (c.path in (2, 7, 8)) == (c.splitk > 1)
+        assert c.launches == (2 if c.path in (2, 8) else 1)
+        assert c.workspace_bytes == c.tail_tiles * c.splitk * c.tile_m * c.tile_n * 4
 
 
 def test_planner_splits_small_output_with_long_k():
     c = g.gemm_choose_config(256, 256, 65536, g.GEMM_F16_F32, 0, 0, 152)
     assert c.splitk > 1 and c.units >= 64
     big = g.gemm_choose_config(8192, 8192, 8192, g.GEMM_BF16_BF16, 0, 0, 152)
-    assert big.splitk == 1 and big.tile_n == 256 and big.tile_m == 256 and big.cta_per_tile == 2
+    assert big.tile_n == 256 and big.tile_m == 256 and big.cta_per_tile == 2
+    assert big.path in (1, 8) and (big.path == 1) == (big.splitk == 1)
 
 
 def test_planner_gemv_paths():
@@ -248,6 +259,23 @@ def test_planner_kpair_switch(monkeypatch):
     monkeypatch.setenv("GEMM_SPLITK_CLUSTER", "1")
     c = g.gemm_choose_config(1024, 1024, 64, 0, 0, 0, 152)
     assert c.path in (1, 2) and c.splitk == 1
+
+
+def test_planner_tail_split(monkeypatch):
+    """Config 5's second-wave shapes: 2304 x 2176 x 4096 has 81 tiles of
+    256 x 256 for 76 CTA pairs, so 5 tiles would run alone in a second wave;
+    the tail split runs 76 whole tiles and splits the 5 along K."""
+    c = g.gemm_choose_config(2304, 2176, 4096, g.GEMM_F16_F32, 0, 0, 152)
+    assert g.PATH_NAMES[c.path] == "tc_tail_split" and c.tiles == 81 and c.tail_tiles == 5
+    assert c.units == 76 + 5 * c.splitk and c.launches == 2
+    # a full last wave has no tail to split
+    assert g.gemm_choose_config(2304, 1984, 4096, g.GEMM_F16_F32, 0, 0, 152).path == 1
+    monkeypatch.setenv("GEMM_TAIL_SPLIT", "0")
+    assert g.gemm_choose_config(2304, 2176, 4096, g.GEMM_F16_F32, 0, 0, 152).path != 8
+    monkeypatch.setenv("GEMM_TAIL_SPLIT", "3")
+    monkeypatch.setenv("GEMM_FORCE_TILE", "128x128")
+    c = g.gemm_choose_config(300, 2000, 1000, g.GEMM_F16_F32, 0, 0, 20)
+    assert c.path == 8 and c.splitk == 3 and c.tiles == 3 * 16 and c.tail_tiles == 48 % 20
 
 
 def test_planner_env_overrides(monkeypatch):
