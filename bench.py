@@ -304,6 +304,9 @@ def main():
     ap.add_argument("--ref-fraction", type=float, default=1.0 / 512)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--autotune", action="store_true",
+                    help="benchmark mode: time the planner's leading candidates once per shape "
+                         "(during warm-up) and keep the fastest")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3  # at least three warm-up steps
@@ -324,6 +327,8 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     plan = gemm.Plan(local)
+    if args.autotune:
+        gemm.gemm_plan_set_autotune(plan.handle, True)
     stream = torch.cuda.current_stream(dev)
     sptr = stream.cuda_stream
 
@@ -515,6 +520,8 @@ def main():
                              "device buffers no other call of the step touches"
                              + ("" if not any(c.group for c in calls) else
                                 " (except the calls of one sweep, which share A and B)"),
+                       "planner": "benchmark mode (timed once per shape in warm-up)" if args.autotune
+                                  else "cost model",
                        "step_bytes": step_bytes, "step_flops": step_flops,
                        "step_tflops": round(ws * args.steps * step_flops / (total_ms / 1e3) / 1e12, 2),
                        "input_generation_s": round(gen_s, 1)},

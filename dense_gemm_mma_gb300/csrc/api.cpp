@@ -44,6 +44,14 @@ struct TcKeyHash {
   }
 };
 
+// One tensor-core plan: tile width, kernel variant, K slices, and whether
+// only the tail wave's tiles are split.
+struct TcChoice {
+  int bn = 256, mode = dg::TC_SOLO, s = 1;
+  bool tail = false;
+  double t = 1e300;  // estimated seconds
+};
+
 // Planner decision, encoded tensor maps and kernel parameters of one call.
 struct TcEntry {
   gemm_config_info_t info;
@@ -69,6 +77,9 @@ struct gemm_plan {
   // descriptor encoding (host time that would otherwise sit in front of the
   // kernels on the stream).
   std::unordered_map<TcKey, TcEntry, TcKeyHash> tc_cache;
+  // Benchmark mode: the fastest measured choice per shape (key without pointers).
+  bool autotune = false;
+  std::unordered_map<TcKey, TcChoice, TcKeyHash> tuned;
 };
 
 namespace {
@@ -287,12 +298,12 @@ int env_int(const char* name, int dflt) {
   return std::atoi(v);
 }
 
-void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
-               gemm_config_info_t* out) {
+// Every candidate the planner estimates, in the order it considers them
+// (best estimate first after sorting); `best` is the planner's pick.
+void tc_candidates(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta, TcChoice* best,
+                   std::vector<TcChoice>* all) {
   const Model md;
-  int best_bn = 256, best_s = 1, best_mode = dg::TC_SOLO;
-  bool best_tail = false;  // split only the tiles of the last, partly filled wave
-  double best_t = 1e300;
+  TcChoice pick;
   int force_bn = 0;
   bool force_pair = false;
   if (const char* f = std::getenv("GEMM_FORCE_TILE")) {
@@ -316,6 +327,8 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
   const bool only_tail = tail_env >= 1;
   const int raster = env_int("GEMM_RASTER_GROUP", 16);
   const int64_t kb = ceil_div(K, dg::TC_BK);
+  // GEMM_PLAN_DEBUG=1 prints every candidate's estimate to stderr.
+  const bool debug = env_int("GEMM_PLAN_DEBUG", 0) != 0;
   // candidates: 128-row tiles of width 256/128/64 on one CTA, 256 x 256 on a
   // CTA pair, 128 x 128 with K halves on a K pair.  The 128 x 256 K pair
   // (two exchange rounds, and a third of each ring stage for A instead of
@@ -324,20 +337,19 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
   struct Cand { int bn; int mode; };
   const Cand cands[6] = {{256, dg::TC_PAIR}, {256, dg::TC_SOLO}, {128, dg::TC_SOLO}, {64, dg::TC_SOLO},
                          {256, dg::TC_KPAIR}, {128, dg::TC_KPAIR}};
-  // GEMM_PLAN_DEBUG=1 prints every candidate's estimate to stderr.
-  const bool debug = env_int("GEMM_PLAN_DEBUG", 0) != 0;
   auto take = [&](double t, int bn, int mode, int s, bool tail) {
     if (debug)
       std::fprintf(stderr, "gemm plan %lldx%lldx%lld: bn %d mode %d split %d tail %d -> %.2f us\n",
                    (long long)M, (long long)N, (long long)K, bn, mode, s, int(tail), t * 1e6);
+    TcChoice c;
+    c.bn = bn;
+    c.mode = mode;
+    c.s = s;
+    c.tail = tail;
+    c.t = t;
+    if (all) all->push_back(c);
     // prefer earlier candidates / fewer slices unless clearly faster (2%)
-    if (t < best_t * 0.98) {
-      best_t = t;
-      best_bn = bn;
-      best_mode = mode;
-      best_s = s;
-      best_tail = tail;
-    }
+    if (t < pick.t * 0.98) pick = c;
   };
   for (const Cand& c : cands) {
     const bool kpair = c.mode == dg::TC_KPAIR;
@@ -383,24 +395,29 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
       }
     }
   }
-  if (best_t == 1e300) {  // forced choices not reachable exactly: take the nearest valid
-    best_s = force_s > 0 ? int(std::min<int64_t>(force_s, kb)) : 1;
-    best_bn = force_bn ? force_bn : 256;
-    best_mode = force_pair ? dg::TC_PAIR : dg::TC_SOLO;
-    best_tail = false;
+  if (pick.t == 1e300) {  // forced choices not reachable exactly: take the nearest valid
+    pick.s = force_s > 0 ? int(std::min<int64_t>(force_s, kb)) : 1;
+    pick.bn = force_bn ? force_bn : 256;
+    pick.mode = force_pair ? dg::TC_PAIR : dg::TC_SOLO;
+    pick.tail = false;
   }
-  const int64_t kbps = ceil_div(kb, best_s);
-  best_s = int(ceil_div(kb, kbps));
-  const bool pair = best_mode == dg::TC_PAIR, kpair = best_mode == dg::TC_KPAIR;
+  *best = pick;
+}
+
+// The configuration record of one choice.
+void fill_info(int64_t M, int64_t N, int64_t K, int sms, const TcChoice& c, gemm_config_info_t* out) {
+  const int64_t kb = ceil_div(K, dg::TC_BK);
+  const int best_s = int(ceil_div(kb, ceil_div(kb, c.s)));
+  const bool pair = c.mode == dg::TC_PAIR, kpair = c.mode == dg::TC_KPAIR;
   const int tile_m = pair ? 2 * dg::TC_BM : dg::TC_BM;
   const int pairs = sms / 2;
   const int slots = pair ? pairs : sms;
   std::memset(out, 0, sizeof(*out));
-  quantization(M, N, tile_m, best_bn, best_s, slots, 1, out);
+  quantization(M, N, tile_m, c.bn, best_s, slots, 1, out);
   out->sms = sms;
   if (kpair) {
     out->path = GEMM_PATH_TC_SPLITK_CLUSTER;
-  } else if (best_tail) {
+  } else if (c.tail && out->tiles % slots != 0) {
     out->path = GEMM_PATH_TC_TAIL_SPLIT;
     out->tail_tiles = int32_t(out->tiles % slots);
     out->units = (out->tiles - out->tail_tiles) + int64_t(out->tail_tiles) * best_s;
@@ -413,10 +430,10 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
     out->path = GEMM_PATH_TC;
   }
   out->tile_k = dg::TC_BK;
-  out->cta_per_tile = best_mode == dg::TC_SOLO ? 1 : 2;
-  out->stages = dg::tc_stages(best_bn, best_mode);
+  out->cta_per_tile = c.mode == dg::TC_SOLO ? 1 : 2;
+  out->stages = dg::tc_stages(c.bn, c.mode);
   const int64_t mblocks = ceil_div(M, tile_m);
-  out->raster_group = int(std::max<int64_t>(1, std::min<int64_t>(raster, mblocks)));
+  out->raster_group = int(std::max<int64_t>(1, std::min<int64_t>(env_int("GEMM_RASTER_GROUP", 16), mblocks)));
   if (pair)
     out->grid = int(2 * std::min<int64_t>(out->units, pairs));
   else if (kpair)
@@ -424,7 +441,14 @@ void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
   else
     out->grid = int(std::min<int64_t>(out->units, sms));
   out->launches = out->tail_tiles > 0 ? 2 : 1;
-  out->workspace_bytes = int64_t(out->tail_tiles) * best_s * tile_m * best_bn * 4;
+  out->workspace_bytes = int64_t(out->tail_tiles) * best_s * tile_m * c.bn * 4;
+}
+
+void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
+               gemm_config_info_t* out) {
+  TcChoice best;
+  tc_candidates(M, N, K, sms, c_es, beta, &best, nullptr);
+  fill_info(M, N, K, sms, best, out);
 }
 
 // ------------------------------------------------------------ tensor maps
@@ -596,10 +620,13 @@ bool planner_overridden() {
 gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* A,
                              int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
                              bool beta_nz, gemm_dtype_t dtype, gemm_op_t ta, gemm_op_t tb,
-                             TcEntry* e) {
+                             const TcChoice* forced, TcEntry* e) {
   gemm_config_info_t* info = &e->info;
   const int c_es = out_is_f32(dtype) ? 4 : 2;
-  choose_tc(M, N, K, plan->sms, c_es, beta_nz, info);
+  if (forced)
+    fill_info(M, N, K, plan->sms, *forced, info);
+  else
+    choose_tc(M, N, K, plan->sms, c_es, beta_nz, info);
   const int bn = info->tile_n;
   const int S = info->splitk;
   const int mode = tc_mode(*info);
@@ -656,31 +683,10 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
   return ok ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
-gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-                     const void* B, int64_t ldb, void* C, int64_t ldc, float alpha, float beta,
-                     gemm_dtype_t dtype, gemm_op_t ta, gemm_op_t tb, gemm_epilogue_t epi,
-                     cudaStream_t s, gemm_config_info_t* info) {
-  const TcKey key{M, N, K, lda, ldb, ldc, reinterpret_cast<uintptr_t>(A), reinterpret_cast<uintptr_t>(B),
-                  reinterpret_cast<uintptr_t>(C), int32_t(dtype), int32_t(ta), int32_t(tb),
-                  int32_t(beta != 0.f)};
-  const bool use_cache = !planner_overridden();
-  TcEntry local;
-  TcEntry* e = nullptr;
-  if (use_cache) {
-    auto it = plan->tc_cache.find(key);
-    if (it != plan->tc_cache.end()) e = &it->second;
-  }
-  if (e == nullptr) {
-    const gemm_status_t st = build_tc_entry(plan, M, N, K, A, lda, B, ldb, C, ldc, beta != 0.f, dtype,
-                                            ta, tb, &local);
-    if (st != GEMM_OK) return st;
-    if (use_cache) {
-      if (plan->tc_cache.size() >= 256) plan->tc_cache.clear();
-      e = &plan->tc_cache.emplace(key, local).first->second;
-    } else {
-      e = &local;
-    }
-  }
+// Launch the kernels of a planned call (the plan's workspace may grow).
+gemm_status_t launch_entry(gemm_plan* plan, TcEntry* e, int64_t M, int64_t N, void* C, int64_t ldc,
+                           float alpha, float beta, gemm_dtype_t dtype, gemm_epilogue_t epi,
+                           cudaStream_t s) {
   dg::TcParams p = e->p;  // per-call fields below
   p.alpha = alpha;
   p.beta = beta;
@@ -700,7 +706,6 @@ gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const voi
       e->ws_ptr = plan->ws;
     }
   }
-  *info = e->info;
   if (dg::launch_gemm_tc(e->info.tile_n, mode, e->ma, e->mb, e->mc, e->mw, p, e->info.grid, s) !=
       cudaSuccess)
     return GEMM_ERR_CUDA;
@@ -723,6 +728,109 @@ gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const voi
     if (dg::launch_tile_reduce(r, s, plan->sms) != cudaSuccess) return GEMM_ERR_CUDA;
   }
   return GEMM_OK;
+}
+
+// Benchmark mode ("Matrix Multiplication Background User's Guide", section
+// 2.3: some frameworks time every implementation option once and keep the
+// fastest): time the planner's leading candidates on this call's stream,
+// writing into a scratch copy of C, and return the fastest.  Falls back to
+// the planner's pick if anything fails.
+TcChoice autotune(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                  const void* B, int64_t ldb, const void* C, int64_t ldc, float alpha, float beta,
+                  gemm_dtype_t dtype, gemm_op_t ta, gemm_op_t tb, gemm_epilogue_t epi, cudaStream_t s) {
+  const int c_es = out_is_f32(dtype) ? 4 : 2;
+  std::vector<TcChoice> all;
+  TcChoice best;
+  tc_candidates(M, N, K, plan->sms, c_es, beta != 0.f, &best, &all);
+  std::stable_sort(all.begin(), all.end(), [](const TcChoice& x, const TcChoice& y) { return x.t < y.t; });
+  std::vector<TcChoice> trial{best};
+  for (const TcChoice& c : all) {
+    if (trial.size() >= 6 || c.t > 1.15 * all.front().t) break;
+    bool dup = false;
+    for (const TcChoice& d : trial) dup |= d.bn == c.bn && d.mode == c.mode && d.s == c.s && d.tail == c.tail;
+    if (!dup) trial.push_back(c);
+  }
+  if (trial.size() < 2) return best;
+  const size_t c_bytes = (size_t(M - 1) * size_t(ldc) + size_t(N)) * size_t(c_es);
+  void* scratch = nullptr;
+  if (cudaMallocAsync(&scratch, c_bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return best;
+  }
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  bool ok = cudaMemcpyAsync(scratch, C, c_bytes, cudaMemcpyDeviceToDevice, s) == cudaSuccess &&
+            cudaEventCreate(&e0) == cudaSuccess && cudaEventCreate(&e1) == cudaSuccess;
+  TcChoice fastest = best;
+  float fastest_ms = 1e30f;
+  constexpr int kReps = 3;
+  for (size_t i = 0; ok && i < trial.size(); ++i) {
+    TcEntry ent;
+    if (build_tc_entry(plan, M, N, K, A, lda, B, ldb, scratch, ldc, beta != 0.f, dtype, ta, tb, &trial[i],
+                       &ent) != GEMM_OK)
+      continue;
+    if (launch_entry(plan, &ent, M, N, scratch, ldc, alpha, beta, dtype, epi, s) != GEMM_OK) continue;
+    bool run_ok = cudaEventRecord(e0, s) == cudaSuccess;
+    for (int r = 0; r < kReps && run_ok; ++r)
+      run_ok = launch_entry(plan, &ent, M, N, scratch, ldc, alpha, beta, dtype, epi, s) == GEMM_OK;
+    float ms = 0.f;
+    run_ok = run_ok && cudaEventRecord(e1, s) == cudaSuccess && cudaEventSynchronize(e1) == cudaSuccess &&
+             cudaEventElapsedTime(&ms, e0, e1) == cudaSuccess;
+    if (!run_ok) {
+      cudaGetLastError();
+      ok = false;
+      break;
+    }
+    if (ms < fastest_ms * 0.99f) {  // the earlier (planner-ranked) choice unless clearly faster
+      fastest_ms = ms;
+      fastest = trial[i];
+    }
+  }
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  cudaFreeAsync(scratch, s);
+  return ok ? fastest : best;
+}
+
+gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                     const void* B, int64_t ldb, void* C, int64_t ldc, float alpha, float beta,
+                     gemm_dtype_t dtype, gemm_op_t ta, gemm_op_t tb, gemm_epilogue_t epi,
+                     cudaStream_t s, gemm_config_info_t* info) {
+  const TcKey key{M, N, K, lda, ldb, ldc, reinterpret_cast<uintptr_t>(A), reinterpret_cast<uintptr_t>(B),
+                  reinterpret_cast<uintptr_t>(C), int32_t(dtype), int32_t(ta), int32_t(tb),
+                  int32_t(beta != 0.f)};
+  const bool use_cache = !planner_overridden();
+  TcEntry local;
+  TcEntry* e = nullptr;
+  if (use_cache) {
+    auto it = plan->tc_cache.find(key);
+    if (it != plan->tc_cache.end()) e = &it->second;
+  }
+  if (e == nullptr) {
+    const TcChoice* forced = nullptr;
+    TcChoice tuned;
+    if (plan->autotune && use_cache) {
+      TcKey shape = key;
+      shape.A = shape.B = shape.C = 0;
+      auto t = plan->tuned.find(shape);
+      if (t == plan->tuned.end())
+        t = plan->tuned.emplace(shape, autotune(plan, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype,
+                                                ta, tb, epi, s)).first;
+      tuned = t->second;
+      forced = &tuned;
+      if (plan->tuned.size() > 4096) plan->tuned.clear();  // bounded; re-tuned on next use
+    }
+    const gemm_status_t st = build_tc_entry(plan, M, N, K, A, lda, B, ldb, C, ldc, beta != 0.f, dtype,
+                                            ta, tb, forced, &local);
+    if (st != GEMM_OK) return st;
+    if (use_cache) {
+      if (plan->tc_cache.size() >= 256) plan->tc_cache.clear();
+      e = &plan->tc_cache.emplace(key, local).first->second;
+    } else {
+      e = &local;
+    }
+  }
+  *info = e->info;
+  return launch_entry(plan, e, M, N, C, ldc, alpha, beta, dtype, epi, s);
 }
 
 }  // namespace
@@ -763,6 +871,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* plan, int device) {
   gemm_plan* p = new gemm_plan();
   p->device = device;
   p->sms = prop.multiProcessorCount;
+  p->autotune = env_int("GEMM_AUTOTUNE", 0) != 0;
   if (const char* w = std::getenv("GEMM_WATCHDOG_NS")) {
     const unsigned long long v = std::strtoull(w, nullptr, 10);
     if (v >= 1000) p->watchdog_ns = v;
@@ -855,6 +964,18 @@ gemm_status_t gemm_plan_poll_error(gemm_plan_t plan, void* stream) {
 gemm_status_t gemm_plan_set_watchdog(gemm_plan_t plan, uint64_t timeout_ns) {
   if (!plan || timeout_ns < 1000) return GEMM_ERR_INVALID_ARG;
   plan->watchdog_ns = timeout_ns;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_set_autotune(gemm_plan_t plan, int enable) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  plan->autotune = enable != 0;
+  return GEMM_OK;
+}
+
+gemm_status_t gemm_plan_tuned_count(gemm_plan_t plan, int64_t* count) {
+  if (!plan || !count) return GEMM_ERR_INVALID_ARG;
+  *count = int64_t(plan->tuned.size());
   return GEMM_OK;
 }
 

@@ -82,6 +82,8 @@ _SIGNATURES = {
                                  ctypes.POINTER(gemm_config_info_t)]),
     "gemm_gemv_noalloc": (_I32, [_I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64, _F, _F,
                                  _I32, _I32, _I32, gemm_epilogue_t, _VP]),
+    "gemm_plan_set_autotune": (_I32, [_VP, ctypes.c_int]),
+    "gemm_plan_tuned_count": (_I32, [_VP, ctypes.POINTER(_I64)]),
 }
 
 
@@ -177,6 +179,18 @@ def gemm_gemv_noalloc(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype, trans
                       act=GEMM_ACT_NONE, slope=0.0, stream=None) -> int:
     return load().gemm_gemv_noalloc(M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype,
                                     transA, transB, gemm_epilogue_t(act, slope), stream)
+
+
+def gemm_plan_set_autotune(plan, enable: bool) -> int:
+    return load().gemm_plan_set_autotune(plan, int(bool(enable)))
+
+
+def gemm_plan_tuned_count(plan) -> int:
+    n = _I64()
+    st = load().gemm_plan_tuned_count(plan, ctypes.byref(n))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_plan_tuned_count")
+    return n.value
 
 
 # ------------------------------------------------------------------ torch helpers

@@ -191,6 +191,28 @@ gemm_status_t gemm_plan_poll_error(gemm_plan_t plan, void* stream);
  * default at plan creation).  Values < 1000 are rejected. */
 gemm_status_t gemm_plan_set_watchdog(gemm_plan_t plan, uint64_t timeout_ns);
 
+/* Benchmark mode ("Matrix Multiplication Background User's Guide", section
+ * 2.3: some frameworks time every implementation option once, before the
+ * real work, and keep the fastest).  With enable != 0, the first
+ * tensor-core gemm_run of each (M, N, K, lda, ldb, ldc, dtype, transA,
+ * transB, beta != 0) on this plan times the planner's leading candidates
+ * (its pick and up to five more estimated within 15% of the best): one
+ * warm-up and three timed runs each, on the call's stream, writing into a
+ * scratch copy of C (stream-ordered allocation the size of C; C, A and B
+ * are not modified).  The fastest is kept for every later call of that
+ * shape on this plan, whatever the pointers.  That first call blocks the
+ * host until the trials have run (a one-time cost per shape); if anything
+ * fails the planner's pick is kept.  enable = 0 (the default; the
+ * environment variable GEMM_AUTOTUNE=1 turns it on at plan creation)
+ * uses the planner's estimate alone.  Ignored while any GEMM_FORCE_* /
+ * GEMM_RASTER_GROUP / GEMM_SPLITK_CLUSTER / GEMM_TAIL_SPLIT override is set.
+ * GEMM_ERR_INVALID_ARG on NULL. */
+gemm_status_t gemm_plan_set_autotune(gemm_plan_t plan, int enable);
+
+/* Number of shapes benchmark mode has timed on this plan (bounded: the
+ * record is cleared past 4096 shapes).  GEMM_ERR_INVALID_ARG on NULL. */
+gemm_status_t gemm_plan_tuned_count(gemm_plan_t plan, int64_t* count);
+
 /* Watchdog self-test: launch one CTA that waits on a barrier nothing will
  * ever arrive on, with this plan's limit, then wait for `stream`.  Returns
  * GEMM_ERR_TIMEOUT when the wait ran out and the kernel returned on its own

@@ -254,6 +254,32 @@ def test_tail_split_planner_choice_wave_shape(plan):
     assert r.info["path"] == "tc_tail_split" and r.info["tail_tiles"] == 5
 
 
+# ----------------------------------------------------------- benchmark mode
+
+def test_autotune_benchmark_mode():
+    """Benchmark mode times the planner's leading candidates once per shape on
+    a scratch copy of C: with beta != 0 the result still matches the oracle
+    (the trials did not touch C), a second call of the same shape on new
+    buffers reuses the decision, and a new shape is timed once more."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_gemm_mma_gb300 import gemm
+    p = gemm.Plan(0)
+    try:
+        assert gemm.gemm_plan_set_autotune(p.handle, True) == gemm.GEMM_OK
+        assert gemm.gemm_plan_tuned_count(p.handle) == 0
+        r1 = run_case(p, 1300, 2000, 700, beta=0.5, act=1, slope=0.1, out_fmt="bf16", seed=90)
+        assert gemm.gemm_plan_tuned_count(p.handle) == 1
+        r2 = run_case(p, 1300, 2000, 700, beta=0.5, act=1, slope=0.1, out_fmt="bf16", seed=91)
+        assert gemm.gemm_plan_tuned_count(p.handle) == 1 and r2.info == r1.info
+        run_case(p, 2304, 2176, 1024, in_fmt="f16", seed=92, sample=2048)
+        assert gemm.gemm_plan_tuned_count(p.handle) == 2
+        assert p.poll_error() == gemm.GEMM_OK
+    finally:
+        p.close()
+
+
 def test_splitk_ragged_with_beta(plan):
     r = run_case(plan, 200, 150, 3000, out_fmt="bf16", beta=0.5, act=1, slope=0.1,
                  env={"GEMM_FORCE_SPLITK": "5", "GEMM_FORCE_TILE": "128x64"}, seed=61)
