@@ -21,7 +21,8 @@
  *  - "OpenAI open-sources the Triton GPU language (part 2)", section Matrix
  *    multiplication: an output transform such as LeakyReLU fused after the
  *    product.  Reading taken: act is applied to alpha*AB + beta*C, and
- *    LeakyReLU(x) = x < 0 ? slope*x : x.
+ *    LeakyReLU(x) = x < 0 ? slope*x : x.  ReLU, GELU and SiLU are further
+ *    transforms of the same kind, written from their definitions (apply_act).
  *
  * Arithmetic: every bf16/fp16 input is decoded exactly to double; the dot
  * product is accumulated in double in ascending k; alpha, beta and the
@@ -34,7 +35,9 @@
  * into 3-element partial dot products and (2,2) blocks; identity and
  * permutation matrices; (A@B)^T = B^T@A^T through the transpose flags;
  * alpha/beta linearity; exact rational brute force for all M,N,K in 1..6;
- * the rounding and decoding routines against numpy and exact rationals.
+ * the rounding and decoding routines against numpy and exact rationals;
+ * the activations against tabulated values of the normal distribution
+ * function and of exp, and the identity f(x) - f(-x) = x of GELU and SiLU.
  */
 #include <math.h>
 #include <stddef.h>
@@ -153,6 +156,24 @@ static void store_out(void* D, int fmt, int64_t idx, double v) {
 
 /* ------------------------------------------------------------ the method */
 
+/* The output transform, in double.  1: LeakyReLU, the pages' example of a
+ * transform fused after the product.  2-4: further activations fused at the
+ * same place, from their textbook definitions:
+ *   ReLU(x) = x < 0 ? 0 : x              (-0 and NaN pass unchanged)
+ *   GELU(x) = x * Phi(x),  Phi(x) = erfc(-x / sqrt(2)) / 2, the standard
+ *             normal distribution function
+ *   SiLU(x) = x * sigmoid(x) = x / (1 + exp(-x))
+ * 0 (or any other code): identity. */
+static double apply_act(double d, int act, double slope) {
+  switch (act) {
+    case 1: return d < 0.0 ? slope * d : d;
+    case 2: return d < 0.0 ? 0.0 : d;
+    case 3: return 0.5 * d * erfc(-d / sqrt(2.0));
+    case 4: return d / (1.0 + exp(-d));
+    default: return d;
+  }
+}
+
 /* One output entry before output rounding: act(alpha * sum_k a(i,k) b(k,j) + beta * c(i,j)). */
 double oracle_entry(int64_t i, int64_t j, int64_t K,
                     const void* A, int64_t lda, const void* B, int64_t ldb,
@@ -164,8 +185,7 @@ double oracle_entry(int64_t i, int64_t j, int64_t K,
     s += elem_a(A, lda, transA, in_fmt, i, k) * elem_b(B, ldb, transB, in_fmt, k, j);
   double d = alpha * s;
   if (beta != 0.0) d += beta * load_in(C, c_fmt, i * ldc + j);
-  if (act == 1 && d < 0.0) d = slope * d;
-  return d;
+  return apply_act(d, act, slope);
 }
 
 /* Full product.  D_exact (M x N doubles, row stride N) receives the value

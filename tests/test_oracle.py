@@ -18,6 +18,8 @@ import json
 import os
 from fractions import Fraction
 
+import math
+
 import numpy as np
 import pytest
 
@@ -227,6 +229,47 @@ def test_leaky_relu_special_cases(oracle_lib):
     neg, _ = oracle_lib.gemm(M, N, K, A, B, act=1, slope=0.25, alpha=-1.0)
     assert np.array_equal(neg[~pos], -plain[~pos])
     assert np.array_equal(neg[plain > 0], -plain[plain > 0] * 0.25)
+
+
+def _act_of(oracle_lib, x, act):
+    """act(x) through the oracle's epilogue: a 1x1x1 product x * 1 (x exact in bf16)."""
+    A = inputs.f32_to_bf16_bits(np.array([[x]], dtype=np.float32))
+    B = inputs.f32_to_bf16_bits(np.array([[1.0]], dtype=np.float32))
+    e, _ = oracle_lib.gemm(1, 1, 1, A, B, act=act)
+    return float(e[0, 0])
+
+
+# Standard normal distribution function Phi and exp at a few points (printed
+# tables of the normal distribution; e^-1, e^-2).
+PHI = {0.5: 0.6914624612740131, 1.0: 0.8413447460685429, 2.0: 0.9772498680518208}
+EXP_NEG = {1.0: 0.36787944117144233, 2.0: 0.1353352832366127}
+
+
+def test_relu_gelu_silu_against_tables_and_identities(oracle_lib):
+    for x in (-3.0, -1.0, -0.5, 0.0, 0.5, 1.0, 2.0, 3.0):
+        assert _act_of(oracle_lib, x, 2) == max(x, 0.0)                      # ReLU
+    for x, phi in PHI.items():
+        assert abs(_act_of(oracle_lib, x, 3) - x * phi) <= 4e-16            # GELU(x) = x Phi(x)
+        assert abs(_act_of(oracle_lib, -x, 3) + x * (1.0 - phi)) <= 4e-16   # Phi(-x) = 1 - Phi(x)
+    for x, en in EXP_NEG.items():
+        assert abs(_act_of(oracle_lib, x, 4) - x / (1.0 + en)) <= 4e-16     # SiLU(x) = x / (1 + e^-x)
+    for act in (3, 4):                                                      # f(x) - f(-x) = x
+        for x in (0.25, 0.5, 1.0, 1.5, 2.0, 3.0, 6.0):
+            assert abs(_act_of(oracle_lib, x, act) - _act_of(oracle_lib, -x, act) - x) <= 1e-15
+        assert _act_of(oracle_lib, 0.0, act) == 0.0
+
+
+def test_activation_follows_alpha_and_beta(oracle_lib):
+    M, N, K = 6, 5, 7
+    A = inputs.matrix(M, K, 14, 0, "bf16")
+    B = inputs.matrix(K, N, 14, 1, "bf16")
+    C = inputs.matrix(M, N, 14, 2, "f32")
+    pre, _ = oracle_lib.gemm(M, N, K, A, B, C=C, alpha=-1.5, beta=0.5)
+    phi = lambda v: 0.5 * np.vectorize(math.erfc)(-v / math.sqrt(2.0))
+    for act, f in ((2, lambda v: np.where(v < 0, 0.0, v)), (3, lambda v: v * phi(v)),
+                   (4, lambda v: v / (1.0 + np.exp(-v)))):
+        got, _ = oracle_lib.gemm(M, N, K, A, B, C=C, alpha=-1.5, beta=0.5, act=act)
+        assert np.allclose(got, f(pre), rtol=1e-15, atol=1e-16)
 
 
 # ------------------------------------------------------------- brute force

@@ -34,6 +34,10 @@ MUTANTS = {
     "f16_subnormal_scale": ("v = ldexp((double)m, -24);", "v = ldexp((double)m, -25);"),
     "bf16_wrong_precision": ("double r = round_to_precision(x, 8, -126);",
                              "double r = round_to_precision(x, 9, -126);"),
+    "gelu_wrong_sign": ("return 0.5 * d * erfc(-d / sqrt(2.0));", "return 0.5 * d * erfc(d / sqrt(2.0));"),
+    "gelu_half_dropped": ("return 0.5 * d * erfc(-d / sqrt(2.0));", "return d * erfc(-d / sqrt(2.0));"),
+    "silu_wrong_sign": ("return d / (1.0 + exp(-d));", "return d / (1.0 + exp(d));"),
+    "relu_as_identity": ("case 2: return d < 0.0 ? 0.0 : d;", "case 2: return d;"),
 }
 
 
