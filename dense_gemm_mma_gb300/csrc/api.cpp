@@ -111,7 +111,7 @@ gemm_status_t check(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   if (dtype < GEMM_BF16_F32 || dtype > GEMM_F16_F16) return GEMM_ERR_INVALID_ARG;
   if ((ta != GEMM_OP_N && ta != GEMM_OP_T) || (tb != GEMM_OP_N && tb != GEMM_OP_T))
     return GEMM_ERR_INVALID_ARG;
-  if (epi.act != GEMM_ACT_NONE && epi.act != GEMM_ACT_LEAKY_RELU) return GEMM_ERR_INVALID_ARG;
+  if (epi.act < GEMM_ACT_NONE || epi.act > GEMM_ACT_SILU) return GEMM_ERR_INVALID_ARG;
   if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return GEMM_ERR_UNSUPPORTED;
   const int64_t a_cols = ta == GEMM_OP_N ? K : M;
   const int64_t b_cols = tb == GEMM_OP_N ? N : K;

@@ -130,8 +130,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
 __device__ __forceinline__ float epi_value(float acc, float c, const TcParams& p, bool has_beta) {
   float v = p.alpha * acc;
   if (has_beta) v = fmaf(p.beta, c, v);
-  if (p.act == 1) v = v < 0.f ? v * p.slope : v;
-  return v;
+  return apply_act(v, p.act, p.slope);
 }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, int out_kind) {

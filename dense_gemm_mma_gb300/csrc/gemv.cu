@@ -88,7 +88,7 @@ __device__ __forceinline__ void store_c(void* C, int64_t idx, float v, int kind)
 __device__ __forceinline__ float epilogue(float acc, const void* C, int64_t idx, const EpiParams& e) {
   float v = e.alpha * acc;
   if (e.beta != 0.f) v = fmaf(e.beta, load_c(C, idx, e.out_kind), v);
-  if (e.act == 1 && v < 0.f) v *= e.slope;
+  v = apply_act(v, e.act, e.slope);
   return v;
 }
 
@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(256) tile_reduce_kernel(const TileReduceArgs a
       for (int j = 0; j < 4; ++j) {
         float v = e.alpha * sv[j];
         if (e.beta != 0.f) v = fmaf(e.beta, cin[j], v);
-        if (e.act == 1 && v < 0.f) v *= e.slope;
+        v = apply_act(v, e.act, e.slope);
         sv[j] = v;
       }
       *cp = make_float4(sv[0], sv[1], sv[2], sv[3]);
@@ -390,7 +390,7 @@ __global__ void __launch_bounds__(256) tile_reduce_kernel(const TileReduceArgs a
                                                  : __half2float(__ushort_as_half(cin[j]));
           v = fmaf(e.beta, c, v);
         }
-        if (e.act == 1 && v < 0.f) v *= e.slope;
+        v = apply_act(v, e.act, e.slope);
         o[j] = e.out_kind == OUT_BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v))
                                       : __half_as_ushort(__float2half_rn(v));
       }
@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(256) scale_kernel(int M, int N, void* C, int64
     const int n = static_cast<int>(i - static_cast<int64_t>(m) * N);
     const int64_t idx = static_cast<int64_t>(m) * ldc + n;
     float v = e.beta != 0.f ? e.beta * load_c(C, idx, e.out_kind) : 0.f;
-    if (e.act == 1 && v < 0.f) v *= e.slope;
+    v = apply_act(v, e.act, e.slope);
     store_c(C, idx, v, e.out_kind);
   }
 }

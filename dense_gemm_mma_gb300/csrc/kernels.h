@@ -101,6 +101,21 @@ cudaError_t launch_gemm_tc(int bn, int mode, const CUtensorMap& a, const CUtenso
 
 
 
+#ifdef __CUDACC__
+// Output transform (gemm_act_t), in fp32: 1 LeakyReLU, 2 ReLU, 3 GELU
+// (x * Phi(x), Phi through erfc so the negative tail keeps its relative
+// accuracy), 4 SiLU; anything else is the identity.
+__device__ __forceinline__ float apply_act(float v, int act, float slope) {
+  switch (act) {
+    case 1: return v < 0.f ? v * slope : v;
+    case 2: return v < 0.f ? 0.f : v;
+    case 3: return 0.5f * v * erfcf(-v * 0.70710678118654752f);
+    case 4: return v / (1.f + expf(-v));
+    default: return v;
+  }
+}
+#endif
+
 struct EpiParams {
   float alpha, beta, slope;
   int act;

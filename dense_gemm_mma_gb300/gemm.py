@@ -24,7 +24,7 @@ GEMM_ERR_TIMEOUT = 7
 
 GEMM_OP_N, GEMM_OP_T = 0, 1
 GEMM_BF16_F32, GEMM_BF16_BF16, GEMM_F16_F32, GEMM_F16_F16 = 0, 1, 2, 3
-GEMM_ACT_NONE, GEMM_ACT_LEAKY_RELU = 0, 1
+GEMM_ACT_NONE, GEMM_ACT_LEAKY_RELU, GEMM_ACT_RELU, GEMM_ACT_GELU, GEMM_ACT_SILU = 0, 1, 2, 3, 4
 
 PATH_NAMES = {0: "none", 1: "tc", 2: "tc_splitk", 3: "gemv_rowdot", 4: "gemv_colstream",
               5: "gemv_generic", 6: "scale", 7: "tc_splitk_cluster", 8: "tc_tail_split"}

@@ -71,9 +71,18 @@ typedef enum {
   GEMM_F16_F16 = 3
 } gemm_dtype_t;
 
-typedef enum { GEMM_ACT_NONE = 0, GEMM_ACT_LEAKY_RELU = 1 } gemm_act_t;
+typedef enum {
+  GEMM_ACT_NONE = 0,
+  GEMM_ACT_LEAKY_RELU = 1, /* x < 0 ? slope*x : x  (the pages' example: "OpenAI open-sources the
+                              Triton GPU language (part 2)", section Matrix multiplication) */
+  GEMM_ACT_RELU = 2,       /* x < 0 ? 0 : x  (-0 and NaN pass unchanged)                    */
+  GEMM_ACT_GELU = 3,       /* x * Phi(x), Phi the standard normal distribution function,
+                              evaluated as erfc(-x / sqrt(2)) / 2 in fp32                    */
+  GEMM_ACT_SILU = 4        /* x * sigmoid(x) = x / (1 + exp(-x)), in fp32                     */
+} gemm_act_t;
 
-/* act = GEMM_ACT_LEAKY_RELU applies x < 0 ? slope*x : x after alpha and beta. */
+/* The activation is applied in fp32 to alpha*acc + beta*C, before the
+ * rounding to the output type; slope is read for GEMM_ACT_LEAKY_RELU only. */
 typedef struct {
   int32_t act;
   float slope;

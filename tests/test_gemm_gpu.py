@@ -162,6 +162,29 @@ def test_splitk_forced_and_deterministic(plan, splits):
     assert np.array_equal(r.outputs[0].view(np.uint8), r.outputs[1].view(np.uint8))
 
 
+# ------------------------------------------------------ further activations
+
+ACTS = {"relu": 2, "gelu": 3, "silu": 4}
+
+
+@pytest.mark.parametrize("act", sorted(ACTS))
+@pytest.mark.parametrize("out_fmt", ["f32", "bf16"])
+def test_activations_every_path(plan, act, out_fmt):
+    """Each activation on every kernel that applies an epilogue: one-CTA tiles,
+    the CTA pair, the K pair, tail and full split-K (reduction kernel), the
+    GEMV kernels and the scale path."""
+    a = ACTS[act]
+    kw = dict(out_fmt=out_fmt, act=a, alpha=1.5, beta=-0.5, seed=100 + a)
+    run_case(plan, 300, 520, 200, env={"GEMM_FORCE_TILE": "128x128", "GEMM_FORCE_SPLITK": "1"}, **kw)
+    run_case(plan, 257, 300, 513, env={"GEMM_FORCE_TILE": "256x256"}, **kw)
+    run_case(plan, 384, 260, 1000, env={"GEMM_SPLITK_CLUSTER": "1", "GEMM_FORCE_SPLITK": "2"}, **kw)
+    run_case(plan, 1300, 2000, 333, env={"GEMM_TAIL_SPLIT": "3", "GEMM_FORCE_TILE": "128x128"}, **kw)
+    run_case(plan, 200, 150, 3000, env={"GEMM_FORCE_SPLITK": "5", "GEMM_SPLITK_CLUSTER": "0"}, **kw)
+    run_case(plan, 1, 4100, 2000, **kw)               # column-stream GEMV
+    run_case(plan, 3000, 1, 2000, **kw)               # row-dot GEMV
+    run_case(plan, 64, 80, 0, **kw)                   # K = 0: act(beta * C)
+
+
 # ------------------------------------------- split-K reduced on chip (K pair)
 
 KPAIR = {"GEMM_SPLITK_CLUSTER": "1", "GEMM_FORCE_SPLITK": "2"}

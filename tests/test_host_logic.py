@@ -94,7 +94,9 @@ def test_check_args_rejects():
     assert chk(8, 8, -1) == E
     assert chk(8, 8, 8, dtype=4) == E
     assert chk(8, 8, 8, ta=2) == E
-    assert chk(8, 8, 8, act=5) == E
+    assert chk(8, 8, 8, act=5) == E and chk(8, 8, 8, act=-1) == E
+    for act in (g.GEMM_ACT_RELU, g.GEMM_ACT_GELU, g.GEMM_ACT_SILU):
+        assert chk(8, 8, 8, act=act) == g.GEMM_OK
     assert chk(2 ** 31, 8, 8) == U
     assert chk(8, 8, 16, lda=8) == E                 # lda < K
     assert chk(8, 16, 8, ldb=8) == E                 # ldb < N
