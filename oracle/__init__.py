@@ -58,10 +58,10 @@ def _load():
                                      i, i, i, i, i, d]
         lib.oracle_entry.restype = d
         lib.oracle_gemm.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, i64, d, d,
-                                    i, i, i, i, i, d, vp, vp]
+                                    i, i, i, i, i, i, d, vp, vp]
         lib.oracle_gemm.restype = i
         lib.oracle_sample.argtypes = [i64, vp, vp, i64, vp, i64, vp, i64, vp, i64, d, d,
-                                      i, i, i, i, i, d, vp, vp]
+                                      i, i, i, i, i, i, d, vp, vp]
         lib.oracle_sample.restype = i
         _lib = lib
     return _lib
@@ -89,16 +89,18 @@ def _out_array(shape, fmt):
 
 
 def gemm(M, N, K, A, B, *, lda=None, ldb=None, C=None, ldc=None, alpha=1.0, beta=0.0,
-         in_fmt="bf16", out_fmt="f32", transA=False, transB=False, act=0, slope=0.0):
+         in_fmt="bf16", out_fmt="f32", transA=False, transB=False, act=0, slope=0.0, c_fmt=None):
     """Full M x N result.  A, B (and C) are the STORED arrays: uint16 bit
     patterns for bf16/fp16, float32 for fp32; row strides lda/ldb/ldc default
-    to the arrays' widths.  Returns (exact_f64[M,N], rounded[M,N])."""
+    to the arrays' widths.  C is in c_fmt (default: out_fmt, C updated in
+    place).  Returns (exact_f64[M,N], rounded[M,N])."""
     lib = _load()
     fi, fo = _fmt(in_fmt), _fmt(out_fmt)
+    fc = _fmt(c_fmt if c_fmt is not None else out_fmt)
     exact = np.empty((M, N), dtype=np.float64)
     out = _out_array((M, N), fo)
     rc = lib.oracle_gemm(M, N, K, _ptr(A), _ld(A, lda), _ptr(B), _ld(B, ldb),
-                         _ptr(C), _ld(C, ldc), float(alpha), float(beta), fi, fo,
+                         _ptr(C), _ld(C, ldc), float(alpha), float(beta), fi, fo, fc,
                          int(bool(transA)), int(bool(transB)), int(act), float(slope),
                          exact.ctypes.data, out.ctypes.data)
     if rc != 0:
@@ -108,10 +110,11 @@ def gemm(M, N, K, A, B, *, lda=None, ldb=None, C=None, ldc=None, alpha=1.0, beta
 
 def sample(rows, cols, K, A, B, *, lda=None, ldb=None, C=None, ldc=None, alpha=1.0,
            beta=0.0, in_fmt="bf16", out_fmt="f32", transA=False, transB=False, act=0,
-           slope=0.0):
+           slope=0.0, c_fmt=None):
     """Entries (rows[t], cols[t]) only; same values as gemm() at those places."""
     lib = _load()
     fi, fo = _fmt(in_fmt), _fmt(out_fmt)
+    fc = _fmt(c_fmt if c_fmt is not None else out_fmt)
     rows = np.ascontiguousarray(rows, dtype=np.int64)
     cols = np.ascontiguousarray(cols, dtype=np.int64)
     n = rows.shape[0]
@@ -119,7 +122,7 @@ def sample(rows, cols, K, A, B, *, lda=None, ldb=None, C=None, ldc=None, alpha=1
     out = _out_array(n, fo)
     rc = lib.oracle_sample(n, rows.ctypes.data, cols.ctypes.data, K, _ptr(A), _ld(A, lda),
                            _ptr(B), _ld(B, ldb), _ptr(C), _ld(C, ldc), float(alpha),
-                           float(beta), fi, fo, int(bool(transA)), int(bool(transB)),
+                           float(beta), fi, fo, fc, int(bool(transA)), int(bool(transB)),
                            int(act), float(slope), exact.ctypes.data, out.ctypes.data)
     if rc != 0:
         raise ValueError("oracle_sample rejected its arguments")

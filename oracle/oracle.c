@@ -190,20 +190,23 @@ double oracle_entry(int64_t i, int64_t j, int64_t K,
 
 /* Full product.  D_exact (M x N doubles, row stride N) receives the value
  * before output rounding; D_out (M x N in out_fmt, row stride N) receives it
- * rounded once.  Either may be NULL.  Returns 0, or -1 on a bad argument. */
+ * rounded once.  Either may be NULL.  C is stored in c_fmt (the output's
+ * format when C is updated in place; any format for a separate C).  Returns
+ * 0, or -1 on a bad argument. */
 int oracle_gemm(int64_t M, int64_t N, int64_t K,
                 const void* A, int64_t lda, const void* B, int64_t ldb,
                 const void* C, int64_t ldc, double alpha, double beta,
-                int in_fmt, int out_fmt, int transA, int transB,
+                int in_fmt, int out_fmt, int c_fmt, int transA, int transB,
                 int act, double slope, double* D_exact, void* D_out) {
   if (M < 0 || N < 0 || K < 0) return -1;
   if (in_fmt != ORC_BF16 && in_fmt != ORC_F16) return -1;
   if (out_fmt != ORC_BF16 && out_fmt != ORC_F16 && out_fmt != ORC_F32) return -1;
+  if (c_fmt != ORC_BF16 && c_fmt != ORC_F16 && c_fmt != ORC_F32) return -1;
   if (beta != 0.0 && C == NULL) return -1;
   for (int64_t i = 0; i < M; ++i) {
     for (int64_t j = 0; j < N; ++j) {
       double d = oracle_entry(i, j, K, A, lda, B, ldb, C, ldc, alpha, beta,
-                              in_fmt, out_fmt, transA, transB, act, slope);
+                              in_fmt, c_fmt, transA, transB, act, slope);
       if (D_exact) D_exact[i * N + j] = d;
       if (D_out) store_out(D_out, out_fmt, i * N + j, d);
     }
@@ -215,13 +218,13 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K,
 int oracle_sample(int64_t n, const int64_t* rows, const int64_t* cols, int64_t K,
                   const void* A, int64_t lda, const void* B, int64_t ldb,
                   const void* C, int64_t ldc, double alpha, double beta,
-                  int in_fmt, int out_fmt, int transA, int transB,
+                  int in_fmt, int out_fmt, int c_fmt, int transA, int transB,
                   int act, double slope, double* D_exact, void* D_out) {
   if (n < 0 || K < 0) return -1;
   if (beta != 0.0 && C == NULL) return -1;
   for (int64_t t = 0; t < n; ++t) {
     double d = oracle_entry(rows[t], cols[t], K, A, lda, B, ldb, C, ldc, alpha, beta,
-                            in_fmt, out_fmt, transA, transB, act, slope);
+                            in_fmt, c_fmt, transA, transB, act, slope);
     if (D_exact) D_exact[t] = d;
     if (D_out) store_out(D_out, out_fmt, t, d);
   }

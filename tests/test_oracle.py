@@ -202,6 +202,27 @@ def test_alpha_beta_linearity(oracle_lib):
         assert np.array_equal(e, alpha * s + beta * C.astype(np.float64))
 
 
+def test_separate_c_format(oracle_lib):
+    """A separate C is decoded in its own format: the same values given as
+    bf16, fp16 or fp32 C give the same result, and D's format only decides
+    the final rounding."""
+    M, N, K = 5, 6, 9
+    A = inputs.matrix(M, K, 15, 0, "bf16")
+    B = inputs.matrix(K, N, 15, 1, "bf16")
+    Cb = inputs.matrix(M, N, 15, 2, "bf16")
+    Cf = (Cb.astype(np.uint32) << np.uint32(16)).view(np.float32)   # the same values, as fp32
+    Ch = inputs.f32_to_f16_bits(Cf)
+    ref, _ = oracle_lib.gemm(M, N, K, A, B, C=Cb, beta=0.75, out_fmt="bf16")
+    for C, fmt in ((Cf, "f32"), (Cb, "bf16")):
+        for out in ("f32", "bf16", "f16"):
+            e, _ = oracle_lib.gemm(M, N, K, A, B, C=C, beta=0.75, out_fmt=out, c_fmt=fmt)
+            assert np.array_equal(e, ref)
+    hvals = Ch.view(np.float16).astype(np.float64)
+    e, _ = oracle_lib.gemm(M, N, K, A, B, C=Ch, beta=0.75, out_fmt="f32", c_fmt="f16")
+    plain, _ = oracle_lib.gemm(M, N, K, A, B)
+    assert np.array_equal(e, plain + 0.75 * hvals)
+
+
 def test_beta_zero_does_not_read_c(oracle_lib):
     M, N, K = 3, 4, 5
     A = inputs.matrix(M, K, 9, 0, "bf16")
