@@ -26,10 +26,13 @@ struct TcKey {
   int64_t M, N, K, lda, ldb, ldc;
   uintptr_t A, B, C;
   int32_t dtype, ta, tb, beta_nz;
+  uintptr_t Cin;  // the C that beta scales (C itself unless gemm_run_ex got a separate one)
+  int64_t ldcin;
+  int32_t cin_kind;
   bool operator==(const TcKey& o) const {
     return M == o.M && N == o.N && K == o.K && lda == o.lda && ldb == o.ldb && ldc == o.ldc &&
            A == o.A && B == o.B && C == o.C && dtype == o.dtype && ta == o.ta && tb == o.tb &&
-           beta_nz == o.beta_nz;
+           beta_nz == o.beta_nz && Cin == o.Cin && ldcin == o.ldcin && cin_kind == o.cin_kind;
   }
 };
 
@@ -39,7 +42,9 @@ struct TcKeyHash {
     auto mix = [&](uint64_t v) { h = (h ^ v) * 1099511628211ull; };
     mix(uint64_t(k.M)); mix(uint64_t(k.N)); mix(uint64_t(k.K)); mix(uint64_t(k.lda));
     mix(uint64_t(k.ldb)); mix(uint64_t(k.ldc)); mix(k.A); mix(k.B); mix(k.C);
-    mix(uint64_t(k.dtype) | (uint64_t(k.ta) << 8) | (uint64_t(k.tb) << 16) | (uint64_t(k.beta_nz) << 24));
+    mix(uint64_t(k.dtype) | (uint64_t(k.ta) << 8) | (uint64_t(k.tb) << 16) | (uint64_t(k.beta_nz) << 24) |
+        (uint64_t(k.cin_kind) << 32));
+    mix(k.Cin); mix(uint64_t(k.ldcin));
     return size_t(h);
   }
 };
@@ -50,6 +55,13 @@ struct TcChoice {
   int bn = 256, mode = dg::TC_SOLO, s = 1;
   bool tail = false;
   double t = 1e300;  // estimated seconds
+};
+
+// The C that beta scales: the output itself, or gemm_run_ex's separate C.
+struct CinRef {
+  const void* ptr;
+  int64_t ld;
+  int kind;  // dg::OutKind
 };
 
 // Planner decision, encoded tensor maps and kernel parameters of one call.
@@ -546,11 +558,13 @@ struct DeviceGuard {
 gemm_status_t run_gemv(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* A,
                        int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
                        gemm_dtype_t dtype, gemm_op_t ta, gemm_op_t tb, const dg::EpiParams& e,
-                       cudaStream_t s, gemm_config_info_t* info) {
+                       const CinRef& cin, cudaStream_t s, gemm_config_info_t* info) {
   dg::GemvArgs g{};
   g.K = int(K);
   g.in_f16 = in_is_f16(dtype);
   g.out = C;
+  g.cin = cin.ptr;
+  g.inc_cin = N == 1 ? cin.ld : 1;  // output r is C(r, 0) (N == 1) or C(0, r) (M == 1)
   g.e = e;
   bool row_major_w;  // true: W rows run along K (rowdot); false: W rows run along R (colstream)
   if (N == 1) {      // C(i,0) = sum_k op(A)(i,k) op(B)(k,0)
@@ -619,8 +633,8 @@ bool planner_overridden() {
 // Plan a tensor-core call and encode its descriptors (cache miss).
 gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* A,
                              int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc,
-                             bool beta_nz, gemm_dtype_t dtype, gemm_op_t ta, gemm_op_t tb,
-                             const TcChoice* forced, TcEntry* e) {
+                             const CinRef& cin, bool beta_nz, gemm_dtype_t dtype, gemm_op_t ta,
+                             gemm_op_t tb, const TcChoice* forced, TcEntry* e) {
   gemm_config_info_t* info = &e->info;
   const int c_es = out_is_f32(dtype) ? 4 : 2;
   if (forced)
@@ -668,6 +682,11 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
   p.idesc = make_idesc(f16, a_mn, b_mn, bn, tile_m);
   p.c_ptr = C;
   p.ldc = ldc;
+  p.cin = cin.ptr;
+  p.ldcin = cin.ld;
+  p.cin_kind = cin.kind;
+  // a C other than the output is read with plain loads in the epilogue
+  p.cin_direct = beta_nz && (cin.ptr != C || cin.ld != ldc || cin.kind != p.out_kind);
   p.err = plan->err;
   // TMA stores write whole 16-byte pieces of a row: the map covers only the
   // 16-byte-aligned prefix of each row of C; the kernel writes the rest.
@@ -687,6 +706,7 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
 gemm_status_t launch_entry(gemm_plan* plan, TcEntry* e, int64_t M, int64_t N, void* C, int64_t ldc,
                            float alpha, float beta, gemm_dtype_t dtype, gemm_epilogue_t epi,
                            cudaStream_t s) {
+  // (the C that beta scales travels in e->p: cin, ldcin, cin_kind)
   dg::TcParams p = e->p;  // per-call fields below
   p.alpha = alpha;
   p.beta = beta;
@@ -724,7 +744,9 @@ gemm_status_t launch_entry(gemm_plan* plan, TcEntry* e, int64_t M, int64_t N, vo
     r.N = int(N);
     r.C = C;
     r.ldc = ldc;
-    r.e = dg::EpiParams{alpha, beta, epi.slope, epi.act, out_kind(dtype)};
+    r.Cin = e->p.cin;
+    r.ldcin = e->p.ldcin;
+    r.e = dg::EpiParams{alpha, beta, epi.slope, epi.act, out_kind(dtype), e->p.cin_kind};
     if (dg::launch_tile_reduce(r, s, plan->sms) != cudaSuccess) return GEMM_ERR_CUDA;
   }
   return GEMM_OK;
@@ -736,8 +758,9 @@ gemm_status_t launch_entry(gemm_plan* plan, TcEntry* e, int64_t M, int64_t N, vo
 // writing into a scratch copy of C, and return the fastest.  Falls back to
 // the planner's pick if anything fails.
 TcChoice autotune(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-                  const void* B, int64_t ldb, const void* C, int64_t ldc, float alpha, float beta,
-                  gemm_dtype_t dtype, gemm_op_t ta, gemm_op_t tb, gemm_epilogue_t epi, cudaStream_t s) {
+                  const void* B, int64_t ldb, const void* C, int64_t ldc, const CinRef& cin, float alpha,
+                  float beta, gemm_dtype_t dtype, gemm_op_t ta, gemm_op_t tb, gemm_epilogue_t epi,
+                  cudaStream_t s) {
   const int c_es = out_is_f32(dtype) ? 4 : 2;
   std::vector<TcChoice> all;
   TcChoice best;
@@ -758,15 +781,20 @@ TcChoice autotune(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* 
     return best;
   }
   cudaEvent_t e0 = nullptr, e1 = nullptr;
-  bool ok = cudaMemcpyAsync(scratch, C, c_bytes, cudaMemcpyDeviceToDevice, s) == cudaSuccess &&
+  // The trials write the scratch; when beta scales the output itself they
+  // read the scratch copy of it too, else the separate C (never written).
+  const bool in_place = cin.ptr == C;
+  const CinRef cin_trial = in_place ? CinRef{scratch, ldc, cin.kind} : cin;
+  bool ok = (!in_place || beta == 0.f ||
+             cudaMemcpyAsync(scratch, C, c_bytes, cudaMemcpyDeviceToDevice, s) == cudaSuccess) &&
             cudaEventCreate(&e0) == cudaSuccess && cudaEventCreate(&e1) == cudaSuccess;
   TcChoice fastest = best;
   float fastest_ms = 1e30f;
   constexpr int kReps = 3;
   for (size_t i = 0; ok && i < trial.size(); ++i) {
     TcEntry ent;
-    if (build_tc_entry(plan, M, N, K, A, lda, B, ldb, scratch, ldc, beta != 0.f, dtype, ta, tb, &trial[i],
-                       &ent) != GEMM_OK)
+    if (build_tc_entry(plan, M, N, K, A, lda, B, ldb, scratch, ldc, cin_trial, beta != 0.f, dtype, ta, tb,
+                       &trial[i], &ent) != GEMM_OK)
       continue;
     if (launch_entry(plan, &ent, M, N, scratch, ldc, alpha, beta, dtype, epi, s) != GEMM_OK) continue;
     bool run_ok = cudaEventRecord(e0, s) == cudaSuccess;
@@ -792,12 +820,12 @@ TcChoice autotune(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* 
 }
 
 gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
-                     const void* B, int64_t ldb, void* C, int64_t ldc, float alpha, float beta,
-                     gemm_dtype_t dtype, gemm_op_t ta, gemm_op_t tb, gemm_epilogue_t epi,
+                     const void* B, int64_t ldb, void* C, int64_t ldc, const CinRef& cin, float alpha,
+                     float beta, gemm_dtype_t dtype, gemm_op_t ta, gemm_op_t tb, gemm_epilogue_t epi,
                      cudaStream_t s, gemm_config_info_t* info) {
   const TcKey key{M, N, K, lda, ldb, ldc, reinterpret_cast<uintptr_t>(A), reinterpret_cast<uintptr_t>(B),
                   reinterpret_cast<uintptr_t>(C), int32_t(dtype), int32_t(ta), int32_t(tb),
-                  int32_t(beta != 0.f)};
+                  int32_t(beta != 0.f), reinterpret_cast<uintptr_t>(cin.ptr), cin.ld, int32_t(cin.kind)};
   const bool use_cache = !planner_overridden();
   TcEntry local;
   TcEntry* e = nullptr;
@@ -810,16 +838,17 @@ gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const voi
     TcChoice tuned;
     if (plan->autotune && use_cache) {
       TcKey shape = key;
-      shape.A = shape.B = shape.C = 0;
+      shape.A = shape.B = shape.C = shape.Cin = 0;
+      shape.cin_kind = cin.ptr == C ? -1 : cin.kind;  // in place, or a separate C of this kind
       auto t = plan->tuned.find(shape);
       if (t == plan->tuned.end())
-        t = plan->tuned.emplace(shape, autotune(plan, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype,
-                                                ta, tb, epi, s)).first;
+        t = plan->tuned.emplace(shape, autotune(plan, M, N, K, A, lda, B, ldb, C, ldc, cin, alpha, beta,
+                                                dtype, ta, tb, epi, s)).first;
       tuned = t->second;
       forced = &tuned;
       if (plan->tuned.size() > 4096) plan->tuned.clear();  // bounded; re-tuned on next use
     }
-    const gemm_status_t st = build_tc_entry(plan, M, N, K, A, lda, B, ldb, C, ldc, beta != 0.f, dtype,
+    const gemm_status_t st = build_tc_entry(plan, M, N, K, A, lda, B, ldb, C, ldc, cin, beta != 0.f, dtype,
                                             ta, tb, forced, &local);
     if (st != GEMM_OK) return st;
     if (use_cache) {
@@ -904,14 +933,43 @@ gemm_status_t gemm_check_args(int64_t M, int64_t N, int64_t K, const void* A, in
   return check(M, N, K, A, lda, B, ldb, C, ldc, alpha, dtype, transA, transB, epilogue);
 }
 
-gemm_status_t gemm_run(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, const void* A,
-                       int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, float alpha,
-                       float beta, gemm_dtype_t dtype, gemm_op_t transA, gemm_op_t transB,
-                       gemm_epilogue_t epilogue, void* stream) {
-  if (!plan) return GEMM_ERR_INVALID_ARG;
-  const gemm_status_t st =
-      check(M, N, K, A, lda, B, ldb, C, ldc, alpha, dtype, transA, transB, epilogue);
-  if (st != GEMM_OK) return st;
+namespace {
+
+int type_kind(gemm_type_t t) {
+  return t == GEMM_TYPE_F32 ? dg::OUT_F32 : (t == GEMM_TYPE_BF16 ? dg::OUT_BF16 : dg::OUT_F16);
+}
+
+// Arguments of gemm_run_ex; *dtype receives the (operand, output) pair.
+gemm_status_t check_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
+                       int64_t ldb, const void* C, int64_t ldc, gemm_type_t c_type, const void* D,
+                       int64_t ldd, gemm_type_t d_type, float alpha, float beta, gemm_type_t ab_type,
+                       gemm_op_t ta, gemm_op_t tb, gemm_epilogue_t epi, gemm_dtype_t* dtype) {
+  if (ab_type != GEMM_TYPE_BF16 && ab_type != GEMM_TYPE_F16) return GEMM_ERR_INVALID_ARG;
+  if (d_type != GEMM_TYPE_F32 && d_type != ab_type) return GEMM_ERR_INVALID_ARG;
+  if (c_type != GEMM_TYPE_BF16 && c_type != GEMM_TYPE_F16 && c_type != GEMM_TYPE_F32)
+    return GEMM_ERR_INVALID_ARG;
+  const bool f32 = d_type == GEMM_TYPE_F32;
+  *dtype = ab_type == GEMM_TYPE_BF16 ? (f32 ? GEMM_BF16_F32 : GEMM_BF16_BF16)
+                                     : (f32 ? GEMM_F16_F32 : GEMM_F16_F16);
+  // D is held to gemm_run's rules for C
+  const gemm_status_t st = check(M, N, K, A, lda, B, ldb, D, ldd, alpha, *dtype, ta, tb, epi);
+  if (st != GEMM_OK || M == 0 || N == 0 || beta == 0.f) return st;
+  if (C == nullptr || ldc < std::max<int64_t>(1, N)) return GEMM_ERR_INVALID_ARG;
+  const size_t c_es = c_type == GEMM_TYPE_F32 ? 4 : 2, d_es = f32 ? 4 : 2;
+  if (!aligned(C, c_es)) return GEMM_ERR_ALIGNMENT;
+  if (C == D) return ldc == ldd && c_type == d_type ? GEMM_OK : GEMM_ERR_INVALID_ARG;
+  const uintptr_t c0 = reinterpret_cast<uintptr_t>(C), d0 = reinterpret_cast<uintptr_t>(D);
+  const uintptr_t c1 = c0 + (uintptr_t(M - 1) * uintptr_t(ldc) + uintptr_t(N)) * c_es;
+  const uintptr_t d1 = d0 + (uintptr_t(M - 1) * uintptr_t(ldd) + uintptr_t(N)) * d_es;
+  if (c0 < d1 && d0 < c1) return GEMM_ERR_INVALID_ARG;  // a separate C must not overlap D
+  return GEMM_OK;
+}
+
+// Dispatch of a checked call: D <- act(alpha * op(A) @ op(B) + beta * cin).
+gemm_status_t run_all(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                      const void* B, int64_t ldb, void* D, int64_t ldd, const CinRef& cin, float alpha,
+                      float beta, gemm_dtype_t dtype, gemm_op_t transA, gemm_op_t transB,
+                      gemm_epilogue_t epilogue, void* stream) {
   gemm_config_info_t info{};
   info.sms = plan->sms;
   info.splitk = 1;
@@ -922,22 +980,64 @@ gemm_status_t gemm_run(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, const 
   }
   DeviceGuard guard(plan->device);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const dg::EpiParams e{alpha, beta, epilogue.slope, epilogue.act, out_kind(dtype)};
+  const dg::EpiParams e{alpha, beta, epilogue.slope, epilogue.act, out_kind(dtype), cin.kind};
   gemm_status_t r;
   if (K == 0 || alpha == 0.f) {
     info.path = GEMM_PATH_SCALE;
     info.launches = 1;
-    r = dg::launch_scale(int(M), int(N), C, ldc, e, s, plan->sms) == cudaSuccess ? GEMM_OK
-                                                                                  : GEMM_ERR_CUDA;
+    r = dg::launch_scale(int(M), int(N), D, ldd, cin.ptr, cin.ld, e, s, plan->sms) == cudaSuccess
+            ? GEMM_OK
+            : GEMM_ERR_CUDA;
   } else if (M == 1 || N == 1) {
-    r = run_gemv(plan, M, N, K, A, lda, B, ldb, C, ldc, dtype, transA, transB, e, s, &info);
+    r = run_gemv(plan, M, N, K, A, lda, B, ldb, D, ldd, dtype, transA, transB, e, cin, s, &info);
   } else {
-    r = run_tc(plan, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype, transA, transB, epilogue,
+    r = run_tc(plan, M, N, K, A, lda, B, ldb, D, ldd, cin, alpha, beta, dtype, transA, transB, epilogue,
                s, &info);
   }
   if (r != GEMM_OK) cudaGetLastError();
   plan->last = info;
   return r;
+}
+
+}  // namespace
+
+gemm_status_t gemm_run(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, const void* A,
+                       int64_t lda, const void* B, int64_t ldb, void* C, int64_t ldc, float alpha,
+                       float beta, gemm_dtype_t dtype, gemm_op_t transA, gemm_op_t transB,
+                       gemm_epilogue_t epilogue, void* stream) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  const gemm_status_t st =
+      check(M, N, K, A, lda, B, ldb, C, ldc, alpha, dtype, transA, transB, epilogue);
+  if (st != GEMM_OK) return st;
+  const CinRef cin{C, ldc, out_kind(dtype)};
+  return run_all(plan, M, N, K, A, lda, B, ldb, C, ldc, cin, alpha, beta, dtype, transA, transB,
+                 epilogue, stream);
+}
+
+gemm_status_t gemm_run_ex(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, const void* A,
+                          int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc,
+                          gemm_type_t c_type, void* D, int64_t ldd, gemm_type_t d_type, float alpha,
+                          float beta, gemm_type_t ab_type, gemm_op_t transA, gemm_op_t transB,
+                          gemm_epilogue_t epilogue, void* stream) {
+  if (!plan) return GEMM_ERR_INVALID_ARG;
+  gemm_dtype_t dtype = GEMM_BF16_F32;
+  const gemm_status_t st = check_ex(M, N, K, A, lda, B, ldb, C, ldc, c_type, D, ldd, d_type, alpha, beta,
+                                    ab_type, transA, transB, epilogue, &dtype);
+  if (st != GEMM_OK) return st;
+  // with beta == 0 C is not read: the output stands in for it
+  const CinRef cin = beta != 0.f ? CinRef{C, ldc, type_kind(c_type)} : CinRef{D, ldd, out_kind(dtype)};
+  return run_all(plan, M, N, K, A, lda, B, ldb, D, ldd, cin, alpha, beta, dtype, transA, transB,
+                 epilogue, stream);
+}
+
+gemm_status_t gemm_check_args_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                                 const void* B, int64_t ldb, const void* C, int64_t ldc,
+                                 gemm_type_t c_type, const void* D, int64_t ldd, gemm_type_t d_type,
+                                 float alpha, float beta, gemm_type_t ab_type, gemm_op_t transA,
+                                 gemm_op_t transB, gemm_epilogue_t epilogue) {
+  gemm_dtype_t dtype = GEMM_BF16_F32;
+  return check_ex(M, N, K, A, lda, B, ldb, C, ldc, c_type, D, ldd, d_type, alpha, beta, ab_type, transA,
+                  transB, epilogue, &dtype);
 }
 
 gemm_status_t gemm_plan_last_config(gemm_plan_t plan, gemm_config_info_t* out) {

@@ -127,12 +127,6 @@ __device__ __forceinline__ Unit decode_unit(int u, const TcParams& p) {
   return x;
 }
 
-__device__ __forceinline__ float epi_value(float acc, float c, const TcParams& p, bool has_beta) {
-  float v = p.alpha * acc;
-  if (has_beta) v = fmaf(p.beta, c, v);
-  return apply_act(v, p.act, p.slope);
-}
-
 __device__ __forceinline__ uint32_t pack2(float a, float b, int out_kind) {
   if (out_kind == OUT_BF16) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
@@ -151,26 +145,103 @@ __device__ __forceinline__ float2 unpack2(uint32_t w, int out_kind) {
   return __half22float2(h);
 }
 
-// 16 bytes of C starting at (row, col), col a multiple of 16 / esize; zero
-// outside the matrix.  C and ldc * esize are 16-byte multiples on this path.
-__device__ __forceinline__ uint4 load_c16(const TcParams& p, int row, int col, int esize) {
-  uint4 v = make_uint4(0u, 0u, 0u, 0u);
-  if (row >= p.M || col >= p.N) return v;
-  const int per = 16 / esize;
-  const uint8_t* src = static_cast<const uint8_t*>(p.c_ptr) + (int64_t(row) * p.ldc + col) * esize;
-  if (col + per <= p.N) return *reinterpret_cast<const uint4*>(src);
-  // ragged end of the row
-  uint32_t w[4] = {0u, 0u, 0u, 0u};
+// Four consecutive values of the C that beta scales, at (row, col .. col+3),
+// as fp32; zero outside the matrix.  One 16- or 8-byte load when aligned.
+__device__ __forceinline__ float4 load_cin4(const TcParams& p, int row, int col) {
+  float v[4] = {0.f, 0.f, 0.f, 0.f};
+  if (row < p.M && col < p.N) {
+    const int es = p.cin_kind == OUT_F32 ? 4 : 2;
+    const uint8_t* src = static_cast<const uint8_t*>(p.cin) + (int64_t(row) * p.ldcin + col) * es;
+    if (col + 4 <= p.N && (reinterpret_cast<uintptr_t>(src) & uintptr_t(4 * es - 1)) == 0) {
+      if (es == 4) return *reinterpret_cast<const float4*>(src);
+      const uint2 w = *reinterpret_cast<const uint2*>(src);
+      const float2 lo = unpack2(w.x, p.cin_kind), hi = unpack2(w.y, p.cin_kind);
+      return make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    if (i < per && col + i < p.N) {
-      if (esize == 4)
-        w[i & 3] = reinterpret_cast<const uint32_t*>(src)[i];
-      else
-        w[i >> 1] |= uint32_t(reinterpret_cast<const uint16_t*>(src)[i]) << (16 * (i & 1));
+    for (int i = 0; i < 4; ++i) {
+      if (col + i < p.N) {
+        if (es == 4) {
+          v[i] = reinterpret_cast<const float*>(src)[i];
+        } else {
+          const uint32_t h = reinterpret_cast<const uint16_t*>(src)[i];
+          v[i] = unpack2(h, p.cin_kind).x;
+        }
+      }
     }
   }
-  return make_uint4(w[0], w[1], w[2], w[3]);
+  return make_float4(v[0], v[1], v[2], v[3]);
+}
+
+// Where the C that beta scales comes from, for one row segment.
+enum CSource : int {
+  C_NONE = 0,    // beta == 0: C is not read
+  C_STAGED = 1,  // C is the output, TMA-loaded into the lane's staging line
+  C_DIRECT = 2   // a separate C (or a K pair's), read from global memory
+};
+
+// v <- act(alpha * v + beta * C) on the 32 consecutive columns [col0, col0+32)
+// of output row `row`.  C_STAGED: the 32 values start at 16-byte chunk
+// `chunk0` of the lane's swizzled 128-byte staging line, in the output's
+// format (esize bytes each).  Every run-time choice is taken once, outside
+// the unrolled loops, so the path a launch takes is straight-line code (the
+// epilogue shares the SM's instruction cache with the producer and MMA warps).
+__device__ __forceinline__ void epi32(float (&v)[32], const TcParams& p, int csrc, const uint8_t* row_p,
+                                      int sw, int chunk0, int esize, int row, int col0) {
+  if (csrc == C_NONE) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= p.alpha;
+  } else if (csrc == C_STAGED && esize == 4) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 c = *reinterpret_cast<const float4*>(row_p + (((chunk0 + j) ^ sw) << 4));
+      v[4 * j + 0] = fmaf(p.beta, c.x, p.alpha * v[4 * j + 0]);
+      v[4 * j + 1] = fmaf(p.beta, c.y, p.alpha * v[4 * j + 1]);
+      v[4 * j + 2] = fmaf(p.beta, c.z, p.alpha * v[4 * j + 2]);
+      v[4 * j + 3] = fmaf(p.beta, c.w, p.alpha * v[4 * j + 3]);
+    }
+  } else if (csrc == C_STAGED) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint4 c = *reinterpret_cast<const uint4*>(row_p + (((chunk0 + j) ^ sw) << 4));
+      const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float2 cc = unpack2(w[t], p.out_kind);
+        v[8 * j + 2 * t] = fmaf(p.beta, cc.x, p.alpha * v[8 * j + 2 * t]);
+        v[8 * j + 2 * t + 1] = fmaf(p.beta, cc.y, p.alpha * v[8 * j + 2 * t + 1]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float4 c = load_cin4(p, row, col0 + 4 * j);
+      v[4 * j + 0] = fmaf(p.beta, c.x, p.alpha * v[4 * j + 0]);
+      v[4 * j + 1] = fmaf(p.beta, c.y, p.alpha * v[4 * j + 1]);
+      v[4 * j + 2] = fmaf(p.beta, c.z, p.alpha * v[4 * j + 2]);
+      v[4 * j + 3] = fmaf(p.beta, c.w, p.alpha * v[4 * j + 3]);
+    }
+  }
+  switch (p.act) {
+    case 0:
+      break;
+    case 1:
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = v[i] < 0.f ? v[i] * p.slope : v[i];
+      break;
+    case 2:
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = v[i] < 0.f ? 0.f : v[i];
+      break;
+    case 3:
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = apply_act(v[i], 3, 0.f);
+      break;
+    default:
+#pragma unroll
+      for (int i = 0; i < 32; ++i) v[i] = apply_act(v[i], 4, 0.f);
+      break;
+  }
 }
 
 template <int BN, int MODE>
@@ -458,23 +529,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             uint32_t r[32];
             tmem_ld_32x32b_x32(t_row + own_c + 32 * c, r);
             tmem_ld_wait(r);
+            float v[32];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              float4* slot = reinterpret_cast<float4*>(row_p + ((j ^ sw) << 4));
-              const float4 pv = *slot;
-              float4 cv = make_float4(0.f, 0.f, 0.f, 0.f);
-              if (has_beta) {
-                const uint4 cw = load_c16(p, row, x0 + 4 * j, 4);
-                cv = make_float4(__uint_as_float(cw.x), __uint_as_float(cw.y), __uint_as_float(cw.z),
-                                 __uint_as_float(cw.w));
-              }
-              float4 o;
-              o.x = epi_value(__uint_as_float(r[4 * j + 0]) + pv.x, cv.x, p, has_beta);
-              o.y = epi_value(__uint_as_float(r[4 * j + 1]) + pv.y, cv.y, p, has_beta);
-              o.z = epi_value(__uint_as_float(r[4 * j + 2]) + pv.z, cv.z, p, has_beta);
-              o.w = epi_value(__uint_as_float(r[4 * j + 3]) + pv.w, cv.w, p, has_beta);
-              *slot = o;
+            for (int j = 0; j < 8; ++j) {  // own partial sums + the peer's
+              const float4 pv = *reinterpret_cast<const float4*>(row_p + ((j ^ sw) << 4));
+              v[4 * j + 0] = __uint_as_float(r[4 * j + 0]) + pv.x;
+              v[4 * j + 1] = __uint_as_float(r[4 * j + 1]) + pv.y;
+              v[4 * j + 2] = __uint_as_float(r[4 * j + 2]) + pv.z;
+              v[4 * j + 3] = __uint_as_float(r[4 * j + 3]) + pv.w;
             }
+            epi32(v, p, has_beta ? C_DIRECT : C_NONE, row_p, sw, 0, 4, row, x0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<float4*>(row_p + ((j ^ sw) << 4)) =
+                  make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
             const int tail_lo = max(x0, p.n_tma), tail_hi = min(x0 + 32, p.N);
             if (tail_lo < tail_hi && row < p.M) {
               for (int col = tail_lo; col < tail_hi; ++col) {
@@ -510,22 +578,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             pv[4 * j + 2] = v.z;
             pv[4 * j + 3] = v.w;
           }
+          float v0[32], v1[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {  // own partial sums + the peer's
+            v0[i] = __uint_as_float(r0[i]) + pv[i];
+            v1[i] = __uint_as_float(r1[i]) + pv[32 + i];
+          }
+          const int csrc = has_beta ? C_DIRECT : C_NONE;
+          epi32(v0, p, csrc, row_p, sw, 0, 2, row, x0);
+          epi32(v1, p, csrc, row_p, sw, 4, 2, row, x0 + 32);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            uint4 cv = make_uint4(0u, 0u, 0u, 0u);
-            if (has_beta) cv = load_c16(p, row, x0 + 8 * j, 2);
-            const uint32_t* src = j < 4 ? &r0[8 * j] : &r1[8 * (j - 4)];
-            const uint32_t cw4[4] = {cv.x, cv.y, cv.z, cv.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const float2 cc = unpack2(cw4[t], p.out_kind);
-              const float a = epi_value(__uint_as_float(src[2 * t]) + pv[8 * j + 2 * t], cc.x, p, has_beta);
-              const float b = epi_value(__uint_as_float(src[2 * t + 1]) + pv[8 * j + 2 * t + 1], cc.y, p,
-                                        has_beta);
-              o[t] = pack2(a, b, p.out_kind);
-            }
-            *reinterpret_cast<uint4*>(row_p + ((j ^ sw) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            const float* h = j < 4 ? &v0[8 * (j & 3)] : &v1[8 * (j & 3)];
+            *reinterpret_cast<uint4*>(row_p + ((j ^ sw) << 4)) =
+                make_uint4(pack2(h[0], h[1], p.out_kind), pack2(h[2], h[3], p.out_kind),
+                           pack2(h[4], h[5], p.out_kind), pack2(h[6], h[7], p.out_kind));
           }
           const int tail_lo = max(x0, p.n_tma), tail_hi = min(x0 + 64, p.N);
           if (tail_lo < tail_hi && row < p.M) {
@@ -575,6 +642,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       // stores the epilogue's result into C.
       const bool partial = x.partial;
       const bool has_beta = !partial && p.beta != 0.f;
+      // beta's C through the output's tensor map (it is the output), or with
+      // plain loads (a separate C of its own type and leading dimension)
+      const bool c_tma = has_beta && !p.cin_direct;
+      const int csrc = c_tma ? C_STAGED : (has_beta ? C_DIRECT : C_NONE);
       const int esize = (partial || p.out_kind == OUT_F32) ? 4 : 2;
       const int cw = 128 / esize;  // columns per 128-byte box row
       const CUtensorMap* const out_map = partial ? &tmW : &tmC;
@@ -597,7 +668,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const bool has_tail = !partial && tail_lo < tail_hi && row < p.M;
         if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
         __syncwarp();
-        if (has_beta && tma_cols) {
+        if (c_tma && tma_cols) {
           if (lane == 0) {
             mbar_arrive_expect_tx(cload0 + 8 * e, Cfg::STG_BYTES);
             tma_load_2d(stg, &tmC, cload0 + 8 * e, x0, y0);
@@ -611,7 +682,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         __syncwarp();
         uint8_t* const row_p = stg_p + lane * 128;
         const int sw = lane & 7;  // 128-byte swizzle: 16-byte chunk j lives at j ^ (row % 8)
-        if (has_beta && has_tail) {
+        if (c_tma && has_tail) {
           for (int col = tail_lo; col < tail_hi; ++col) {
             const int b = (col - x0) * esize;
             uint8_t* dst = row_p + ((((b >> 4) ^ sw)) << 4) + (b & 15);
@@ -626,45 +697,34 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           uint32_t r[32];
           tmem_ld_32x32b_x32(t_row + c * 32, r);
           tmem_ld_wait(r);
+          float v[32];
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            float4* dst = reinterpret_cast<float4*>(row_p + ((j ^ sw) << 4));
-            float4 cv = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (has_beta) cv = *dst;
-            float4 o;
-            if (partial) {
-              o = make_float4(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                              __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-            } else {
-              o.x = epi_value(__uint_as_float(r[4 * j + 0]), cv.x, p, has_beta);
-              o.y = epi_value(__uint_as_float(r[4 * j + 1]), cv.y, p, has_beta);
-              o.z = epi_value(__uint_as_float(r[4 * j + 2]), cv.z, p, has_beta);
-              o.w = epi_value(__uint_as_float(r[4 * j + 3]), cv.w, p, has_beta);
-            }
-            *dst = o;
-          }
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          if (!partial) epi32(v, p, csrc, row_p, sw, 0, 4, row, x0);  // partials stay raw
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(row_p + ((j ^ sw) << 4)) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         } else {
           uint32_t r0[32], r1[32];
           tmem_ld_32x32b_x32(t_row + c * 64, r0);
           tmem_ld_32x32b_x32(t_row + c * 64 + 32, r1);
           tmem_ld_wait(r0);
           tmem_ld_wait(r1);
+          float v0[32], v1[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            v0[i] = __uint_as_float(r0[i]);
+            v1[i] = __uint_as_float(r1[i]);
+          }
+          epi32(v0, p, csrc, row_p, sw, 0, 2, row, x0);  // (16-bit output: never a partial unit)
+          epi32(v1, p, csrc, row_p, sw, 4, 2, row, x0 + 32);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            uint4* dst = reinterpret_cast<uint4*>(row_p + ((j ^ sw) << 4));
-            uint4 cv = make_uint4(0u, 0u, 0u, 0u);
-            if (has_beta) cv = *dst;
-            const uint32_t* src = j < 4 ? &r0[8 * j] : &r1[8 * (j - 4)];
-            const uint32_t cw4[4] = {cv.x, cv.y, cv.z, cv.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-              const float2 cc = unpack2(cw4[t], p.out_kind);
-              const float a = epi_value(__uint_as_float(src[2 * t]), cc.x, p, has_beta);
-              const float b = epi_value(__uint_as_float(src[2 * t + 1]), cc.y, p, has_beta);
-              o[t] = pack2(a, b, p.out_kind);
-            }
-            *dst = make_uint4(o[0], o[1], o[2], o[3]);
+            const float* h = j < 4 ? &v0[8 * (j & 3)] : &v1[8 * (j & 3)];
+            *reinterpret_cast<uint4*>(row_p + ((j ^ sw) << 4)) =
+                make_uint4(pack2(h[0], h[1], p.out_kind), pack2(h[2], h[3], p.out_kind),
+                           pack2(h[4], h[5], p.out_kind), pack2(h[6], h[7], p.out_kind));
           }
         }
         if (has_tail) {

@@ -84,10 +84,11 @@ __device__ __forceinline__ void store_c(void* C, int64_t idx, float v, int kind)
   }
 }
 
-// alpha*acc + beta*C (C not read when beta == 0), then the activation.
+// alpha*acc + beta*C[idx] (C, of kind e.cin_kind, not read when beta == 0),
+// then the activation.
 __device__ __forceinline__ float epilogue(float acc, const void* C, int64_t idx, const EpiParams& e) {
   float v = e.alpha * acc;
-  if (e.beta != 0.f) v = fmaf(e.beta, load_c(C, idx, e.out_kind), v);
+  if (e.beta != 0.f) v = fmaf(e.beta, load_c(C, idx, e.cin_kind), v);
   v = apply_act(v, e.act, e.slope);
   return v;
 }
@@ -145,8 +146,8 @@ __global__ void __launch_bounds__(kRowdotThreads)
       a1 = fmaf(to_f<F16>(wrow[k]), to_f<F16>(kXDirect ? x[k] : xs[k]), a1);
     const float acc = warp_sum(a0 + a1);
     if (lane == 0) {
-      const int64_t idx = static_cast<int64_t>(r) * g.inc_out;
-      store_c(g.out, idx, epilogue(acc, g.out, idx, g.e), g.e.out_kind);
+      store_c(g.out, static_cast<int64_t>(r) * g.inc_out,
+              epilogue(acc, g.cin, static_cast<int64_t>(r) * g.inc_cin, g.e), g.e.out_kind);
     }
   }
 }
@@ -237,8 +238,8 @@ __global__ void __launch_bounds__(kColThreads)
     for (int q = 1; q < kColGroups; ++q) s += red[q][c];
     if (col < g.R) {
       if (cp.ksplit == 1) {
-        const int64_t idx = static_cast<int64_t>(col) * g.inc_out;
-        store_c(g.out, idx, epilogue(s, g.out, idx, g.e), g.e.out_kind);
+        store_c(g.out, static_cast<int64_t>(col) * g.inc_out,
+                epilogue(s, g.cin, static_cast<int64_t>(col) * g.inc_cin, g.e), g.e.out_kind);
       } else {
         ws[static_cast<int64_t>(z) * rpad + col] = s;
       }
@@ -290,8 +291,8 @@ __global__ void __launch_bounds__(kColThreads)
     const int col = panel * kColCols + c;
     if (col >= g.R) break;
     const float s = half[c] + half[kColCols + c];
-    const int64_t idx = static_cast<int64_t>(col) * g.inc_out;
-    store_c(g.out, idx, epilogue(s, g.out, idx, g.e), g.e.out_kind);
+    store_c(g.out, static_cast<int64_t>(col) * g.inc_out,
+            epilogue(s, g.cin, static_cast<int64_t>(col) * g.inc_cin, g.e), g.e.out_kind);
   }
   if (threadIdx.x == 0) counters[panel] = 0u;
 }
@@ -312,8 +313,8 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvArgs g) {
                  to_f<F16>(x[static_cast<int64_t>(k) * g.incx]), acc);
     acc = warp_sum(acc);
     if (lane == 0) {
-      const int64_t idx = static_cast<int64_t>(r) * g.inc_out;
-      store_c(g.out, idx, epilogue(acc, g.out, idx, g.e), g.e.out_kind);
+      store_c(g.out, static_cast<int64_t>(r) * g.inc_out,
+              epilogue(acc, g.cin, static_cast<int64_t>(r) * g.inc_cin, g.e), g.e.out_kind);
     }
   }
 }
@@ -333,6 +334,8 @@ __global__ void __launch_bounds__(256) tile_reduce_kernel(const TileReduceArgs a
   const int64_t slice = static_cast<int64_t>(a.tail_tiles) * a.tile_m * a.tile_n;
   void* const C = a.C;
   const int N = a.N;
+  // beta scales the output itself: 16- or 8-byte read-modify-write of 4 outputs
+  const bool in_place = a.Cin == a.C && a.ldcin == a.ldc && e.cin_kind == e.out_kind;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int t = static_cast<int>(i / per_tile);
@@ -357,9 +360,11 @@ __global__ void __launch_bounds__(256) tile_reduce_kernel(const TileReduceArgs a
     const int64_t base = static_cast<int64_t>(m) * a.ldc + n;
     const int nn = min(4, N - n);
     const int esz = e.out_kind == OUT_F32 ? 4 : 2;
-    const bool vec = nn == 4 && ((reinterpret_cast<uintptr_t>(C) + base * esz) & (4 * esz - 1)) == 0;
+    const bool vec = in_place && nn == 4 &&
+                     ((reinterpret_cast<uintptr_t>(C) + base * esz) & (4 * esz - 1)) == 0;
     if (!vec) {
-      for (int j = 0; j < nn; ++j) store_c(C, base + j, epilogue(sv[j], C, base + j, e), e.out_kind);
+      const int64_t cbase = static_cast<int64_t>(m) * a.ldcin + n;
+      for (int j = 0; j < nn; ++j) store_c(C, base + j, epilogue(sv[j], a.Cin, cbase + j, e), e.out_kind);
       continue;
     }
     // Four adjacent outputs with one 16-byte (fp32) or 8-byte (16-bit) access.
@@ -400,16 +405,16 @@ __global__ void __launch_bounds__(256) tile_reduce_kernel(const TileReduceArgs a
 }
 
 // ------------------------------------------------------------------- scale
-__global__ void __launch_bounds__(256) scale_kernel(int M, int N, void* C, int64_t ldc, const EpiParams e) {
+__global__ void __launch_bounds__(256) scale_kernel(int M, int N, void* D, int64_t ldd, const void* C,
+                                                    int64_t ldc, const EpiParams e) {
   const int64_t total = static_cast<int64_t>(M) * N;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int m = static_cast<int>(i / N);
     const int n = static_cast<int>(i - static_cast<int64_t>(m) * N);
-    const int64_t idx = static_cast<int64_t>(m) * ldc + n;
-    float v = e.beta != 0.f ? e.beta * load_c(C, idx, e.out_kind) : 0.f;
+    float v = e.beta != 0.f ? e.beta * load_c(C, static_cast<int64_t>(m) * ldc + n, e.cin_kind) : 0.f;
     v = apply_act(v, e.act, e.slope);
-    store_c(C, idx, v, e.out_kind);
+    store_c(D, static_cast<int64_t>(m) * ldd + n, v, e.out_kind);
   }
 }
 
@@ -514,9 +519,10 @@ cudaError_t launch_tile_reduce(const TileReduceArgs& a, cudaStream_t s, int sms)
   return cudaLaunchKernelEx(&cfg, tile_reduce_kernel, a);
 }
 
-cudaError_t launch_scale(int M, int N, void* C, int64_t ldc, EpiParams e, cudaStream_t s, int sms) {
+cudaError_t launch_scale(int M, int N, void* D, int64_t ldd, const void* C, int64_t ldc, EpiParams e,
+                         cudaStream_t s, int sms) {
   const int64_t items = static_cast<int64_t>(M) * N;
-  scale_kernel<<<grid_for(items, 256, sms, 8), 256, 0, s>>>(M, N, C, ldc, e);
+  scale_kernel<<<grid_for(items, 256, sms, 8), 256, 0, s>>>(M, N, D, ldd, C, ldc, e);
   return cudaGetLastError();
 }
 

@@ -72,9 +72,16 @@ struct TcParams {
   int kb_per_split;  // k-blocks per slice (the last one may be shorter); a K pair: per half
   int units;         // dp_units + tail_tiles * splitk (a K pair: tiles)
   int out_kind;      // OutKind of C
-  int n_tma;         // columns [0, n_tma) of C go through TMA (a 16-byte multiple per row)
-  void* c_ptr;       // C, for the columns [n_tma, N) written directly
+  int n_tma;         // columns [0, n_tma) of the output go through TMA (a 16-byte multiple per row)
+  void* c_ptr;       // the output (C, or D of gemm_run_ex), for columns [n_tma, N) written directly
   int64_t ldc;
+  // The C that beta scales: the output itself (cin == c_ptr, read through the
+  // output's tensor map) or, with cin_direct, a separate matrix of kind
+  // cin_kind read with plain loads.
+  const void* cin;
+  int64_t ldcin;
+  int cin_kind;
+  int cin_direct;
   int a_mn_major;    // A stored K x M (M contiguous)
   int b_mn_major;    // B stored K x N (N contiguous)
   uint32_t idesc;    // tcgen05 instruction descriptor
@@ -119,7 +126,8 @@ __device__ __forceinline__ float apply_act(float v, int act, float slope) {
 struct EpiParams {
   float alpha, beta, slope;
   int act;
-  int out_kind;  // OUT_F32 / OUT_BF16 / OUT_F16
+  int out_kind;  // OUT_F32 / OUT_BF16 / OUT_F16 of the output
+  int cin_kind;  // of the C that beta scales
 };
 
 // Fixed-order sum of the K slices of the tail tiles of a tensor-core call
@@ -131,15 +139,17 @@ struct TileReduceArgs {
   int tile_m, tile_n;
   int num_m_blocks, num_n_blocks, raster_group;
   int M, N;
-  void* C;
+  void* C;  // output
   int64_t ldc;
+  const void* Cin;  // the C that beta scales (may be the output)
+  int64_t ldcin;
   EpiParams e;
 };
 cudaError_t launch_tile_reduce(const TileReduceArgs& a, cudaStream_t s, int sms);
 
-// C <- act(beta * C) (K == 0 or alpha == 0).
-cudaError_t launch_scale(int M, int N, void* C, int64_t ldc, EpiParams e, cudaStream_t s,
-                         int sms);
+// D <- act(beta * C) (K == 0 or alpha == 0); C may be D.
+cudaError_t launch_scale(int M, int N, void* D, int64_t ldd, const void* C, int64_t ldc, EpiParams e,
+                         cudaStream_t s, int sms);
 
 // GEMV, operand type in_f16 (0 = bf16, 1 = fp16).
 // rowdot:    out[r*inc_out] = epi(sum_k W[r*ldw + k] * x[k*incx]),  r < R
@@ -154,6 +164,8 @@ struct GemvArgs {
   int64_t incx;
   void* out;
   int64_t inc_out;
+  const void* cin;  // the C that beta scales, element r at cin[r * inc_cin] (may be out)
+  int64_t inc_cin;
   int in_f16;
   EpiParams e;
 };

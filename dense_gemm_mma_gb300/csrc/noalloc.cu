@@ -93,10 +93,10 @@ extern "C" gemm_status_t gemm_gemv_noalloc(int64_t M, int64_t N, int64_t K, cons
   g.K = int(K);
   g.in_f16 = (dtype == GEMM_F16_F32 || dtype == GEMM_F16_F16) ? 1 : 0;
   g.out = C;
-  g.e = dg::EpiParams{alpha, beta, epilogue.slope, epilogue.act,
-                      dtype == GEMM_BF16_F32 || dtype == GEMM_F16_F32
-                          ? dg::OUT_F32
-                          : (dtype == GEMM_BF16_BF16 ? dg::OUT_BF16 : dg::OUT_F16)};
+  const int kind = dtype == GEMM_BF16_F32 || dtype == GEMM_F16_F32
+                       ? dg::OUT_F32
+                       : (dtype == GEMM_BF16_BF16 ? dg::OUT_BF16 : dg::OUT_F16);
+  g.e = dg::EpiParams{alpha, beta, epilogue.slope, epilogue.act, kind, kind};  // beta scales C itself
   if (N == 1 && transA == GEMM_OP_T) {
     g.R = int(M);
     g.inc_out = ldc;
@@ -114,6 +114,8 @@ extern "C" gemm_status_t gemm_gemv_noalloc(int64_t M, int64_t N, int64_t K, cons
   } else {
     return GEMM_ERR_UNSUPPORTED;
   }
+  g.cin = C;
+  g.inc_cin = g.inc_out;
   if (!aligned16(g.W) || ((g.ldw * 2) % 16 != 0 && K != 1)) return GEMM_ERR_UNSUPPORTED;
 
   int dev = -1;

@@ -23,6 +23,7 @@ GEMM_ERR_CUDA = 6
 GEMM_ERR_TIMEOUT = 7
 
 GEMM_OP_N, GEMM_OP_T = 0, 1
+GEMM_TYPE_BF16, GEMM_TYPE_F16, GEMM_TYPE_F32 = 0, 1, 2
 GEMM_BF16_F32, GEMM_BF16_BF16, GEMM_F16_F32, GEMM_F16_F16 = 0, 1, 2, 3
 GEMM_ACT_NONE, GEMM_ACT_LEAKY_RELU, GEMM_ACT_RELU, GEMM_ACT_GELU, GEMM_ACT_SILU = 0, 1, 2, 3, 4
 
@@ -83,6 +84,10 @@ _SIGNATURES = {
     "gemm_gemv_noalloc": (_I32, [_I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64, _F, _F,
                                  _I32, _I32, _I32, gemm_epilogue_t, _VP]),
     "gemm_plan_set_autotune": (_I32, [_VP, ctypes.c_int]),
+    "gemm_run_ex": (_I32, [_VP, _I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64, _I32, _VP, _I64, _I32,
+                           _F, _F, _I32, _I32, _I32, gemm_epilogue_t, _VP]),
+    "gemm_check_args_ex": (_I32, [_I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64, _I32, _VP, _I64, _I32,
+                                  _F, _F, _I32, _I32, _I32, gemm_epilogue_t]),
     "gemm_plan_tuned_count": (_I32, [_VP, ctypes.POINTER(_I64)]),
 }
 
@@ -130,6 +135,18 @@ def gemm_run(plan, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype, transA, 
              act=GEMM_ACT_NONE, slope=0.0, stream=None) -> int:
     return load().gemm_run(plan, M, N, K, A, lda, B, ldb, C, ldc, alpha, beta, dtype,
                            transA, transB, gemm_epilogue_t(act, slope), stream)
+
+
+def gemm_run_ex(plan, M, N, K, A, lda, B, ldb, C, ldc, c_type, D, ldd, d_type, alpha, beta, ab_type,
+                transA, transB, act=GEMM_ACT_NONE, slope=0.0, stream=None) -> int:
+    return load().gemm_run_ex(plan, M, N, K, A, lda, B, ldb, C, ldc, c_type, D, ldd, d_type, alpha, beta,
+                              ab_type, transA, transB, gemm_epilogue_t(act, slope), stream)
+
+
+def gemm_check_args_ex(M, N, K, A, lda, B, ldb, C, ldc, c_type, D, ldd, d_type, alpha, beta, ab_type,
+                       transA, transB, act=GEMM_ACT_NONE, slope=0.0) -> int:
+    return load().gemm_check_args_ex(M, N, K, A, lda, B, ldb, C, ldc, c_type, D, ldd, d_type, alpha, beta,
+                                     ab_type, transA, transB, gemm_epilogue_t(act, slope))
 
 
 def gemm_plan_last_config(plan) -> gemm_config_info_t:

@@ -186,6 +186,34 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
 /* Static, human-readable text for a status code. */
 const char* gemm_status_string(gemm_status_t status);
 
+/* Element types of gemm_run_ex's matrices. */
+typedef enum { GEMM_TYPE_BF16 = 0, GEMM_TYPE_F16 = 1, GEMM_TYPE_F32 = 2 } gemm_type_t;
+
+/* D <- act(alpha * op(A) @ op(B) + beta * C) with a separate output D: the
+ * gemm_run operation where the C that beta scales is read from one matrix and
+ * the result written to another, each with its own leading dimension and
+ * element type (e.g. fp32 C in, bf16 D out).
+ *   ab_type  GEMM_TYPE_BF16 or GEMM_TYPE_F16: A and B, as in gemm_run.
+ *   d_type   GEMM_TYPE_F32 or ab_type: D (M x N, row stride ldd >= N), held to
+ *            gemm_run's rules for C (device pointer, alignment, NULL only
+ *            if M*N == 0).
+ *   c_type   GEMM_TYPE_BF16, GEMM_TYPE_F16 or GEMM_TYPE_F32: C (M x N, row
+ *            stride ldc >= N), read only when beta != 0 (it may then be NULL
+ *            and ldc is ignored); it needs only its element alignment.  C may
+ *            be D itself (same pointer, ldc == ldd, c_type == d_type: that is
+ *            gemm_run); otherwise the two must not overlap.
+ * Violations return GEMM_ERR_INVALID_ARG or GEMM_ERR_ALIGNMENT before any
+ * launch.  Paths, workspace, streams and errors as in gemm_run; the plan's
+ * last configuration is updated the same way.  The pages fuse input and
+ * output transforms into the product ("OpenAI open-sources the Triton GPU
+ * language (part 2)", section Matrix multiplication); a separate D is the
+ * output side of that with C left intact. */
+gemm_status_t gemm_run_ex(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, const void* A,
+                          int64_t lda, const void* B, int64_t ldb, const void* C, int64_t ldc,
+                          gemm_type_t c_type, void* D, int64_t ldd, gemm_type_t d_type, float alpha,
+                          float beta, gemm_type_t ab_type, gemm_op_t transA, gemm_op_t transB,
+                          gemm_epilogue_t epilogue, void* stream);
+
 /* Decisions of the plan's most recent gemm_run (path, tile, split-K, grid,
  * waves, tail fraction, kernels launched).  GEMM_ERR_INVALID_ARG on NULL. */
 gemm_status_t gemm_plan_last_config(gemm_plan_t plan, gemm_config_info_t* out);
@@ -235,6 +263,13 @@ gemm_status_t gemm_check_args(int64_t M, int64_t N, int64_t K,
                               const void* C, int64_t ldc, float alpha,
                               gemm_dtype_t dtype, gemm_op_t transA, gemm_op_t transB,
                               gemm_epilogue_t epilogue);
+
+/* The argument checks of gemm_run_ex without a plan or a device. */
+gemm_status_t gemm_check_args_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                                 const void* B, int64_t ldb, const void* C, int64_t ldc,
+                                 gemm_type_t c_type, const void* D, int64_t ldd, gemm_type_t d_type,
+                                 float alpha, float beta, gemm_type_t ab_type, gemm_op_t transA,
+                                 gemm_op_t transB, gemm_epilogue_t epilogue);
 
 /* The planner of gemm_run as a pure host function: the decisions it would
  * make for this problem on a GPU with `sms` multiprocessors.  Does not need a

@@ -200,3 +200,84 @@ def run_case(plan, M, N, K, in_fmt="bf16", out_fmt="f32", ta=False, tb=False, al
                 os.environ.pop(k, None)
             else:
                 os.environ[k] = v
+
+
+TYPES = {"bf16": gemm.GEMM_TYPE_BF16, "f16": gemm.GEMM_TYPE_F16, "f32": gemm.GEMM_TYPE_F32}
+
+
+def run_case_ex(plan, M, N, K, in_fmt="bf16", c_fmt="f32", d_fmt="bf16", ta=False, tb=False, alpha=1.0,
+                beta=0.5, act=0, slope=0.0, seed=1, pad=(0, 0, 0, 0), sample=None, env=None, c_none=False):
+    """gemm_run_ex with a separate C (c_fmt, row stride ldc) and output D
+    (d_fmt, ldd): D is compared with the oracle as run_case compares C, C
+    must come back bitwise unchanged, and D's row padding (NaN sentinels)
+    must not be written."""
+    import torch
+    old_env = {}
+    for k, v in (env or {}).items():
+        old_env[k] = os.environ.get(k)
+        os.environ[k] = v
+    try:
+        a_rows, a_cols = (K, M) if ta else (M, K)
+        b_rows, b_cols = (N, K) if tb else (K, N)
+        ie = ESIZE[in_fmt]
+        lda = round_up(max(a_cols, 1), 16 // ie) + pad[0]
+        ldb = round_up(max(b_cols, 1), 16 // ie) + pad[1]
+        ldc = max(N, 1) + pad[2]                       # a separate C needs no 16-byte rows
+        ldd = round_up(max(N, 1), 16 // ESIZE[d_fmt]) + pad[3]
+        A = inputs.matrix(a_rows, a_cols, seed, inputs.TENSOR_A, in_fmt, ld=lda)
+        B = inputs.matrix(b_rows, b_cols, seed, inputs.TENSOR_B, in_fmt, ld=ldb)
+        C0 = inputs.matrix(M, N, seed, inputs.TENSOR_C, c_fmt, ld=ldc)
+        nan = {"bf16": inputs.BF16_NAN, "f16": inputs.F16_NAN, "f32": np.float32(np.nan)}[d_fmt]
+        D0 = np.full((M, ldd), nan, dtype=np.float32 if d_fmt == "f32" else np.uint16)
+        Ad, Bd, Cd, Dd = (to_device(A, in_fmt), to_device(B, in_fmt), to_device(C0, c_fmt),
+                          to_device(D0, d_fmt))
+        stream = torch.cuda.current_stream().cuda_stream
+        st = gemm.gemm_run_ex(plan.handle, M, N, K, Ad.data_ptr(), lda, Bd.data_ptr(), ldb,
+                              None if c_none else Cd.data_ptr(), ldc, TYPES[c_fmt], Dd.data_ptr(), ldd,
+                              TYPES[d_fmt], alpha, beta, TYPES[in_fmt], int(ta), int(tb), act, slope, stream)
+        assert st == gemm.GEMM_OK, gemm.gemm_status_string(st)
+        torch.cuda.synchronize()
+        assert plan.poll_error() == gemm.GEMM_OK, "watchdog fired"
+        res = Result()
+        res.info = plan.last_config()
+        C_after = from_device(Cd, c_fmt).reshape(M, ldc)
+        assert np.array_equal(C_after.view(np.uint8), C0.view(np.uint8)), "C was modified"
+        D = from_device(Dd, d_fmt).reshape(M, ldd)
+        if ldd > N:
+            assert np.array_equal(D[:, N:].view(np.uint8), D0[:, N:].view(np.uint8)), "D padding written"
+        a_dec = decode(A[:, :a_cols], in_fmt)
+        b_dec = decode(B[:, :b_cols], in_fmt)
+        amax = float(np.abs(a_dec).max()) if a_dec.size else 0.0
+        bmax = float(np.abs(b_dec).max()) if b_dec.size else 0.0
+        kw = dict(lda=lda, ldb=ldb, C=C0, ldc=ldc, alpha=alpha, beta=beta, in_fmt=in_fmt, out_fmt=d_fmt,
+                  c_fmt=c_fmt, transA=ta, transB=tb)
+        if sample is None:
+            exact, rounded = oracle.gemm(M, N, K, A, B, act=act, slope=slope, **kw)
+            pre, _ = oracle.gemm(M, N, K, A, B, **kw)
+            got = decode(D[:, :N], d_fmt)
+            cterm = np.abs(decode(C0[:, :N], c_fmt))
+        else:
+            rows, cols = sample_positions(M, N, sample, seed)
+            exact, rounded = oracle.sample(rows, cols, K, A, B, act=act, slope=slope, **kw)
+            pre, _ = oracle.sample(rows, cols, K, A, B, **kw)
+            got = decode(D[rows, cols], d_fmt)
+            cterm = np.abs(decode(C0[rows, cols], c_fmt))
+        ref = decode(rounded, d_fmt)
+        lip = 1.1 if act in (gemm.GEMM_ACT_GELU, gemm.GEMM_ACT_SILU) else 1.0
+        tol = (lip * (1e-5 * K * amax * bmax * max(1.0, abs(alpha)) + 2.0 ** -21 * (np.abs(pre) + abs(beta) * cterm))
+               + 2.0 ** -20 * np.abs(exact) + ulp(exact, d_fmt))
+        err = np.abs(got - ref)
+        bad = ~(err <= tol)
+        if bad.any():
+            idx = np.argwhere(bad)[:5]
+            raise AssertionError(
+                f"{int(bad.sum())} of {bad.size} outputs off ({M}x{N}x{K} {in_fmt}, C {c_fmt}, D {d_fmt}, "
+                f"info={res.info}); first: " +
+                "; ".join(f"{tuple(i)} gpu={got[tuple(i)]!r} oracle={ref[tuple(i)]!r}" for i in idx))
+        return res
+    finally:
+        for k, v in old_env.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v

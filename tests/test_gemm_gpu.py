@@ -10,7 +10,7 @@ import os
 import numpy as np
 import pytest
 
-from tests.gemm_case import run_case
+from tests.gemm_case import run_case, run_case_ex
 
 pytestmark = pytest.mark.gpu
 
@@ -183,6 +183,37 @@ def test_activations_every_path(plan, act, out_fmt):
     run_case(plan, 1, 4100, 2000, **kw)               # column-stream GEMV
     run_case(plan, 3000, 1, 2000, **kw)               # row-dot GEMV
     run_case(plan, 64, 80, 0, **kw)                   # K = 0: act(beta * C)
+
+
+# ------------------------------------------------ separate C and D (run_ex)
+
+@pytest.mark.parametrize("c_fmt,d_fmt", [("f32", "bf16"), ("bf16", "f32"), ("f16", "bf16"), ("f32", "f32")])
+def test_separate_c_d_every_path(plan, c_fmt, d_fmt):
+    """D <- act(alpha AB + beta C) with C kept apart, on every path that reads
+    C: one-CTA tiles, the CTA pair, the K pair, the tail split and split-K
+    (tile reduction), both GEMV kernels and the K = 0 scale path.  Odd ldc
+    (a separate C needs no 16-byte rows), ragged shapes."""
+    kw = dict(c_fmt=c_fmt, d_fmt=d_fmt, alpha=1.25, beta=-0.75, act=1, slope=0.2, seed=120, pad=(0, 0, 3, 8))
+    run_case_ex(plan, 300, 520, 200, env={"GEMM_FORCE_TILE": "128x128", "GEMM_FORCE_SPLITK": "1"}, **kw)
+    run_case_ex(plan, 257, 300, 513, env={"GEMM_FORCE_TILE": "256x256"}, **kw)
+    run_case_ex(plan, 384, 260, 1000, env={"GEMM_SPLITK_CLUSTER": "1", "GEMM_FORCE_SPLITK": "2"}, **kw)
+    run_case_ex(plan, 1300, 2000, 333, env={"GEMM_TAIL_SPLIT": "3", "GEMM_FORCE_TILE": "128x128"}, **kw)
+    run_case_ex(plan, 200, 150, 3000, env={"GEMM_FORCE_SPLITK": "5", "GEMM_SPLITK_CLUSTER": "0"}, **kw)
+    run_case_ex(plan, 1, 4100, 2000, **kw)
+    run_case_ex(plan, 3000, 1, 2000, **kw)
+    run_case_ex(plan, 64, 80, 0, **kw)
+
+
+def test_separate_c_d_config3_alternative_reading(plan):
+    """Config 3's second run read the other way: fp32 C (beta 0.5) in, bf16 D
+    out, LeakyReLU 0.01, at the full 8192^3 size on 4096 sampled outputs."""
+    r = run_case_ex(plan, 8192, 8192, 8192, c_fmt="f32", d_fmt="bf16", beta=0.5, act=1, slope=0.01,
+                    seed=1236, sample=4096)
+    assert r.info["cta_per_tile"] == 2
+
+
+def test_separate_c_d_beta_zero_without_c(plan):
+    run_case_ex(plan, 260, 300, 400, c_fmt="f32", d_fmt="bf16", beta=0.0, c_none=True, seed=121)
 
 
 # ------------------------------------------- split-K reduced on chip (K pair)

@@ -87,6 +87,32 @@ def test_check_args_accepts_good_calls():
     assert chk(24, 40, 16, ta=1, tb=1, dtype=3) == g.GEMM_OK
 
 
+def test_check_args_ex_separate_c():
+    """gemm_run_ex: D keeps gemm_run's rules for C; a separate C needs its
+    element alignment, may be NULL only with beta == 0, and must not overlap D."""
+    T16, TF, TH = g.GEMM_TYPE_BF16, g.GEMM_TYPE_F32, g.GEMM_TYPE_F16
+    OK, E, AL = g.GEMM_OK, g.GEMM_ERR_INVALID_ARG, g.GEMM_ERR_ALIGNMENT
+    A, B = 0x100000, 0x200000
+    D, C = 0x400000, 0x800000            # 16-byte aligned, far apart
+
+    def ex(M=64, N=64, K=64, c=C, ldc=64, c_type=TF, d=D, ldd=64, d_type=T16, beta=0.5, ab=T16):
+        return g.gemm_check_args_ex(M, N, K, A, K, B, N, c, ldc, c_type, d, ldd, d_type, 1.0, beta, ab, 0, 0)
+    assert ex() == OK                                        # fp32 C in, bf16 D out
+    assert ex(c_type=TH) == OK and ex(c_type=T16) == OK      # any C type
+    assert ex(c=None, beta=0.0) == OK                        # C unused
+    assert ex(c=None) == E                                   # beta != 0 needs C
+    assert ex(ldc=32) == E                                   # ldc < N
+    assert ex(c=C + 2) == AL and ex(c=C + 4) == OK           # fp32 C: 4-byte alignment only
+    assert ex(d=D + 4) == AL                                 # D: 16 bytes on the tensor-core path
+    assert ex(d_type=TH) == E                                # 16-bit D must be the operand type
+    assert ex(d_type=TF) == OK
+    assert ex(ab=TF) == E                                    # fp32 operands: not a dtype of this library
+    assert ex(c=D, c_type=T16) == OK                         # in place: same matrix
+    assert ex(c=D, c_type=TF) == E and ex(c=D, c_type=T16, ldc=72) == E
+    assert ex(c=D + 64 * 64) == E                            # overlaps D (D spans 64*64*2 bytes)
+    assert ex(c=D + 64 * 64 * 2) == OK                       # right after D
+
+
 def test_check_args_rejects():
     E, AL, U = g.GEMM_ERR_INVALID_ARG, g.GEMM_ERR_ALIGNMENT, g.GEMM_ERR_UNSUPPORTED
     assert chk(-1, 8, 8) == E
