@@ -216,6 +216,60 @@ def test_separate_c_d_beta_zero_without_c(plan):
     run_case_ex(plan, 260, 300, 400, c_fmt="f32", d_fmt="bf16", beta=0.0, c_none=True, seed=121)
 
 
+# ------------------------------------------------------------ input slices
+
+def test_input_slices_through_strides(plan):
+    """Slicing fused into the product: A, B and C are row/column slices of
+    larger tensors, passed as a pointer into the parent plus its row stride
+    (torch views through Plan.run), on the tensor-core, K-pair and GEMV paths;
+    the parents' elements outside the slices hold NaN and are neither read
+    nor written."""
+    import torch
+    import oracle
+    from dense_gemm_mma_gb300 import inputs
+    from tests.gemm_case import decode, from_device, to_device
+
+    def parent(rows, cols, tid, fmt, seed):
+        cols = -(-cols // 8) * 8                      # rows of 16-byte multiples (the ld rule)
+        X = inputs.matrix(rows, cols, seed, tid, fmt)
+        return X, to_device(X, fmt)
+
+    for (M, N, K, r0, c0, env) in [(300, 200, 500, 7, 24, {}),
+                                   (1024, 128, 2048, 3, 16, {"GEMM_SPLITK_CLUSTER": "1", "GEMM_FORCE_SPLITK": "2"}),
+                                   (1, 3000, 1000, 5, 8, {})]:
+        seed = 130 + M
+        Ap, Apd = parent(M + r0 + 9, K + c0 + 40, 0, "bf16", seed)
+        Bp, Bpd = parent(K + r0 + 5, N + c0 + 24, 1, "bf16", seed)
+        Cp = np.full((M + r0 + 3, -(-(N + c0 + 12) // 4) * 4), np.nan, dtype=np.float32)
+        Cpd = to_device(Cp, "f32")
+        A = Ap[r0:r0 + M, c0:c0 + K]
+        B = Bp[r0:r0 + K, c0:c0 + N]
+        # NaN around the slices of A and B: any read outside them would poison a result
+        Apd[:r0] = float("nan"); Apd[r0 + M:] = float("nan"); Apd[:, :c0] = float("nan"); Apd[:, c0 + K:] = float("nan")
+        Bpd[:r0] = float("nan"); Bpd[r0 + K:] = float("nan"); Bpd[:, :c0] = float("nan"); Bpd[:, c0 + N:] = float("nan")
+        old = {k: os.environ.get(k) for k in env}
+        os.environ.update(env)
+        try:
+            st = plan.run(Apd[r0:r0 + M, c0:c0 + K], Bpd[r0:r0 + K, c0:c0 + N], Cpd[r0:r0 + M, c0:c0 + N])
+        finally:
+            for k, v in old.items():
+                if v is None:
+                    os.environ.pop(k, None)
+                else:
+                    os.environ[k] = v
+        assert st == 0
+        torch.cuda.synchronize()
+        out = from_device(Cpd, "f32")
+        inside = np.zeros(out.shape, dtype=bool)
+        inside[r0:r0 + M, c0:c0 + N] = True
+        assert np.isnan(out[~inside]).all()                   # nothing written outside the slice of C
+        exact, _ = oracle.gemm(M, N, K, np.ascontiguousarray(A), np.ascontiguousarray(B))
+        amax = np.abs(decode(A, "bf16")).max()
+        bmax = np.abs(decode(B, "bf16")).max()
+        got = out[r0:r0 + M, c0:c0 + N].astype(np.float64)
+        assert np.all(np.abs(got - exact) <= 1e-5 * K * amax * bmax + 2.0 ** -21 * np.abs(exact)), (M, N, K)
+
+
 # ------------------------------------------- split-K reduced on chip (K pair)
 
 KPAIR = {"GEMM_SPLITK_CLUSTER": "1", "GEMM_FORCE_SPLITK": "2"}
