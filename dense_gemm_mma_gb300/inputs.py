@@ -76,7 +76,7 @@ def _encode(vals: np.ndarray, fmt: str) -> np.ndarray:
         return f32_to_bf16_bits(vals)
     if fmt == "f16":
         return f32_to_f16_bits(vals)
-    if fmt == "f32":
+    if fmt in ("f32", "tf32"):  # a TF32 operand is a full fp32 word; the tensor core drops its low bits
         return vals.astype(np.float32)
     raise ValueError(fmt)
 
@@ -84,11 +84,11 @@ def _encode(vals: np.ndarray, fmt: str) -> np.ndarray:
 def matrix(rows: int, cols: int, seed: int, tensor_id: int, fmt: str = "bf16",
            ld: int | None = None, chunk: int = 1 << 23) -> np.ndarray:
     """Stored matrix of shape (rows, ld): uint16 bit patterns for bf16/fp16,
-    float32 for f32.  Entry (r, c) with c < cols is drawn from index r*cols+c."""
+    float32 for f32 and tf32.  Entry (r, c) with c < cols is drawn from index r*cols+c."""
     ld = cols if ld is None else ld
     if ld < cols:
         raise ValueError("ld < cols")
-    dtype = np.float32 if fmt == "f32" else np.uint16
+    dtype = np.float32 if fmt in ("f32", "tf32") else np.uint16
     total = rows * cols
     flat = np.empty(total, dtype=dtype)
     for s in range(0, total, chunk):

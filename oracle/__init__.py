@@ -24,8 +24,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB = os.path.join(_HERE, "liboracle.so")
 
-BF16, F16, F32 = 0, 1, 2
-FMT_NAMES = {"bf16": BF16, "f16": F16, "f32": F32}
+BF16, F16, F32, TF32 = 0, 1, 2, 3
+FMT_NAMES = {"bf16": BF16, "f16": F16, "f32": F32, "tf32": TF32}
 
 _lib = None
 

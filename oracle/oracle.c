@@ -23,6 +23,12 @@
  *    product.  Reading taken: act is applied to alpha*AB + beta*C, and
  *    LeakyReLU(x) = x < 0 ? slope*x : x.  ReLU, GELU and SiLU are further
  *    transforms of the same kind, written from their definitions (apply_act).
+ *  - "Matrix Multiplication Background User's Guide", section 2.2, Table 1:
+ *    TF32 is one of the Tensor Core precisions.  Reading taken: a TF32
+ *    operand is an fp32 word of which the sign, exponent and 10 highest
+ *    fraction bits are used (the 13 lowest dropped, decode_tf32); products of
+ *    two such values have at most 22 significant bits, so they are exact in
+ *    fp32 as bf16/fp16 products are.
  *
  * Arithmetic: every bf16/fp16 input is decoded exactly to double; the dot
  * product is accumulated in double in ascending k; alpha, beta and the
@@ -45,7 +51,7 @@
 #include <string.h>
 
 /* element formats */
-enum { ORC_BF16 = 0, ORC_F16 = 1, ORC_F32 = 2 };
+enum { ORC_BF16 = 0, ORC_F16 = 1, ORC_F32 = 2, ORC_TF32 = 3 };
 
 /* ---------------------------------------------------------------- decode */
 
@@ -72,9 +78,20 @@ static double decode_f16(uint16_t h) {
   return sign ? -v : v;
 }
 
+/* TF32 operand in an fp32 word: the tensor core uses the sign, the 8-bit
+ * exponent and the 10 highest of the 23 fraction bits; the 13 lowest are
+ * dropped (truncation of the significand toward zero). */
+static double decode_tf32(uint32_t w) {
+  w &= 0xFFFFE000u;
+  float f;
+  memcpy(&f, &w, sizeof f);
+  return (double)f;
+}
+
 double oracle_decode(uint32_t bits, int fmt) {
   if (fmt == ORC_BF16) return decode_bf16((uint16_t)bits);
   if (fmt == ORC_F16) return decode_f16((uint16_t)bits);
+  if (fmt == ORC_TF32) return decode_tf32(bits);
   float f;
   memcpy(&f, &bits, sizeof f);
   return (double)f;
@@ -132,6 +149,7 @@ float oracle_round_f32(double x) {
  *             transA == 1 -> A stored K x M row-major, A[k*lda + i]. */
 static double load_in(const void* p, int fmt, int64_t idx) {
   if (fmt == ORC_F32) return (double)((const float*)p)[idx];
+  if (fmt == ORC_TF32) return decode_tf32(((const uint32_t*)p)[idx]);
   return oracle_decode(((const uint16_t*)p)[idx], fmt);
 }
 
@@ -199,7 +217,7 @@ int oracle_gemm(int64_t M, int64_t N, int64_t K,
                 int in_fmt, int out_fmt, int c_fmt, int transA, int transB,
                 int act, double slope, double* D_exact, void* D_out) {
   if (M < 0 || N < 0 || K < 0) return -1;
-  if (in_fmt != ORC_BF16 && in_fmt != ORC_F16) return -1;
+  if (in_fmt != ORC_BF16 && in_fmt != ORC_F16 && in_fmt != ORC_TF32) return -1;
   if (out_fmt != ORC_BF16 && out_fmt != ORC_F16 && out_fmt != ORC_F32) return -1;
   if (c_fmt != ORC_BF16 && c_fmt != ORC_F16 && c_fmt != ORC_F32) return -1;
   if (beta != 0.0 && C == NULL) return -1;

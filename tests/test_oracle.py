@@ -66,6 +66,9 @@ def dec(bits, fmt):
         return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
     if fmt == "f16":
         return bits.astype(np.uint16).view(np.float16).astype(np.float64)
+    if fmt == "tf32":  # 10 of the 23 fraction bits: clear the 13 lowest of the fp32 word
+        w = np.ascontiguousarray(bits, dtype=np.float32).view(np.uint32) & np.uint32(0xFFFFE000)
+        return w.view(np.float32).astype(np.float64)
     return np.asarray(bits, dtype=np.float32).astype(np.float64)
 
 
@@ -303,7 +306,7 @@ def _exact_product(Ad, Bd, M, N, K):
 
 
 @pytest.mark.parametrize("in_fmt,out_fmt", [("bf16", "f32"), ("bf16", "bf16"), ("f16", "f32"),
-                                            ("f16", "f16")])
+                                            ("f16", "f16"), ("tf32", "f32")])
 def test_brute_force_exact_rationals(oracle_lib, in_fmt, out_fmt):
     """Every M, N, K in 1..6: oracle vs exact rational arithmetic."""
     u = Fraction(1, 2 ** 53)
@@ -338,6 +341,23 @@ def test_brute_force_exact_rationals(oracle_lib, in_fmt, out_fmt):
 
 
 # ------------------------------------------------------------ rounding / decoding
+
+def test_tf32_operand_decode(oracle_lib):
+    """TF32 (section 2.2, Table 1): sign, 8-bit exponent, 10 fraction bits of
+    an fp32 word.  Words with low bits set lose them toward zero: 1 + 2^-11 +
+    2^-12 gives 1.0 (nearest rounding would give 1 + 2^-10)."""
+    cases = {0x3F802000: 1.0 + 2.0 ** -10, 0x3F801000: 1.0, 0x3F801800: 1.0, 0x3F803000: 1.0 + 2.0 ** -10,
+             0xBF803000: -(1.0 + 2.0 ** -10), 0x3FFFE000: 2.0 - 2.0 ** -10, 0x3FFFFFFF: 2.0 - 2.0 ** -10,
+             0x40490FDB: 3.140625, 0x00800000: 2.0 ** -126, 0x00000000: 0.0, 0x80000000: -0.0}
+    for bits, v in cases.items():
+        got = oracle_lib.decode(bits, "tf32")
+        assert got == v and math.copysign(1.0, got) == math.copysign(1.0, v), hex(bits)
+    # products of two TF32 values (11 significant bits each) are exact in fp32
+    rng = np.random.default_rng(5)
+    a = dec(rng.uniform(-4, 4, 10000).astype(np.float32), "tf32")
+    b = dec(rng.uniform(-4, 4, 10000).astype(np.float32), "tf32")
+    assert np.array_equal((a.astype(np.float32) * b.astype(np.float32)).astype(np.float64), a * b)
+
 
 def test_decode_all_patterns(oracle_lib):
     for fmt in ("bf16", "f16"):

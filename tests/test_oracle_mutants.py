@@ -38,6 +38,8 @@ MUTANTS = {
     "gelu_half_dropped": ("return 0.5 * d * erfc(-d / sqrt(2.0));", "return d * erfc(-d / sqrt(2.0));"),
     "silu_wrong_sign": ("return d / (1.0 + exp(-d));", "return d / (1.0 + exp(d));"),
     "relu_as_identity": ("case 2: return d < 0.0 ? 0.0 : d;", "case 2: return d;"),
+    "tf32_rounds_instead": ("w &= 0xFFFFE000u;", "w = (w + 0x1000u) & 0xFFFFE000u;"),
+    "tf32_keeps_11_bits": ("w &= 0xFFFFE000u;", "w &= 0xFFFFF000u;"),
 }
 
 
