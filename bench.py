@@ -86,6 +86,11 @@ def workload(name: str):
             Call("square_bf16_out", 8192, 8192, 8192, out_fmt="bf16", seed=s),
             Call("square_beta_leaky", 8192, 8192, 8192, out_fmt="f32", beta=0.5, act=1, slope=0.01,
                  seed=s)])
+    if name == "tf32":
+        s = inputs.config_seed(2)
+        return ("square_gemm_8192_cubed_tf32", [
+            Call("square_tf32_NT", 8192, 8192, 8192, in_fmt="tf32", tb=True, seed=s),
+            Call("square_tf32_NN", 8192, 8192, 8192, in_fmt="tf32", seed=s)])
     if name == "small":
         return ("gemm_512_cubed_bf16", [Call("gemm_512", 512, 512, 512, seed=inputs.config_seed(0))])
     if name == "tile":
@@ -202,6 +207,12 @@ def ref_tiling(c, sms: int):
     return {"tiles": q.tiles, "waves": round(q.waves, 3), "tail_fraction": round(q.tail_fraction, 4)}
 
 
+# Dense tensor-core peak of a call's operand type in TFLOP/s: the measured bf16
+# figure, times the nominal TF32 / bf16 ratio (1.1 / 2.25 PFLOP/s) for TF32.
+def tensor_peak(c, peaks) -> float:
+    return peaks["bf16_tflops"] * (1.1 / 2.25 if c.in_fmt == "tf32" else 1.0)
+
+
 def max_over_ranks(value: float, dist, device) -> float:
     """Largest `value` over all ranks (the slowest replica sets the job time)."""
     if dist is None:
@@ -298,7 +309,7 @@ def main():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="skinny", choices=["skinny", "square", "small", "tile", "wave"])
+    ap.add_argument("--workload", default="skinny", choices=["skinny", "square", "small", "tile", "wave", "tf32"])
     ap.add_argument("--cpu-fraction", type=float, default=None,
                     help="fraction of each call's outputs the cpu_baseline oracle computes")
     ap.add_argument("--ref-fraction", type=float, default=1.0 / 512)
@@ -465,15 +476,16 @@ def main():
         sec = mean_call[i] / 1e3
         info = infos[i].as_dict()
         ai = c.flops / c.bytes
-        att = rl.attainable(ai, peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9)
+        att = rl.attainable(ai, tensor_peak(c, peaks) * 1e12, peaks["hbm_gbs"] * 1e9)
         parts.append({
             "name": c.name, "us": round(mean_call[i] * 1e3, 2),
             "us_median": round(float(np.median(call_ms[:, i])) * 1e3, 2),
             "us_iqr": round(float(np.subtract(*np.percentile(call_ms[:, i], [75, 25]))) * 1e3, 2),
             "tflops": round(c.flops / sec / 1e12, 2), "gbs": round(c.bytes / sec / 1e9, 1),
-            "intensity": round(ai, 1), "bound": rl.bound(ai, peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9),
+            "intensity": round(ai, 1), "bound": rl.bound(ai, tensor_peak(c, peaks) * 1e12, peaks["hbm_gbs"] * 1e9),
             "frac_of_roofline": round(c.flops / sec / att, 3),
-            "frac_of_nominal_roofline": round(c.flops / sec / rl.attainable(ai, 2.25e15, 8e12), 3),
+            "frac_of_nominal_roofline": round(c.flops / sec / rl.attainable(
+                ai, (1.1e15 if c.in_fmt == "tf32" else 2.25e15), 8e12), 3),
             "path": info["path"], "tile": f"{info['tile_m']}x{info['tile_n']}", "splitk": info["splitk"],
             "grid": info["grid"], "units": info["units"], "waves": round(info["waves"], 3),
             "tail_fraction": round(info["tail_fraction"], 4), "launches": info["launches"],
@@ -482,11 +494,11 @@ def main():
     dc = calls[dom]
     dom_sec = mean_call[dom] / 1e3
     dom_ai = dc.flops / dc.bytes
-    dom_bound = rl.bound(dom_ai, peaks["bf16_tflops"] * 1e12, peaks["hbm_gbs"] * 1e9)
+    dom_bound = rl.bound(dom_ai, tensor_peak(dc, peaks) * 1e12, peaks["hbm_gbs"] * 1e9)
     if dom_bound == "hbm":
         achieved, peak, unit = dc.bytes / dom_sec / 1e9, peaks["hbm_gbs"], "GB/s"
     else:
-        achieved, peak, unit = dc.flops / dom_sec / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+        achieved, peak, unit = dc.flops / dom_sec / 1e12, round(tensor_peak(dc, peaks), 1), "TFLOP/s"
     roof = {"bound": dom_bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
             "frac": round(achieved / peak, 4), "traffic": traffic_for(dc.name),
             "kernel": dc.name, "peak_source": f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback",
@@ -500,7 +512,7 @@ def main():
     # ---- CPU oracle baseline (rank 0, N == 1 only)
     cpu = None
     if not args.no_cpu and rank == 0 and ws == 1:
-        frac = args.cpu_fraction or {"skinny": 1 / 4, "square": 1 / 8192, "small": 1 / 8,
+        frac = args.cpu_fraction or {"skinny": 1 / 4, "square": 1 / 8192, "tf32": 1 / 8192, "small": 1 / 8,
                                      "tile": 1 / 4096, "wave": 1 / 2048}[args.workload]
         secs, byts, desc = oracle_sample(calls, host, frac)
         cpu = {"value": round(byts / secs / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",

@@ -27,6 +27,9 @@ SOURCES = [
     "gemm_tc_bn64.cu",
     "gemm_tc_bn128.cu",
     "gemm_tc_bn256.cu",
+    "gemm_tc_tf32_bn64.cu",
+    "gemm_tc_tf32_bn128.cu",
+    "gemm_tc_tf32_bn256.cu",
     "noalloc.cu",
 ]
 HEADERS = ["ptx.cuh", "kernels.h", "gemm_tc.cuh"]

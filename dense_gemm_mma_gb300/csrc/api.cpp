@@ -82,6 +82,8 @@ struct gemm_plan {
   void* ws = nullptr;  // workspace (split-K partials, GEMV partials)
   size_t ws_bytes = 0;
   unsigned* counters = nullptr;  // GEMV per-panel arrival counters: zero between calls
+  void* tws = nullptr;  // K-major copies of TF32 operands stored M/N-major
+  size_t tws_bytes = 0;
   size_t counter_count = 0;
   uint64_t watchdog_ns = 2000000000ull;
   gemm_config_info_t last{};
@@ -98,13 +100,16 @@ namespace {
 
 constexpr int64_t kMaxDim = (int64_t(1) << 31) - 1;
 
-bool out_is_f32(gemm_dtype_t d) { return d == GEMM_BF16_F32 || d == GEMM_F16_F32; }
+bool out_is_f32(gemm_dtype_t d) { return d == GEMM_BF16_F32 || d == GEMM_F16_F32 || d == GEMM_TF32_F32; }
 bool in_is_f16(gemm_dtype_t d) { return d == GEMM_F16_F32 || d == GEMM_F16_F16; }
+bool in_is_tf32(gemm_dtype_t d) { return d == GEMM_TF32_F32; }
+int in_bytes(gemm_dtype_t d) { return in_is_tf32(d) ? 4 : 2; }
 
 int out_kind(gemm_dtype_t d) {
   switch (d) {
     case GEMM_BF16_F32:
-    case GEMM_F16_F32: return dg::OUT_F32;
+    case GEMM_F16_F32:
+    case GEMM_TF32_F32: return dg::OUT_F32;
     case GEMM_BF16_BF16: return dg::OUT_BF16;
     default: return dg::OUT_F16;
   }
@@ -120,7 +125,7 @@ gemm_status_t check(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                     int64_t ldb, const void* C, int64_t ldc, float alpha, gemm_dtype_t dtype,
                     gemm_op_t ta, gemm_op_t tb, gemm_epilogue_t epi) {
   if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
-  if (dtype < GEMM_BF16_F32 || dtype > GEMM_F16_F16) return GEMM_ERR_INVALID_ARG;
+  if (dtype < GEMM_BF16_F32 || dtype > GEMM_TF32_F32) return GEMM_ERR_INVALID_ARG;
   if ((ta != GEMM_OP_N && ta != GEMM_OP_T) || (tb != GEMM_OP_N && tb != GEMM_OP_T))
     return GEMM_ERR_INVALID_ARG;
   if (epi.act < GEMM_ACT_NONE || epi.act > GEMM_ACT_SILU) return GEMM_ERR_INVALID_ARG;
@@ -136,7 +141,14 @@ gemm_status_t check(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   if (reads_ab && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_ARG;
   const size_t ces = out_is_f32(dtype) ? 4 : 2;
   if (!aligned(C, ces)) return GEMM_ERR_ALIGNMENT;
-  if (reads_ab && (!aligned(A, 2) || !aligned(B, 2))) return GEMM_ERR_ALIGNMENT;
+  const int ies = in_bytes(dtype);
+  if (reads_ab && (!aligned(A, ies) || !aligned(B, ies))) return GEMM_ERR_ALIGNMENT;
+  if (in_is_tf32(dtype)) {  // always the tensor-core path
+    if (reads_ab && (!aligned(A, 16) || !aligned(B, 16) || (lda * 4) % 16 || (ldb * 4) % 16))
+      return GEMM_ERR_ALIGNMENT;
+    if (N >= 4 && (!aligned(C, 16) || (ldc * 4) % 16)) return GEMM_ERR_ALIGNMENT;
+    return GEMM_OK;
+  }
   if (reads_ab && M >= 2 && N >= 2) {
     if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16)) return GEMM_ERR_ALIGNMENT;
     if ((lda * 2) % 16 || (ldb * 2) % 16 || (ldc * int64_t(ces)) % 16) return GEMM_ERR_ALIGNMENT;
@@ -217,10 +229,14 @@ void distinct_panels(int64_t mb, int64_t nb, int64_t group, int64_t count, int64
   *db += dn;
 }
 
+// eb: operand element bytes (2: bf16/fp16, 4: TF32, whose tensor-core rate is
+// half of the 16-bit one); a k-block is one 128-byte row of every operand.
 double estimate(int64_t M, int64_t N, int64_t K, int bn, int mode, int splitk, int sms, int c_es,
-                bool beta, int raster_group, const Model& md, int* splitk_eff) {
+                bool beta, int raster_group, const Model& md, int* splitk_eff, int eb) {
   const bool pair = mode == dg::TC_PAIR, kpair = mode == dg::TC_KPAIR;
-  const int64_t kb = ceil_div(K, dg::TC_BK);
+  const int kbe = 128 / eb;
+  const double peak = md.peak_flops * (eb == 4 ? 0.5 : 1.0);
+  const int64_t kb = ceil_div(K, kbe);
   const int64_t kbps = ceil_div(kb, splitk);
   const int s_eff = int(ceil_div(kb, kbps));
   *splitk_eff = s_eff;
@@ -245,9 +261,9 @@ double estimate(int64_t M, int64_t N, int64_t K, int bn, int mode, int splitk, i
     distinct_panels(mb, nb, group, active, &da, &db);
   }
   int64_t streams = da + db;
-  const double t_mma = 2.0 * dg::TC_BM * bn * double(kbps * dg::TC_BK) / (md.peak_flops / sms * tile_efficiency(bn));
-  const double unit_bytes = double(dg::TC_BM + (pair ? bn / 2 : bn)) * double(kbps * dg::TC_BK) * 2.0;
-  const double unique = double(M * K + K * N) * 2.0;
+  const double t_mma = 2.0 * dg::TC_BM * bn * double(kbps * kbe) / (peak / sms * tile_efficiency(bn));
+  const double unit_bytes = double(dg::TC_BM + (pair ? bn / 2 : bn)) * double(kbps) * 128.0;
+  const double unique = double(M * K + K * N) * eb;
   const double reuse = (1.0 - 1.0 / waves) *
                        std::max(0.0, 1.0 - unique / (double(units) * (pair ? 2 : 1) * unit_bytes));
   const double feed = md.feed * (1.0 + md.reuse_gain * reuse);
@@ -275,23 +291,24 @@ constexpr double kTailExtra = 1.0e-6;
 // tiles in S K slices each (one more wave, T*S <= slots), whose partials a
 // reduction launch sums.  Same ingredients as estimate().
 double estimate_tail(int64_t M, int64_t N, int64_t K, int bn, int mode, int S, int sms, int c_es,
-                     bool beta, int raster_group, const Model& md) {
+                     bool beta, int raster_group, const Model& md, int eb) {
   const bool pair = mode == dg::TC_PAIR;
   const int tile_m = pair ? 2 * dg::TC_BM : dg::TC_BM;
   const int slots = pair ? sms / 2 : sms;
   const int64_t mb = ceil_div(M, tile_m), nb = ceil_div(N, bn), tiles = mb * nb;
   const int64_t W = tiles / slots, T = tiles - W * slots;
-  const int64_t kb = ceil_div(K, dg::TC_BK), kbps = ceil_div(kb, S);
+  const int kbe = 128 / eb;
+  const int64_t kb = ceil_div(K, kbe), kbps = ceil_div(kb, S);
   const int64_t group = std::max<int64_t>(1, std::min<int64_t>(raster_group, mb));
   int64_t da = 0, db = 0;
   distinct_panels(mb, nb, group, std::min<int64_t>(tiles, slots), &da, &db);
   const int64_t streams = (da + db) * (pair ? 2 : 1);
-  const double rate = md.peak_flops / sms * tile_efficiency(bn);
-  const double t_mma_full = 2.0 * dg::TC_BM * bn * double(kb * dg::TC_BK) / rate;
-  const double t_mma_tail = 2.0 * dg::TC_BM * bn * double(kbps * dg::TC_BK) / rate;
-  const double row_bytes = double(dg::TC_BM + (pair ? bn / 2 : bn)) * dg::TC_BK * 2.0;
+  const double rate = md.peak_flops * (eb == 4 ? 0.5 : 1.0) / sms * tile_efficiency(bn);
+  const double t_mma_full = 2.0 * dg::TC_BM * bn * double(kb * kbe) / rate;
+  const double t_mma_tail = 2.0 * dg::TC_BM * bn * double(kbps * kbe) / rate;
+  const double row_bytes = double(dg::TC_BM + (pair ? bn / 2 : bn)) * 128.0;
   const double ub_full = row_bytes * double(kb), ub_tail = row_bytes * double(kbps);
-  const double unique = double(M * K + K * N) * 2.0;
+  const double unique = double(M * K + K * N) * eb;
   const double waves = double(W + 1);
   const double all_units = (double(W * slots) * ub_full + double(T * S) * ub_tail) * (pair ? 2 : 1);
   const double reuse = (1.0 - 1.0 / waves) * std::max(0.0, 1.0 - unique / all_units);
@@ -313,7 +330,7 @@ int env_int(const char* name, int dflt) {
 // Every candidate the planner estimates, in the order it considers them
 // (best estimate first after sorting); `best` is the planner's pick.
 void tc_candidates(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta, TcChoice* best,
-                   std::vector<TcChoice>* all) {
+                   std::vector<TcChoice>* all, int eb) {
   const Model md;
   TcChoice pick;
   int force_bn = 0;
@@ -338,7 +355,7 @@ void tc_candidates(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta
   const int tail_env = env_int("GEMM_TAIL_SPLIT", -1);
   const bool only_tail = tail_env >= 1;
   const int raster = env_int("GEMM_RASTER_GROUP", 16);
-  const int64_t kb = ceil_div(K, dg::TC_BK);
+  const int64_t kb = ceil_div(K, 128 / eb);
   // GEMM_PLAN_DEBUG=1 prints every candidate's estimate to stderr.
   const bool debug = env_int("GEMM_PLAN_DEBUG", 0) != 0;
   // candidates: 128-row tiles of width 256/128/64 on one CTA, 256 x 256 on a
@@ -380,7 +397,7 @@ void tc_candidates(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta
       if (s > kb) break;
       if (s > 1 && tiles * s > 4 * int64_t(slots)) break;
       int s_eff = 1;
-      const double t = estimate(M, N, K, c.bn, c.mode, s, sms, c_es, beta, raster, md, &s_eff);
+      const double t = estimate(M, N, K, c.bn, c.mode, s, sms, c_es, beta, raster, md, &s_eff, eb);
       if (s_eff != s) continue;
       take(t, c.bn, c.mode, s, false);
     }
@@ -401,7 +418,7 @@ void tc_candidates(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta
           st = std::min<int64_t>(st, kb);
           if (st >= 2) st = ceil_div(kb, ceil_div(kb, st));  // no empty slice
           if (st < 2) break;
-          const double t = estimate_tail(M, N, K, c.bn, c.mode, int(st), sms, c_es, beta, raster, md);
+          const double t = estimate_tail(M, N, K, c.bn, c.mode, int(st), sms, c_es, beta, raster, md, eb);
           take(t, c.bn, c.mode, int(st), true);
         }
       }
@@ -417,8 +434,9 @@ void tc_candidates(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta
 }
 
 // The configuration record of one choice.
-void fill_info(int64_t M, int64_t N, int64_t K, int sms, const TcChoice& c, gemm_config_info_t* out) {
-  const int64_t kb = ceil_div(K, dg::TC_BK);
+void fill_info(int64_t M, int64_t N, int64_t K, int sms, const TcChoice& c, gemm_config_info_t* out,
+               int eb) {
+  const int64_t kb = ceil_div(K, 128 / eb);
   const int best_s = int(ceil_div(kb, ceil_div(kb, c.s)));
   const bool pair = c.mode == dg::TC_PAIR, kpair = c.mode == dg::TC_KPAIR;
   const int tile_m = pair ? 2 * dg::TC_BM : dg::TC_BM;
@@ -441,7 +459,7 @@ void fill_info(int64_t M, int64_t N, int64_t K, int sms, const TcChoice& c, gemm
   } else {
     out->path = GEMM_PATH_TC;
   }
-  out->tile_k = dg::TC_BK;
+  out->tile_k = 128 / eb;
   out->cta_per_tile = c.mode == dg::TC_SOLO ? 1 : 2;
   out->stages = dg::tc_stages(c.bn, c.mode);
   const int64_t mblocks = ceil_div(M, tile_m);
@@ -456,11 +474,11 @@ void fill_info(int64_t M, int64_t N, int64_t K, int sms, const TcChoice& c, gemm
   out->workspace_bytes = int64_t(out->tail_tiles) * best_s * tile_m * c.bn * 4;
 }
 
-void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta,
-               gemm_config_info_t* out) {
+void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta, gemm_config_info_t* out,
+               int eb) {
   TcChoice best;
-  tc_candidates(M, N, K, sms, c_es, beta, &best, nullptr);
-  fill_info(M, N, K, sms, best, out);
+  tc_candidates(M, N, K, sms, c_es, beta, &best, nullptr, eb);
+  fill_info(M, N, K, sms, best, out, eb);
 }
 
 // ------------------------------------------------------------ tensor maps
@@ -498,29 +516,36 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType t, int esize, const void* ptr,
 // tcgen05 instruction descriptor, kind::f16 with fp32 accumulation:
 // bits 4-5 D type (1 = f32), 7-9 A type and 10-12 B type (0 = f16, 1 = bf16),
 // 15/16 A/B major (0 = K-major, 1 = M/N-major), 17-22 N>>3, 24-28 M>>4.
-uint32_t make_idesc(bool f16, bool a_mn, bool b_mn, int n, int m) {
-  const uint32_t ab = f16 ? 0u : 1u;
+// kind::tf32 takes the same descriptor with A and B type 2 (TF32).
+uint32_t make_idesc(int in_type, bool a_mn, bool b_mn, int n, int m) {
+  const uint32_t ab = uint32_t(in_type);  // 0 fp16, 1 bf16, 2 TF32
   return (1u << 4) | (ab << 7) | (ab << 10) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
          (uint32_t(n >> 3) << 17) | (uint32_t(m >> 4) << 24);
 }
 
 // ------------------------------------------------------------- workspace
 
-gemm_status_t ensure_ws(gemm_plan* plan, size_t bytes, cudaStream_t s) {
-  if (bytes <= plan->ws_bytes) return GEMM_OK;
+// Grow a plan buffer to at least `bytes` (1 MiB steps, stream-ordered,
+// zero-filled).
+gemm_status_t ensure_buffer(void** buf, size_t* have, size_t bytes, cudaStream_t s) {
+  if (bytes <= *have) return GEMM_OK;
   size_t nb = std::max<size_t>(bytes, size_t(1) << 20);
   nb = (nb + (size_t(1) << 20) - 1) & ~((size_t(1) << 20) - 1);
-  if (plan->ws) cudaFreeAsync(plan->ws, s);
-  plan->ws = nullptr;
-  plan->ws_bytes = 0;
-  if (cudaMallocAsync(&plan->ws, nb, s) != cudaSuccess) {
+  if (*buf) cudaFreeAsync(*buf, s);
+  *buf = nullptr;
+  *have = 0;
+  if (cudaMallocAsync(buf, nb, s) != cudaSuccess) {
     cudaGetLastError();
-    plan->ws = nullptr;
+    *buf = nullptr;
     return GEMM_ERR_OUT_OF_MEMORY;
   }
-  if (cudaMemsetAsync(plan->ws, 0, nb, s) != cudaSuccess) return GEMM_ERR_CUDA;
-  plan->ws_bytes = nb;
+  if (cudaMemsetAsync(*buf, 0, nb, s) != cudaSuccess) return GEMM_ERR_CUDA;
+  *have = nb;
   return GEMM_OK;
+}
+
+gemm_status_t ensure_ws(gemm_plan* plan, size_t bytes, cudaStream_t s) {
+  return ensure_buffer(&plan->ws, &plan->ws_bytes, bytes, s);
 }
 
 // The counters are zeroed once when allocated; every kernel that uses one
@@ -637,10 +662,11 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
                              gemm_op_t tb, const TcChoice* forced, TcEntry* e) {
   gemm_config_info_t* info = &e->info;
   const int c_es = out_is_f32(dtype) ? 4 : 2;
+  const int eb = in_bytes(dtype);
   if (forced)
-    fill_info(M, N, K, plan->sms, *forced, info);
+    fill_info(M, N, K, plan->sms, *forced, info, eb);
   else
-    choose_tc(M, N, K, plan->sms, c_es, beta_nz, info);
+    choose_tc(M, N, K, plan->sms, c_es, beta_nz, info, eb);
   const int bn = info->tile_n;
   const int S = info->splitk;
   const int mode = tc_mode(*info);
@@ -651,13 +677,17 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
     if (mc <= 0) return GEMM_ERR_UNSUPPORTED;
     info->grid = int(2 * std::min<int64_t>(pair ? info->units : info->tiles, mc));
   }
-  const bool f16 = in_is_f16(dtype);
-  const CUtensorMapDataType in_t = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const bool f16 = in_is_f16(dtype), tf32 = in_is_tf32(dtype);
+  const CUtensorMapDataType in_t = tf32  ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                         : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int kbe = 128 / eb;  // K elements in one 128-byte swizzle row
   const bool a_mn = ta == GEMM_OP_T, b_mn = tb == GEMM_OP_N;
-  bool ok = a_mn ? make_map(&e->ma, in_t, 2, A, M, K, lda, 64, 64)
-                 : make_map(&e->ma, in_t, 2, A, K, M, lda, 64, dg::TC_BM);
-  ok = ok && (b_mn ? make_map(&e->mb, in_t, 2, B, N, K, ldb, 64, 64)
-                   : make_map(&e->mb, in_t, 2, B, K, N, ldb, 64, pair ? bn / 2 : bn));
+  if (tf32 && (a_mn || b_mn)) return GEMM_ERR_UNSUPPORTED;  // the caller transposes TF32 operands first
+  bool ok = a_mn ? make_map(&e->ma, in_t, eb, A, M, K, lda, 64, 64)
+                 : make_map(&e->ma, in_t, eb, A, K, M, lda, kbe, dg::TC_BM);
+  ok = ok && (b_mn ? make_map(&e->mb, in_t, eb, B, N, K, ldb, 64, 64)
+                   : make_map(&e->mb, in_t, eb, B, K, N, ldb, kbe, pair ? bn / 2 : bn));
   dg::TcParams& p = e->p;
   p = dg::TcParams{};
   p.M = int(M);
@@ -665,7 +695,9 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
   p.K = int(K);
   p.num_m_blocks = int(ceil_div(M, tile_m));
   p.num_n_blocks = int(ceil_div(N, bn));
-  p.k_blocks = int(ceil_div(K, dg::TC_BK));
+  p.kb_elems = kbe;
+  p.k_blocks = int(ceil_div(K, kbe));
+  p.tf32 = tf32;
   p.raster_group = info->raster_group;
   // units: whole tiles first, then the K slices of the tail tiles (all tiles
   // for split-K, the last wave's for a tail split, none otherwise)
@@ -679,7 +711,7 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
   p.out_kind = out_kind(dtype);
   p.a_mn_major = a_mn;
   p.b_mn_major = b_mn;
-  p.idesc = make_idesc(f16, a_mn, b_mn, bn, tile_m);
+  p.idesc = make_idesc(tf32 ? 2 : (f16 ? 0 : 1), a_mn, b_mn, bn, tile_m);
   p.c_ptr = C;
   p.ldc = ldc;
   p.cin = cin.ptr;
@@ -692,7 +724,10 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
   // 16-byte-aligned prefix of each row of C; the kernel writes the rest.
   p.n_tma = int((N * c_es) / 16 * 16 / c_es);
   const CUtensorMapDataType ct = out_is_f32(dtype) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : in_t;
-  ok = ok && make_map(&e->mc, ct, c_es, C, std::max<int64_t>(p.n_tma, 1), M, ldc, 128 / c_es, 32);
+  if (p.n_tma > 0)
+    ok = ok && make_map(&e->mc, ct, c_es, C, p.n_tma, M, ldc, 128 / c_es, 32);
+  else  // every column is written (and read for beta) by the threads: a placeholder map
+    ok = ok && make_map(&e->mc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, plan->err, 32, 32, 32, 32, 32);
   e->mw = e->mc;  // replaced by the workspace map before a launch that has tail tiles
   e->ws_ptr = nullptr;
   // fp32 partials, tile-major: [slice][tail tile][tile_m rows][bn columns]
@@ -764,7 +799,7 @@ TcChoice autotune(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const void* 
   const int c_es = out_is_f32(dtype) ? 4 : 2;
   std::vector<TcChoice> all;
   TcChoice best;
-  tc_candidates(M, N, K, plan->sms, c_es, beta != 0.f, &best, &all);
+  tc_candidates(M, N, K, plan->sms, c_es, beta != 0.f, &best, &all, in_bytes(dtype));
   std::stable_sort(all.begin(), all.end(), [](const TcChoice& x, const TcChoice& y) { return x.t < y.t; });
   std::vector<TcChoice> trial{best};
   for (const TcChoice& c : all) {
@@ -920,6 +955,7 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan) {
   DeviceGuard guard(plan->device);
   cudaDeviceSynchronize();
   if (plan->ws) cudaFree(plan->ws);
+  if (plan->tws) cudaFree(plan->tws);
   if (plan->counters) cudaFree(plan->counters);
   if (plan->err) cudaFree(plan->err);
   delete plan;
@@ -944,13 +980,15 @@ gemm_status_t check_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t l
                        int64_t ldb, const void* C, int64_t ldc, gemm_type_t c_type, const void* D,
                        int64_t ldd, gemm_type_t d_type, float alpha, float beta, gemm_type_t ab_type,
                        gemm_op_t ta, gemm_op_t tb, gemm_epilogue_t epi, gemm_dtype_t* dtype) {
-  if (ab_type != GEMM_TYPE_BF16 && ab_type != GEMM_TYPE_F16) return GEMM_ERR_INVALID_ARG;
-  if (d_type != GEMM_TYPE_F32 && d_type != ab_type) return GEMM_ERR_INVALID_ARG;
+  if (ab_type != GEMM_TYPE_BF16 && ab_type != GEMM_TYPE_F16 && ab_type != GEMM_TYPE_TF32)
+    return GEMM_ERR_INVALID_ARG;
+  if (d_type != GEMM_TYPE_F32 && (d_type != ab_type || ab_type == GEMM_TYPE_TF32)) return GEMM_ERR_INVALID_ARG;
   if (c_type != GEMM_TYPE_BF16 && c_type != GEMM_TYPE_F16 && c_type != GEMM_TYPE_F32)
     return GEMM_ERR_INVALID_ARG;
   const bool f32 = d_type == GEMM_TYPE_F32;
-  *dtype = ab_type == GEMM_TYPE_BF16 ? (f32 ? GEMM_BF16_F32 : GEMM_BF16_BF16)
-                                     : (f32 ? GEMM_F16_F32 : GEMM_F16_F16);
+  *dtype = ab_type == GEMM_TYPE_TF32 ? GEMM_TF32_F32
+           : ab_type == GEMM_TYPE_BF16 ? (f32 ? GEMM_BF16_F32 : GEMM_BF16_BF16)
+                                       : (f32 ? GEMM_F16_F32 : GEMM_F16_F16);
   // D is held to gemm_run's rules for C
   const gemm_status_t st = check(M, N, K, A, lda, B, ldb, D, ldd, alpha, *dtype, ta, tb, epi);
   if (st != GEMM_OK || M == 0 || N == 0 || beta == 0.f) return st;
@@ -988,8 +1026,35 @@ gemm_status_t run_all(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, const v
     r = dg::launch_scale(int(M), int(N), D, ldd, cin.ptr, cin.ld, e, s, plan->sms) == cudaSuccess
             ? GEMM_OK
             : GEMM_ERR_CUDA;
-  } else if (M == 1 || N == 1) {
+  } else if ((M == 1 || N == 1) && !in_is_tf32(dtype)) {
     r = run_gemv(plan, M, N, K, A, lda, B, ldb, D, ldd, dtype, transA, transB, e, cin, s, &info);
+  } else if (in_is_tf32(dtype) && (transA == GEMM_OP_T || transB == GEMM_OP_N)) {
+    // The TF32 MMAs read K-major tiles: transpose an M/N-major operand into
+    // plan workspace first (row stride rounded to 4 elements, 16 bytes).
+    const int64_t lda_t = (K + 3) & ~int64_t(3), ldb_t = lda_t;
+    const size_t a_bytes = transA == GEMM_OP_T ? size_t(M) * size_t(lda_t) * 4 : 0;
+    const size_t b_bytes = transB == GEMM_OP_N ? size_t(N) * size_t(ldb_t) * 4 : 0;
+    const size_t a_off = 0, b_off = (a_bytes + 255) & ~size_t(255);
+    r = ensure_buffer(&plan->tws, &plan->tws_bytes, b_off + b_bytes, s);
+    const void* A2 = A;
+    const void* B2 = B;
+    int64_t lda2 = lda, ldb2 = ldb;
+    if (r == GEMM_OK && a_bytes) {  // A stored K x M -> M x K
+      A2 = static_cast<char*>(plan->tws) + a_off;
+      lda2 = lda_t;
+      if (dg::launch_transpose32(A, lda, int(K), int(M), const_cast<void*>(A2), lda2, s) != cudaSuccess)
+        r = GEMM_ERR_CUDA;
+    }
+    if (r == GEMM_OK && b_bytes) {  // B stored K x N -> N x K
+      B2 = static_cast<char*>(plan->tws) + b_off;
+      ldb2 = ldb_t;
+      if (dg::launch_transpose32(B, ldb, int(K), int(N), const_cast<void*>(B2), ldb2, s) != cudaSuccess)
+        r = GEMM_ERR_CUDA;
+    }
+    if (r == GEMM_OK)
+      r = run_tc(plan, M, N, K, A2, lda2, B2, ldb2, D, ldd, cin, alpha, beta, dtype, GEMM_OP_N, GEMM_OP_T,
+                 epilogue, s, &info);
+    info.launches += int(a_bytes > 0) + int(b_bytes > 0);
   } else {
     r = run_tc(plan, M, N, K, A, lda, B, ldb, D, ldd, cin, alpha, beta, dtype, transA, transB, epilogue,
                s, &info);
@@ -1094,7 +1159,7 @@ gemm_status_t gemm_choose_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t d
                                  gemm_op_t transA, gemm_op_t transB, int32_t sms,
                                  gemm_config_info_t* out) {
   if (!out || sms <= 0 || M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
-  if (dtype < GEMM_BF16_F32 || dtype > GEMM_F16_F16) return GEMM_ERR_INVALID_ARG;
+  if (dtype < GEMM_BF16_F32 || dtype > GEMM_TF32_F32) return GEMM_ERR_INVALID_ARG;
   if ((transA != GEMM_OP_N && transA != GEMM_OP_T) || (transB != GEMM_OP_N && transB != GEMM_OP_T))
     return GEMM_ERR_INVALID_ARG;
   std::memset(out, 0, sizeof(*out));
@@ -1109,7 +1174,7 @@ gemm_status_t gemm_choose_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t d
     out->launches = 1;
     return GEMM_OK;
   }
-  if (M == 1 || N == 1) {
+  if ((M == 1 || N == 1) && !in_is_tf32(dtype)) {
     const bool row_major_w = N == 1 ? transA == GEMM_OP_N : transB == GEMM_OP_T;
     const int64_t R = N == 1 ? M : N;
     out->launches = 1;
@@ -1124,7 +1189,7 @@ gemm_status_t gemm_choose_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t d
     }
     return GEMM_OK;
   }
-  choose_tc(M, N, K, sms, out_is_f32(dtype) ? 4 : 2, false, out);
+  choose_tc(M, N, K, sms, out_is_f32(dtype) ? 4 : 2, false, out, in_bytes(dtype));
   return GEMM_OK;
 }
 

@@ -244,7 +244,32 @@ __device__ __forceinline__ void epi32(float (&v)[32], const TcParams& p, int csr
   }
 }
 
-template <int BN, int MODE>
+// The TC_BK/16 MMAs of one ring stage (each reads 32 bytes of K per row:
+// 16 bf16/fp16 or 8 TF32 elements), accumulating unless this is the first
+// stage of the unit.
+template <bool PAIR, bool TF32>
+__device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint32_t sa, uint32_t sb, uint32_t lbo_a,
+                                            uint32_t lbo_b, uint32_t kstep_a, uint32_t kstep_b, uint32_t idesc,
+                                            bool first) {
+#pragma unroll
+  for (int kk = 0; kk < TC_BK / 16; ++kk) {
+    const uint64_t ad = smem_desc_sw128(sa + kk * kstep_a, lbo_a, 1024);
+    const uint64_t bd = smem_desc_sw128(sb + kk * kstep_b, lbo_b, 1024);
+    const uint32_t accum = (!first || kk > 0) ? 1u : 0u;
+    if constexpr (PAIR && TF32)
+      tc_mma_tf32_pair(d_tmem, ad, bd, idesc, accum);
+    else if constexpr (PAIR)
+      tc_mma_f16_pair(d_tmem, ad, bd, idesc, accum);
+    else if constexpr (TF32)
+      tc_mma_tf32(d_tmem, ad, bd, idesc, accum);
+    else
+      tc_mma_f16(d_tmem, ad, bd, idesc, accum);
+  }
+}
+
+// TF32: operands are TF32 (fp32 words; kind::tf32 MMAs, 32 K elements per
+// k-block); a compile-time choice, so the 16-bit kernels carry none of it.
+template <int BN, int MODE, bool TF32 = false>
 __global__ void __launch_bounds__(TC_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmW,
@@ -342,6 +367,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      constexpr int kbe = TF32 ? TC_BK_TF32 : TC_BK;
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -359,7 +385,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           const uint32_t fb = full0 + 8 * stage;
           const uint32_t sa = base + Cfg::OFF_A + stage * Cfg::A_STAGE;
           const uint32_t sb = base + Cfg::OFF_B + stage * Cfg::B_STAGE;
-          const int k0 = kb * TC_BK;
+          const int k0 = kb * kbe;
           // Pair: both CTAs' loads complete on the leader's barrier, which the
           // leader arms with both CTAs' bytes.
           uint32_t fbc = fb;
@@ -405,6 +431,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint32_t lbo_b = p.b_mn_major ? 64 * 128 : 16;
       const uint32_t kstep_a = p.a_mn_major ? 16 * 128 : 32;
       const uint32_t kstep_b = p.b_mn_major ? 16 * 128 : 32;
+      const uint32_t idesc = p.idesc;
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -423,15 +450,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tc_fence_after();
           const uint32_t sa = base + Cfg::OFF_A + stage * Cfg::A_STAGE;
           const uint32_t sb = base + Cfg::OFF_B + stage * Cfg::B_STAGE;
-#pragma unroll
-          for (int kk = 0; kk < TC_BK / 16; ++kk) {
-            const uint64_t ad = smem_desc_sw128(sa + kk * kstep_a, lbo_a, 1024);
-            const uint64_t bd = smem_desc_sw128(sb + kk * kstep_b, lbo_b, 1024);
-            if constexpr (PAIR)
-              tc_mma_f16_pair(d_tmem, ad, bd, p.idesc, (kb > x.kb_begin || kk > 0) ? 1u : 0u);
-            else
-              tc_mma_f16(d_tmem, ad, bd, p.idesc, (kb > x.kb_begin || kk > 0) ? 1u : 0u);
-          }
+          issue_stage<PAIR, TF32>(d_tmem, sa, sb, lbo_a, lbo_b, kstep_a, kstep_b, idesc, kb == x.kb_begin);
           // stage free (in both CTAs of a pair) once these MMAs finish
           if constexpr (PAIR)
             tc_commit_pair_multicast(empty0 + 8 * stage, 0x3);
@@ -781,11 +800,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   }
 }
 
-template <int BN, int MODE>
+template <int BN, int MODE, bool TF32 = false>
 cudaError_t launch_gemm_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                               const CUtensorMap& ws, const TcParams& p, int grid, cudaStream_t s) {
   constexpr int smem = TcCfg<BN, MODE>::SMEM_BYTES;
-  auto kern = gemm_tc_kernel<BN, MODE>;
+  auto kern = gemm_tc_kernel<BN, MODE, TF32>;
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   cudaLaunchConfig_t cfg = {};

@@ -4,7 +4,7 @@
 
 namespace dg {
 #define DG_INST(MODE)                                                                              \
-  template cudaError_t launch_gemm_tc_bn<256, MODE>(const CUtensorMap&, const CUtensorMap&,        \
+  template cudaError_t launch_gemm_tc_bn<256, MODE, false>(const CUtensorMap&, const CUtensorMap&,        \
                                                    const CUtensorMap&, const CUtensorMap&, const TcParams&, int, cudaStream_t);
 DG_INST(TC_SOLO)
 DG_INST(TC_PAIR)

@@ -2,6 +2,6 @@
 #include "gemm_tc.cuh"
 
 namespace dg {
-template cudaError_t launch_gemm_tc_bn<64, TC_SOLO>(const CUtensorMap&, const CUtensorMap&,
+template cudaError_t launch_gemm_tc_bn<64, TC_SOLO, false>(const CUtensorMap&, const CUtensorMap&,
                                                    const CUtensorMap&, const CUtensorMap&, const TcParams&, int, cudaStream_t);
 }  // namespace dg

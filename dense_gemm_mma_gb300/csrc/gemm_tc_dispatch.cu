@@ -3,17 +3,19 @@
 
 namespace dg {
 
-#define DG_EXTERN(BN, MODE)                                                                        \
-  extern template cudaError_t launch_gemm_tc_bn<BN, MODE>(const CUtensorMap&, const CUtensorMap&, \
-                                                          const CUtensorMap&, const CUtensorMap&, \
-                                                          const TcParams&, int, cudaStream_t);
-DG_EXTERN(64, TC_SOLO)
-DG_EXTERN(128, TC_SOLO)
-DG_EXTERN(256, TC_SOLO)
-DG_EXTERN(128, TC_PAIR)
-DG_EXTERN(256, TC_PAIR)
-DG_EXTERN(128, TC_KPAIR)
-DG_EXTERN(256, TC_KPAIR)
+#define DG_EXTERN(BN, MODE, TF32)                                                                    \
+  extern template cudaError_t launch_gemm_tc_bn<BN, MODE, TF32>(const CUtensorMap&, const CUtensorMap&, \
+                                                                const CUtensorMap&, const CUtensorMap&, \
+                                                                const TcParams&, int, cudaStream_t);
+#define DG_EXTERN_BOTH(BN, MODE) DG_EXTERN(BN, MODE, false) DG_EXTERN(BN, MODE, true)
+DG_EXTERN_BOTH(64, TC_SOLO)
+DG_EXTERN_BOTH(128, TC_SOLO)
+DG_EXTERN_BOTH(256, TC_SOLO)
+DG_EXTERN_BOTH(128, TC_PAIR)
+DG_EXTERN_BOTH(256, TC_PAIR)
+DG_EXTERN_BOTH(128, TC_KPAIR)
+DG_EXTERN_BOTH(256, TC_KPAIR)
+#undef DG_EXTERN_BOTH
 #undef DG_EXTERN
 extern template int max_clusters<128, TC_PAIR>();
 extern template int max_clusters<256, TC_PAIR>();
@@ -49,25 +51,34 @@ int tc_max_clusters(int bn, int mode) {
   return 0;
 }
 
-cudaError_t launch_gemm_tc(int bn, int mode, const CUtensorMap& a, const CUtensorMap& b,
-                           const CUtensorMap& c, const CUtensorMap& ws, const TcParams& p, int grid,
-                           cudaStream_t s) {
+namespace {
+template <bool TF32>
+cudaError_t launch_kind(int bn, int mode, const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                        const CUtensorMap& ws, const TcParams& p, int grid, cudaStream_t s) {
   if (mode == TC_PAIR) {
-    if (bn == 256) return launch_gemm_tc_bn<256, TC_PAIR>(a, b, c, ws, p, grid, s);
-    if (bn == 128) return launch_gemm_tc_bn<128, TC_PAIR>(a, b, c, ws, p, grid, s);
+    if (bn == 256) return launch_gemm_tc_bn<256, TC_PAIR, TF32>(a, b, c, ws, p, grid, s);
+    if (bn == 128) return launch_gemm_tc_bn<128, TC_PAIR, TF32>(a, b, c, ws, p, grid, s);
     return cudaErrorInvalidValue;
   }
   if (mode == TC_KPAIR) {
-    if (bn == 256) return launch_gemm_tc_bn<256, TC_KPAIR>(a, b, c, ws, p, grid, s);
-    if (bn == 128) return launch_gemm_tc_bn<128, TC_KPAIR>(a, b, c, ws, p, grid, s);
+    if (bn == 256) return launch_gemm_tc_bn<256, TC_KPAIR, TF32>(a, b, c, ws, p, grid, s);
+    if (bn == 128) return launch_gemm_tc_bn<128, TC_KPAIR, TF32>(a, b, c, ws, p, grid, s);
     return cudaErrorInvalidValue;
   }
   switch (bn) {
-    case 64: return launch_gemm_tc_bn<64, TC_SOLO>(a, b, c, ws, p, grid, s);
-    case 128: return launch_gemm_tc_bn<128, TC_SOLO>(a, b, c, ws, p, grid, s);
-    case 256: return launch_gemm_tc_bn<256, TC_SOLO>(a, b, c, ws, p, grid, s);
+    case 64: return launch_gemm_tc_bn<64, TC_SOLO, TF32>(a, b, c, ws, p, grid, s);
+    case 128: return launch_gemm_tc_bn<128, TC_SOLO, TF32>(a, b, c, ws, p, grid, s);
+    case 256: return launch_gemm_tc_bn<256, TC_SOLO, TF32>(a, b, c, ws, p, grid, s);
     default: return cudaErrorInvalidValue;
   }
+}
+}  // namespace
+
+cudaError_t launch_gemm_tc(int bn, int mode, const CUtensorMap& a, const CUtensorMap& b,
+                           const CUtensorMap& c, const CUtensorMap& ws, const TcParams& p, int grid,
+                           cudaStream_t s) {
+  return p.tf32 ? launch_kind<true>(bn, mode, a, b, c, ws, p, grid, s)
+                : launch_kind<false>(bn, mode, a, b, c, ws, p, grid, s);
 }
 
 }  // namespace dg

@@ -12,6 +12,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cstdlib>
 
 #include "kernels.h"
@@ -404,6 +405,31 @@ __global__ void __launch_bounds__(256) tile_reduce_kernel(const TileReduceArgs a
   }
 }
 
+// --------------------------------------------------------------- transpose
+// out (cols x rows) <- in (rows x cols)^T for 32-bit words, in 32 x 32 tiles
+// staged in shared memory (a padding column keeps the column-wise reads free
+// of bank conflicts); both the loads and the stores are row-contiguous.
+__global__ void __launch_bounds__(256) transpose32_kernel(const uint32_t* __restrict__ in, int64_t ld_in,
+                                                          int rows, int cols, uint32_t* __restrict__ out,
+                                                          int64_t ld_out) {
+  __shared__ uint32_t tile[32][33];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 8 rows of 32 per pass
+  for (int by = blockIdx.y * 32; by < rows; by += gridDim.y * 32) {
+    for (int bx = blockIdx.x * 32; bx < cols; bx += gridDim.x * 32) {
+      for (int j = ty; j < 32; j += 8) {
+        const int r = by + j, c = bx + tx;
+        if (r < rows && c < cols) tile[j][tx] = in[static_cast<int64_t>(r) * ld_in + c];
+      }
+      __syncthreads();
+      for (int j = ty; j < 32; j += 8) {
+        const int r = bx + j, c = by + tx;  // row of out = column of in
+        if (r < cols && c < rows) out[static_cast<int64_t>(r) * ld_out + c] = tile[tx][j];
+      }
+      __syncthreads();
+    }
+  }
+}
+
 // ------------------------------------------------------------------- scale
 __global__ void __launch_bounds__(256) scale_kernel(int M, int N, void* D, int64_t ldd, const void* C,
                                                     int64_t ldc, const EpiParams e) {
@@ -517,6 +543,16 @@ cudaError_t launch_tile_reduce(const TileReduceArgs& a, cudaStream_t s, int sms)
   if (const char* v = std::getenv("GEMM_PDL"))  // GEMM_PDL=0: ordinary launch, for comparison
     if (v[0] == '0') cfg.numAttrs = 0;
   return cudaLaunchKernelEx(&cfg, tile_reduce_kernel, a);
+}
+
+cudaError_t launch_transpose32(const void* in, int64_t ld_in, int rows, int cols, void* out, int64_t ld_out,
+                               cudaStream_t s) {
+  if (rows <= 0 || cols <= 0) return cudaSuccess;
+  const dim3 grid(static_cast<unsigned>(std::min(65535, (cols + 31) / 32)),
+                  static_cast<unsigned>(std::min(65535, (rows + 31) / 32)));
+  transpose32_kernel<<<grid, 256, 0, s>>>(static_cast<const uint32_t*>(in), ld_in, rows, cols,
+                                          static_cast<uint32_t*>(out), ld_out);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_scale(int M, int N, void* D, int64_t ldd, const void* C, int64_t ldc, EpiParams e,

@@ -37,7 +37,8 @@ enum TcMode : int {
 };
 
 constexpr int TC_BM = 128;       // output rows per tile (one tcgen05.mma M=128)
-constexpr int TC_BK = 64;        // K elements per stage: 64 x 2 B = one 128-B swizzle row
+constexpr int TC_BK = 64;        // 16-bit K elements per stage: 64 x 2 B = one 128-B swizzle row
+constexpr int TC_BK_TF32 = 32;   // TF32 (fp32 word) K elements per stage: the same 128 bytes
 constexpr int TC_THREADS = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int TC_EPI_WARPS = 4;
 
@@ -58,7 +59,9 @@ __host__ __device__ inline void tile_coords(int t, int num_m_blocks, int num_n_b
 struct TcParams {
   int M, N, K;
   int num_m_blocks, num_n_blocks;
-  int k_blocks;      // ceil(K / TC_BK)
+  int k_blocks;      // ceil(K / kb_elems)
+  int kb_elems;      // K elements per k-block: TC_BK (bf16/fp16) or TC_BK_TF32
+  int tf32;          // operands are TF32 (kind::tf32 MMAs; both K-major)
   int raster_group;  // output-tile rows per rasterisation group
   // Work units, in this order: dp_units whole tiles (raster positions
   // 0 .. dp_units-1, all of K, final output); then `splitk` K slices of each of
@@ -102,6 +105,7 @@ int tc_max_clusters(int bn, int mode);
 // k-blocks (rounded up), and no unit is a tail slice (tail_tiles = 0).
 // c: C (box 32 rows x 128 bytes); ws: the fp32 partial workspace (box 32 x 32),
 // used only when p.tail_tiles > 0.
+// p.tf32 selects the TF32 instantiation (kind::tf32, 32 K elements per k-block).
 cudaError_t launch_gemm_tc(int bn, int mode, const CUtensorMap& a, const CUtensorMap& b,
                            const CUtensorMap& c, const CUtensorMap& ws, const TcParams& p, int grid,
                            cudaStream_t s);
@@ -146,6 +150,11 @@ struct TileReduceArgs {
   EpiParams e;
 };
 cudaError_t launch_tile_reduce(const TileReduceArgs& a, cudaStream_t s, int sms);
+
+// out (cols x rows, row stride ld_out) <- transpose of in (rows x cols, row
+// stride ld_in), 32-bit elements: makes a TF32 operand K-major.
+cudaError_t launch_transpose32(const void* in, int64_t ld_in, int rows, int cols, void* out, int64_t ld_out,
+                               cudaStream_t s);
 
 // D <- act(beta * C) (K == 0 or alpha == 0); C may be D.
 cudaError_t launch_scale(int M, int N, void* D, int64_t ldd, const void* C, int64_t ldc, EpiParams e,

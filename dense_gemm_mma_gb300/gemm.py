@@ -23,15 +23,15 @@ GEMM_ERR_CUDA = 6
 GEMM_ERR_TIMEOUT = 7
 
 GEMM_OP_N, GEMM_OP_T = 0, 1
-GEMM_TYPE_BF16, GEMM_TYPE_F16, GEMM_TYPE_F32 = 0, 1, 2
-GEMM_BF16_F32, GEMM_BF16_BF16, GEMM_F16_F32, GEMM_F16_F16 = 0, 1, 2, 3
+GEMM_TYPE_BF16, GEMM_TYPE_F16, GEMM_TYPE_F32, GEMM_TYPE_TF32 = 0, 1, 2, 3
+GEMM_BF16_F32, GEMM_BF16_BF16, GEMM_F16_F32, GEMM_F16_F16, GEMM_TF32_F32 = 0, 1, 2, 3, 4
 GEMM_ACT_NONE, GEMM_ACT_LEAKY_RELU, GEMM_ACT_RELU, GEMM_ACT_GELU, GEMM_ACT_SILU = 0, 1, 2, 3, 4
 
 PATH_NAMES = {0: "none", 1: "tc", 2: "tc_splitk", 3: "gemv_rowdot", 4: "gemv_colstream",
               5: "gemv_generic", 6: "scale", 7: "tc_splitk_cluster", 8: "tc_tail_split"}
 
 DTYPES = {("bf16", "f32"): GEMM_BF16_F32, ("bf16", "bf16"): GEMM_BF16_BF16,
-          ("f16", "f32"): GEMM_F16_F32, ("f16", "f16"): GEMM_F16_F16}
+          ("f16", "f32"): GEMM_F16_F32, ("f16", "f16"): GEMM_F16_F16, ("tf32", "f32"): GEMM_TF32_F32}
 
 
 class gemm_epilogue_t(ctypes.Structure):
@@ -241,7 +241,8 @@ class Plan:
         """C <- act(alpha*op(A)@op(B) + beta*C) on torch tensors holding the
         STORED matrices (A is K x M when transA, B is N x K when transB)."""
         import torch
-        in_t = {torch.bfloat16: "bf16", torch.float16: "f16"}[A.dtype]
+        # fp32 operands are read as TF32 by the tensor cores (GEMM_TF32_F32)
+        in_t = {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "tf32"}[A.dtype]
         out_t = {torch.float32: "f32", torch.bfloat16: "bf16", torch.float16: "f16"}[C.dtype]
         if B.dtype != A.dtype:
             raise ValueError("A and B must have the same dtype")

@@ -9,7 +9,7 @@ attainable rate is min(peak FLOP/s, intensity * memory bandwidth).
 """
 from __future__ import annotations
 
-ELEM_BYTES = {"bf16": 2, "f16": 2, "f32": 4}
+ELEM_BYTES = {"bf16": 2, "f16": 2, "f32": 4, "tf32": 4}
 
 
 def gemm_flops(M: int, N: int, K: int) -> int:

@@ -68,7 +68,14 @@ typedef enum {
   GEMM_BF16_F32 = 0,
   GEMM_BF16_BF16 = 1,
   GEMM_F16_F32 = 2,
-  GEMM_F16_F16 = 3
+  GEMM_F16_F16 = 3,
+  /* A and B are fp32 words read as TF32 by the tensor core: sign, exponent and
+   * the 10 highest fraction bits (the 13 lowest are dropped), fp32
+   * accumulation, C fp32 ("Matrix Multiplication Background User's Guide",
+   * section 2.2, Table 1).  Every shape runs on the tensor cores, M = 1 or
+   * N = 1 included.  Operands stored M/N-major (transA = T, transB = N) are
+   * first transposed into plan workspace: the TF32 MMAs read K-major tiles. */
+  GEMM_TF32_F32 = 4
 } gemm_dtype_t;
 
 typedef enum {
@@ -162,6 +169,9 @@ gemm_status_t gemm_plan_create(gemm_plan_t* plan, int device);
  *    lda, ldb, ldc times the element size are multiples of 16 bytes -- the
  *    rule of Table 1 of the guide's section 2.2 for FP16 (multiples of 8
  *    elements), which the Tensor Memory Accelerator requires here.
+ *  - GEMM_TF32_F32 (always the tensor-core path): A and B 16-byte aligned with
+ *    lda, ldb multiples of 4 elements (Table 1's TF32 row); C 4-byte aligned,
+ *    and 16-byte aligned with ldc a multiple of 4 when N >= 4.
  * Violations return GEMM_ERR_INVALID_ARG or GEMM_ERR_ALIGNMENT.
  *
  * Split-K and GEMV with K split use the plan's workspace; the first call that
@@ -187,14 +197,16 @@ gemm_status_t gemm_plan_destroy(gemm_plan_t plan);
 const char* gemm_status_string(gemm_status_t status);
 
 /* Element types of gemm_run_ex's matrices. */
-typedef enum { GEMM_TYPE_BF16 = 0, GEMM_TYPE_F16 = 1, GEMM_TYPE_F32 = 2 } gemm_type_t;
+typedef enum { GEMM_TYPE_BF16 = 0, GEMM_TYPE_F16 = 1, GEMM_TYPE_F32 = 2,
+               GEMM_TYPE_TF32 = 3 /* operands only (ab_type): fp32 words read as TF32 */ } gemm_type_t;
 
 /* D <- act(alpha * op(A) @ op(B) + beta * C) with a separate output D: the
  * gemm_run operation where the C that beta scales is read from one matrix and
  * the result written to another, each with its own leading dimension and
  * element type (e.g. fp32 C in, bf16 D out).
- *   ab_type  GEMM_TYPE_BF16 or GEMM_TYPE_F16: A and B, as in gemm_run.
- *   d_type   GEMM_TYPE_F32 or ab_type: D (M x N, row stride ldd >= N), held to
+ *   ab_type  GEMM_TYPE_BF16, GEMM_TYPE_F16 or GEMM_TYPE_TF32: A and B, as in gemm_run.
+ *   d_type   GEMM_TYPE_F32 or ab_type (GEMM_TYPE_F32 with TF32 operands): D (M x N,
+ *            row stride ldd >= N), held to
  *            gemm_run's rules for C (device pointer, alignment, NULL only
  *            if M*N == 0).
  *   c_type   GEMM_TYPE_BF16, GEMM_TYPE_F16 or GEMM_TYPE_F32: C (M x N, row

@@ -25,7 +25,7 @@ import numpy as np
 import oracle
 from dense_gemm_mma_gb300 import gemm, inputs
 
-ESIZE = {"bf16": 2, "f16": 2, "f32": 4}
+ESIZE = {"bf16": 2, "f16": 2, "f32": 4, "tf32": 4}
 
 
 def decode(bits, fmt):
@@ -52,7 +52,7 @@ def round_up(x, m):
 
 def to_device(arr, fmt):
     import torch
-    if fmt == "f32":
+    if fmt in ("f32", "tf32"):
         return torch.from_numpy(np.ascontiguousarray(arr)).cuda()
     t = torch.from_numpy(np.ascontiguousarray(arr).view(np.int16))
     return t.view(torch.bfloat16 if fmt == "bf16" else torch.float16).cuda()
@@ -61,7 +61,7 @@ def to_device(arr, fmt):
 def from_device(t, fmt):
     import torch
     t = t.cpu()
-    if fmt == "f32":
+    if fmt in ("f32", "tf32"):
         return t.numpy()
     return t.view(torch.int16).numpy().view(np.uint16)
 

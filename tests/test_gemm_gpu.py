@@ -270,6 +270,53 @@ def test_input_slices_through_strides(plan):
         assert np.all(np.abs(got - exact) <= 1e-5 * K * amax * bmax + 2.0 ** -21 * np.abs(exact)), (M, N, K)
 
 
+# --------------------------------------------------------------------- TF32
+
+@pytest.mark.parametrize("ta,tb", [(False, True), (False, False), (True, True), (True, False)])
+def test_tf32_layouts_ragged(plan, ta, tb):
+    """TF32 operands (fp32 words, low 13 fraction bits dropped) in every
+    layout; M/N-major operands are transposed into workspace first."""
+    r = run_case(plan, 300, 520, 333, in_fmt="tf32", ta=ta, tb=tb, seed=140 + 2 * ta + tb)
+    assert r.info["tile_k"] == 32 and r.info["launches"] >= 1 + int(ta) + int(not tb)
+
+
+def test_tf32_tile_widths_pair_kpair_splits(plan):
+    envs = [{"GEMM_FORCE_TILE": "128x64"}, {"GEMM_FORCE_TILE": "128x128"}, {"GEMM_FORCE_TILE": "128x256"},
+            {"GEMM_FORCE_TILE": "256x256"}, {"GEMM_SPLITK_CLUSTER": "1", "GEMM_FORCE_SPLITK": "2"},
+            {"GEMM_FORCE_SPLITK": "5", "GEMM_SPLITK_CLUSTER": "0"},
+            {"GEMM_TAIL_SPLIT": "3", "GEMM_FORCE_TILE": "128x128"}]
+    for env in envs:
+        M, N = (1300, 2000) if "GEMM_TAIL_SPLIT" in env else (257, 300)
+        run_case(plan, M, N, 515, in_fmt="tf32", tb=True, beta=0.5, act=1, slope=0.1, env=env, seed=150)
+
+
+def test_tf32_gemv_shapes_and_edges(plan):
+    run_case(plan, 1, 3000, 1000, in_fmt="tf32", seed=160)            # M = 1 on the tensor cores
+    run_case(plan, 3000, 1, 1000, in_fmt="tf32", tb=True, seed=161)   # N = 1
+    run_case(plan, 200, 3, 300, in_fmt="tf32", tb=True, beta=1.0, seed=162, pad=(0, 0, 1))  # N < 4, odd ldc
+    run_case(plan, 129, 257, 7, in_fmt="tf32", seed=163)              # K < 32: one partial k-block
+
+
+def test_tf32_drops_the_low_fraction_bits(plan):
+    """Every A entry is the fp32 word 1 + 2^-11 + 2^-12, every B entry 1: with
+    the 13 low fraction bits dropped each product is 1 and every output is
+    exactly K; rounding to 10 bits would give K * (1 + 2^-10)."""
+    torch = pytest.importorskip("torch")
+    from dense_gemm_mma_gb300 import gemm
+    M, N, K = 256, 256, 1024
+    A = torch.full((M, K), 1.0 + 2.0 ** -11 + 2.0 ** -12, device="cuda", dtype=torch.float32)
+    B = torch.ones(N, K, device="cuda", dtype=torch.float32)
+    C = torch.zeros(M, N, device="cuda", dtype=torch.float32)
+    assert plan.run(A, B, C, transB=True) == gemm.GEMM_OK
+    torch.cuda.synchronize()
+    assert torch.all(C == float(K)).item()
+
+
+def test_tf32_full_size_sampled(plan):
+    r = run_case(plan, 8192, 8192, 8192, in_fmt="tf32", tb=True, sample=4096, seed=1236)
+    assert r.info["tile_k"] == 32
+
+
 # ------------------------------------------- split-K reduced on chip (K pair)
 
 KPAIR = {"GEMM_SPLITK_CLUSTER": "1", "GEMM_FORCE_SPLITK": "2"}

@@ -118,7 +118,7 @@ def test_check_args_rejects():
     assert chk(-1, 8, 8) == E
     assert chk(8, -1, 8) == E
     assert chk(8, 8, -1) == E
-    assert chk(8, 8, 8, dtype=4) == E
+    assert chk(8, 8, 8, dtype=5) == E
     assert chk(8, 8, 8, ta=2) == E
     assert chk(8, 8, 8, act=5) == E and chk(8, 8, 8, act=-1) == E
     for act in (g.GEMM_ACT_RELU, g.GEMM_ACT_GELU, g.GEMM_ACT_SILU):
@@ -270,6 +270,23 @@ def test_planner_forced_pair(monkeypatch):
     c = g.gemm_choose_config(1000, 1000, 1000, 0, 0, 0, 152)
     assert c.tile_m == 256 and c.tile_n == 256 and c.cta_per_tile == 2
     assert c.tiles == 4 * 4 and c.grid == 2 * c.units
+
+
+def test_planner_tf32():
+    """TF32: 32 K elements per 128-byte stage row, tensor-core path for every
+    shape (GEMV shapes included)."""
+    c = g.gemm_choose_config(8192, 8192, 8192, g.GEMM_TF32_F32, 0, 1, 152)
+    assert c.tile_k == 32 and c.path in (1, 8)
+    for shape in [(1, 4096, 4096), (4096, 1, 4096)]:
+        c = g.gemm_choose_config(*shape, g.GEMM_TF32_F32, 0, 1, 152)
+        assert c.path in (1, 2, 7, 8) and c.tile_k == 32
+    ok = g.GEMM_OK
+    chk = lambda *a, **k: g.gemm_check_args(*a, **k)
+    A, B, C = 0x100000, 0x200000, 0x300000
+    assert chk(64, 64, 64, A, 64, B, 64, C, 64, 1.0, g.GEMM_TF32_F32, 0, 1) == ok
+    assert chk(64, 64, 62, A, 62, B, 62, C, 64, 1.0, g.GEMM_TF32_F32, 0, 1) == g.GEMM_ERR_ALIGNMENT  # ld % 4
+    assert chk(64, 3, 64, A, 64, B, 64, C + 4, 5, 1.0, g.GEMM_TF32_F32, 0, 1) == ok   # N < 4: C 4-byte aligned
+    assert chk(64, 64, 64, A, 64, B, 64, C, 64, 1.0, 5, 0, 1) == g.GEMM_ERR_INVALID_ARG
 
 
 def test_planner_kpair_switch(monkeypatch):
