@@ -695,7 +695,6 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
   p.K = int(K);
   p.num_m_blocks = int(ceil_div(M, tile_m));
   p.num_n_blocks = int(ceil_div(N, bn));
-  p.kb_elems = kbe;
   p.k_blocks = int(ceil_div(K, kbe));
   p.tf32 = tf32;
   p.raster_group = info->raster_group;

@@ -406,24 +406,41 @@ __global__ void __launch_bounds__(256) tile_reduce_kernel(const TileReduceArgs a
 }
 
 // --------------------------------------------------------------- transpose
-// out (cols x rows) <- in (rows x cols)^T for 32-bit words, in 32 x 32 tiles
+// out (cols x rows) <- in (rows x cols)^T for 32-bit words, in 64 x 64 tiles
 // staged in shared memory (a padding column keeps the column-wise reads free
-// of bank conflicts); both the loads and the stores are row-contiguous.
+// of bank conflicts).  Each thread issues its 16 loads before any store, so
+// enough bytes are in flight to stream from HBM; loads and stores are both
+// row-contiguous (32 words per warp instruction).
+constexpr int kTrTile = 64;
 __global__ void __launch_bounds__(256) transpose32_kernel(const uint32_t* __restrict__ in, int64_t ld_in,
                                                           int rows, int cols, uint32_t* __restrict__ out,
                                                           int64_t ld_out) {
-  __shared__ uint32_t tile[32][33];
+  __shared__ uint32_t tile[kTrTile][kTrTile + 1];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 8 rows of 32 per pass
-  for (int by = blockIdx.y * 32; by < rows; by += gridDim.y * 32) {
-    for (int bx = blockIdx.x * 32; bx < cols; bx += gridDim.x * 32) {
-      for (int j = ty; j < 32; j += 8) {
-        const int r = by + j, c = bx + tx;
-        if (r < rows && c < cols) tile[j][tx] = in[static_cast<int64_t>(r) * ld_in + c];
+  for (int by = blockIdx.y * kTrTile; by < rows; by += gridDim.y * kTrTile) {
+    for (int bx = blockIdx.x * kTrTile; bx < cols; bx += gridDim.x * kTrTile) {
+      uint32_t v[16];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = by + ty + 8 * j, c = bx + tx + 32 * h;
+          v[2 * j + h] = (r < rows && c < cols) ? in[static_cast<int64_t>(r) * ld_in + c] : 0u;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) tile[ty + 8 * j][tx + 32 * h] = v[2 * j + h];
       }
       __syncthreads();
-      for (int j = ty; j < 32; j += 8) {
-        const int r = bx + j, c = by + tx;  // row of out = column of in
-        if (r < cols && c < rows) out[static_cast<int64_t>(r) * ld_out + c] = tile[tx][j];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = bx + ty + 8 * j, c = by + tx + 32 * h;  // row of out = column of in
+          if (r < cols && c < rows) out[static_cast<int64_t>(r) * ld_out + c] = tile[tx + 32 * h][ty + 8 * j];
+        }
       }
       __syncthreads();
     }
@@ -548,8 +565,8 @@ cudaError_t launch_tile_reduce(const TileReduceArgs& a, cudaStream_t s, int sms)
 cudaError_t launch_transpose32(const void* in, int64_t ld_in, int rows, int cols, void* out, int64_t ld_out,
                                cudaStream_t s) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
-  const dim3 grid(static_cast<unsigned>(std::min(65535, (cols + 31) / 32)),
-                  static_cast<unsigned>(std::min(65535, (rows + 31) / 32)));
+  const dim3 grid(static_cast<unsigned>(std::min(65535, (cols + kTrTile - 1) / kTrTile)),
+                  static_cast<unsigned>(std::min(65535, (rows + kTrTile - 1) / kTrTile)));
   transpose32_kernel<<<grid, 256, 0, s>>>(static_cast<const uint32_t*>(in), ld_in, rows, cols,
                                           static_cast<uint32_t*>(out), ld_out);
   return cudaGetLastError();

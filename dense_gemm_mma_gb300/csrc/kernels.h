@@ -59,9 +59,8 @@ __host__ __device__ inline void tile_coords(int t, int num_m_blocks, int num_n_b
 struct TcParams {
   int M, N, K;
   int num_m_blocks, num_n_blocks;
-  int k_blocks;      // ceil(K / kb_elems)
-  int kb_elems;      // K elements per k-block: TC_BK (bf16/fp16) or TC_BK_TF32
-  int tf32;          // operands are TF32 (kind::tf32 MMAs; both K-major)
+  int k_blocks;      // ceil(K / k-block elements): TC_BK (bf16/fp16) or TC_BK_TF32 per k-block
+  int tf32;          // operands are TF32 (the kind::tf32 instantiation; both K-major)
   int raster_group;  // output-tile rows per rasterisation group
   // Work units, in this order: dp_units whole tiles (raster positions
   // 0 .. dp_units-1, all of K, final output); then `splitk` K slices of each of
