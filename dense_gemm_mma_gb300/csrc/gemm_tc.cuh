@@ -94,6 +94,9 @@ struct TcCfg {
   // staging buffers of a warp hold 32 rows x 64 fp32 partials).
   static constexpr int KP_ROUNDS = BN / 128;
   static_assert(!KPAIR || BN >= 128, "a K pair finishes 64-column pieces");
+  // On a cluster's last tile the A ring is idle once the accumulator is
+  // complete: it holds the outgoing partials of every warp and round.
+  static_assert(!KPAIR || KP_ROUNDS * TC_EPI_WARPS * 2 * STG_BYTES <= STAGES * A_STAGE, "send buffer");
 };
 
 struct Unit {
@@ -493,7 +496,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     const uint32_t stg0 = base + Cfg::OFF_STG + e * 2 * Cfg::STG_BYTES;
     uint8_t* const stg_p0 = sbase + Cfg::OFF_STG + e * 2 * Cfg::STG_BYTES;
     const uint32_t xfull = xfull0 + 8 * e, xfree = xfree0 + 8 * e;
-    const uint32_t peer_stg = mapa_shared(stg0, peer) + lane * 128;
+    const uint32_t peer_stg0 = mapa_shared(stg0, peer);
+    const uint32_t peer_stg = peer_stg0 + lane * 128;
     const uint32_t peer_xfull = mapa_shared(xfull, peer);
     const uint32_t peer_xfree = mapa_shared(xfree, peer);
     const int sw = lane & 7;  // 128-byte swizzle: 16-byte chunk j of row r lives at j ^ (r % 8)
@@ -524,16 +528,37 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tmem_ld_32x32b_x32(t_row + peer_c + 32, r1);
           tmem_ld_wait(r0);
           tmem_ld_wait(r1);
+          // The cluster's last tile: no stage will be refilled, so the partials
+          // go through this warp's 8 KB of the idle A ring and move as one
+          // bulk copy (faster over distributed shared memory than 16-byte
+          // stores); an earlier tile sends them with st.async.
+          const bool last = u + ncta >= p.units;
+          const uint32_t snd = base + Cfg::OFF_A + (rd * TC_EPI_WARPS + e) * 2 * Cfg::STG_BYTES;
+          if (last) {
+            uint8_t* const snd_p = sbase + Cfg::OFF_A + (rd * TC_EPI_WARPS + e) * 2 * Cfg::STG_BYTES + lane * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int off = (j ^ sw) << 4;
+              *reinterpret_cast<uint4*>(snd_p + off) = make_uint4(r0[4 * j], r0[4 * j + 1], r0[4 * j + 2], r0[4 * j + 3]);
+              *reinterpret_cast<uint4*>(snd_p + Cfg::STG_BYTES + off) =
+                  make_uint4(r1[4 * j], r1[4 * j + 1], r1[4 * j + 2], r1[4 * j + 3]);
+            }
+            fence_proxy_async_smem();  // the copy reads them through the async proxy
+          }
           if (!__all_sync(0xffffffffu, wait_peer(xfree, xphase, WAIT_EPI_EXCHANGE))) {
             ok = false;
             break;
           }
+          if (last) {
+            if (lane == 0) bulk_copy_to_cluster(peer_stg0, snd, 2 * Cfg::STG_BYTES, peer_xfull);
+          } else {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const uint32_t off = uint32_t((j ^ sw) << 4);
-            st_async_v4(peer_stg + off, r0[4 * j], r0[4 * j + 1], r0[4 * j + 2], r0[4 * j + 3], peer_xfull);
-            st_async_v4(peer_stg + Cfg::STG_BYTES + off, r1[4 * j], r1[4 * j + 1], r1[4 * j + 2],
-                        r1[4 * j + 3], peer_xfull);
+            for (int j = 0; j < 8; ++j) {
+              const uint32_t off = uint32_t((j ^ sw) << 4);
+              st_async_v4(peer_stg + off, r0[4 * j], r0[4 * j + 1], r0[4 * j + 2], r0[4 * j + 3], peer_xfull);
+              st_async_v4(peer_stg + Cfg::STG_BYTES + off, r1[4 * j], r1[4 * j + 1], r1[4 * j + 2],
+                          r1[4 * j + 3], peer_xfull);
+            }
           }
         }
         if (!__all_sync(0xffffffffu, wait_peer(xfull, xphase, WAIT_EPI_EXCHANGE))) {

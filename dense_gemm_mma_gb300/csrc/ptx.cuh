@@ -355,6 +355,17 @@ __device__ __forceinline__ void st_async_v4(uint32_t dst_cluster, uint32_t a, ui
       : "memory");
 }
 
+// Bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned) from
+// this CTA's shared memory into the shared memory of a CTA of this cluster,
+// counted in bytes on a barrier of the destination CTA.
+__device__ __forceinline__ void bulk_copy_to_cluster(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                     uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(src), "r"(bytes), "r"(bar_cluster)
+               : "memory");
+}
+
 static __device__ __noinline__ bool wait_bar_slow_cluster(uint32_t bar, uint32_t parity, const Watch w,
                                                           int code) {
   const uint64_t t0 = global_timer_ns();
