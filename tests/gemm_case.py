@@ -202,7 +202,8 @@ def run_case(plan, M, N, K, in_fmt="bf16", out_fmt="f32", ta=False, tb=False, al
                 os.environ[k] = v
 
 
-TYPES = {"bf16": gemm.GEMM_TYPE_BF16, "f16": gemm.GEMM_TYPE_F16, "f32": gemm.GEMM_TYPE_F32}
+TYPES = {"bf16": gemm.GEMM_TYPE_BF16, "f16": gemm.GEMM_TYPE_F16, "f32": gemm.GEMM_TYPE_F32,
+         "tf32": gemm.GEMM_TYPE_TF32}
 
 
 def run_case_ex(plan, M, N, K, in_fmt="bf16", c_fmt="f32", d_fmt="bf16", ta=False, tb=False, alpha=1.0,

@@ -312,6 +312,24 @@ def test_tf32_drops_the_low_fraction_bits(plan):
     assert torch.all(C == float(K)).item()
 
 
+def test_tf32_with_separate_c_and_benchmark_mode():
+    """TF32 operands through gemm_run_ex (bf16 C in, fp32 D out, both operand
+    layouts that need the transpose pre-pass) and under benchmark mode."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_gemm_mma_gb300 import gemm
+    p = gemm.Plan(0)
+    try:
+        run_case_ex(p, 300, 260, 515, in_fmt="tf32", c_fmt="bf16", d_fmt="f32", beta=0.5, act=3, seed=170,
+                    ta=True, pad=(0, 0, 1, 4))
+        assert gemm.gemm_plan_set_autotune(p.handle, True) == gemm.GEMM_OK
+        r = run_case(p, 1300, 1000, 700, in_fmt="tf32", beta=-1.0, seed=171)
+        assert gemm.gemm_plan_tuned_count(p.handle) == 1 and r.info["tile_k"] == 32
+    finally:
+        p.close()
+
+
 def test_tf32_full_size_sampled(plan):
     r = run_case(plan, 8192, 8192, 8192, in_fmt="tf32", tb=True, sample=4096, seed=1236)
     assert r.info["tile_k"] == 32
