@@ -870,7 +870,14 @@ gemm_status_t run_tc(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const voi
   if (e == nullptr) {
     const TcChoice* forced = nullptr;
     TcChoice tuned;
-    if (plan->autotune && use_cache) {
+    // Benchmark mode synchronizes on its trials: not while the stream is
+    // being captured into a CUDA graph (the planner's estimate decides then).
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (plan->autotune && cudaStreamIsCapturing(s, &capture) != cudaSuccess) {
+      cudaGetLastError();
+      capture = cudaStreamCaptureStatusActive;
+    }
+    if (plan->autotune && use_cache && capture == cudaStreamCaptureStatusNone) {
       TcKey shape = key;
       shape.A = shape.B = shape.C = shape.Cin = 0;
       shape.cin_kind = cin.ptr == C ? -1 : cin.kind;  // in place, or a separate C of this kind

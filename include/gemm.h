@@ -147,7 +147,9 @@ typedef struct {
 gemm_status_t gemm_plan_create(gemm_plan_t* plan, int device);
 
 /* C <- act(alpha * op(A) @ op(B) + beta * C), enqueued on `stream` (a
- * cudaStream_t; NULL means the legacy default stream).  See the top of this
+ * cudaStream_t; NULL means the legacy default stream).  Calls may be captured
+ * into a CUDA graph; a call whose shape, pointers and flags the plan has seen
+ * before (same workspace size) adds only kernel launches to the capture.  See the top of this
  * file for the layout of A, B and C; all three are device pointers.
  *
  * Dispatch: M == 0 or N == 0 launches nothing; K == 0 or alpha == 0 gives
@@ -253,7 +255,9 @@ gemm_status_t gemm_plan_set_watchdog(gemm_plan_t plan, uint64_t timeout_ns);
  * host until the trials have run (a one-time cost per shape); if anything
  * fails the planner's pick is kept.  enable = 0 (the default; the
  * environment variable GEMM_AUTOTUNE=1 turns it on at plan creation)
- * uses the planner's estimate alone.  Ignored while any GEMM_FORCE_* /
+ * uses the planner's estimate alone.  Not applied while `stream` is being
+ * captured into a CUDA graph (the planner's estimate decides there).
+ * Ignored while any GEMM_FORCE_* /
  * GEMM_RASTER_GROUP / GEMM_SPLITK_CLUSTER / GEMM_TAIL_SPLIT override is set.
  * GEMM_ERR_INVALID_ARG on NULL. */
 gemm_status_t gemm_plan_set_autotune(gemm_plan_t plan, int enable);

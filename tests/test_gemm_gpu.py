@@ -427,6 +427,53 @@ def test_tail_split_planner_choice_wave_shape(plan):
     assert r.info["path"] == "tc_tail_split" and r.info["tail_tiles"] == 5
 
 
+# ------------------------------------------------------------ CUDA graphs
+
+def test_cuda_graph_capture_and_replay(plan):
+    """A sequence of calls (K pair, tail split, pair tile, GEMV, TF32 with a
+    transpose) captured into one CUDA graph after a warm-up call of each, then
+    replayed on new input values: results match eager calls bit for bit."""
+    torch = pytest.importorskip("torch")
+    from dense_gemm_mma_gb300 import gemm
+    g = torch.Generator(device="cuda").manual_seed(5)
+    shapes = [(8192, 128, 2048, torch.bfloat16, True), (1300, 2000, 512, torch.bfloat16, False),
+              (1024, 1024, 1024, torch.float16, False), (1, 4096, 2048, torch.bfloat16, False),
+              (300, 264, 320, torch.float32, False)]
+    bufs = []
+    for M, N, K, dt, tb in shapes:
+        A = torch.empty(M, K, device="cuda", dtype=dt)
+        B = torch.empty((N, K) if tb else (K, N), device="cuda", dtype=dt)
+        bufs.append((A, B, torch.zeros(M, N, device="cuda"), tb))
+
+    def fill():
+        for A, B, C, _ in bufs:
+            A.copy_(torch.randn(A.shape, device="cuda", generator=g))
+            B.copy_(torch.randn(B.shape, device="cuda", generator=g))
+
+    def run_all():
+        for A, B, C, tb in bufs:
+            assert plan.run(A, B, C, transB=tb) == gemm.GEMM_OK
+
+    fill()
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        run_all()                      # warm-up: plans, descriptors and workspace exist
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        run_all()
+    fill()                             # new values in the same buffers
+    graph.replay()
+    torch.cuda.synchronize()
+    replayed = [C.clone() for _, _, C, _ in bufs]
+    with torch.cuda.stream(stream):
+        run_all()
+    torch.cuda.synchronize()
+    for (_, _, C, _), R in zip(bufs, replayed):
+        assert torch.equal(C, R)
+    assert plan.poll_error() == gemm.GEMM_OK
+
+
 # ----------------------------------------------------------- benchmark mode
 
 def test_autotune_benchmark_mode():
