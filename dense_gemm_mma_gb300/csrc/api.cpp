@@ -190,7 +190,7 @@ void quantization(int64_t M, int64_t N, int tm, int tn, int splitk, int sms, int
 struct Model {
   double peak_flops = 1.7e15;   // sustained dense bf16 rate the kernel reaches per GPU
   double feed = 8.0e10;         // B/s one SM's ring receives from DRAM
-  double reuse_gain = 0.5;      // feed speed-up at full cross-wave L2 reuse
+  double reuse_gain = 0.25;      // feed speed-up at full cross-wave L2 reuse
   double stream_bw = 4.9e12;    // B/s DRAM rate reachable by TMA box streams
   double panel_bw = 5.0e10;     // B/s of one streamed panel
   double hbm_bw = 6.8e12;       // B/s, copy bandwidth
@@ -203,9 +203,10 @@ double tile_efficiency(int bn) { return bn >= 256 ? 1.0 : (bn >= 128 ? 0.85 : 0.
 // Extra fixed cost of a CTA-pair (cluster) launch, fitted on GB300.
 constexpr double kPairFixed = 8.0e-6;
 // Cost of a K pair's on-chip exchange per 64-column round (bn/128 rounds):
-// 32 KB of fp32 partials each way between two SMs, measured on GB300 at
-// ~2 us (distributed shared memory moves ~15-27 GB/s per SM each way).
-constexpr double kKPairRound = 2.0e-6;
+// 32 KB of fp32 partials each way between two SMs (distributed shared memory
+// moves ~15-27 GB/s per SM each way); fitted on GB300 to the K pair against
+// one-CTA tiles at 256^3 ... 2048^3 and 8192 x 128 x 8192.
+constexpr double kKPairRound = 1.2e-6;
 
 // Distinct A row-panels and B column-panels among the first `count` units of
 // the kernel's unit order (gemm_tc.cuh: decode_unit): slice-major, then groups
