@@ -86,6 +86,9 @@ struct gemm_plan {
   size_t tws_bytes = 0;
   size_t counter_count = 0;
   uint64_t watchdog_ns = 2000000000ull;
+  // Kernels launch as programmatic dependents of the stream's previous kernel
+  // (their launch and prologue overlap its tail); GEMM_PDL=0 turns this off.
+  bool pdl = true;
   gemm_config_info_t last{};
   // Repeated calls with the same shapes, pointers and flags skip planning and
   // descriptor encoding (host time that would otherwise sit in front of the
@@ -592,6 +595,7 @@ gemm_status_t run_gemv(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const v
   g.cin = cin.ptr;
   g.inc_cin = N == 1 ? cin.ld : 1;  // output r is C(r, 0) (N == 1) or C(0, r) (M == 1)
   g.e = e;
+  g.pdl = plan->pdl;
   bool row_major_w;  // true: W rows run along K (rowdot); false: W rows run along R (colstream)
   if (N == 1) {      // C(i,0) = sum_k op(A)(i,k) op(B)(k,0)
     g.R = int(M);
@@ -748,6 +752,7 @@ gemm_status_t launch_entry(gemm_plan* plan, TcEntry* e, int64_t M, int64_t N, vo
   p.act = epi.act;
   p.slope = epi.slope;
   p.timeout_ns = plan->watchdog_ns;
+  p.pdl = plan->pdl;
   const int mode = tc_mode(e->info);
   const int tail = e->p.tail_tiles;  // tiles whose K slices a second launch reduces
   if (tail > 0) {
@@ -943,6 +948,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* plan, int device) {
   p->device = device;
   p->sms = prop.multiProcessorCount;
   p->autotune = env_int("GEMM_AUTOTUNE", 0) != 0;
+  p->pdl = env_int("GEMM_PDL", 1) != 0;
   if (const char* w = std::getenv("GEMM_WATCHDOG_NS")) {
     const unsigned long long v = std::strtoull(w, nullptr, 10);
     if (v >= 1000) p->watchdog_ns = v;

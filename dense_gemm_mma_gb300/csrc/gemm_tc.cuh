@@ -300,6 +300,52 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(sbase + Cfg::OFF_MISC);
   volatile int* const abort_flag = reinterpret_cast<volatile int*>(sbase + Cfg::OFF_MISC + 4);
 
+  // Units: a cluster walks tiles; a K pair's CTA r takes the r-th K half.
+  const int cta0 = CLUSTER ? int(blockIdx.x) / 2 : int(blockIdx.x);
+  const int ncta = CLUSTER ? int(gridDim.x) / 2 : int(gridDim.x);
+  auto unit_of = [&](int u) {
+    Unit x = decode_unit(u, p);
+    if constexpr (KPAIR) {
+      x.split = int(rank);
+      x.kb_begin = int(rank) * p.kb_per_split;
+      x.kb_end = min(p.k_blocks, x.kb_begin + p.kb_per_split);
+    }
+    return x;
+  };
+  // One ring stage's loads (producer thread): this CTA's rows of A and
+  // columns of B for k-block kb of unit x.  A pair's loads complete on the
+  // leader's barrier, which the leader arms with both CTAs' bytes.
+  auto issue_loads = [&](int stage, const Unit& x, int kb) {
+    constexpr int kbe = TF32 ? TC_BK_TF32 : TC_BK;
+    const int m0 = x.m_blk * Cfg::TILE_M + (PAIR ? int(rank) * TC_BM : 0);
+    const int n0 = x.n_blk * BN + (PAIR ? int(rank) * BNC : 0);
+    const uint32_t fb = full0 + 8 * stage;
+    const uint32_t sa = base + Cfg::OFF_A + stage * Cfg::A_STAGE;
+    const uint32_t sb = base + Cfg::OFF_B + stage * Cfg::B_STAGE;
+    const int k0 = kb * kbe;
+    uint32_t fbc = fb;
+    if constexpr (PAIR) fbc = mapa_shared(fb, 0);
+    if (leader) mbar_arrive_expect_tx(fb, (PAIR ? 2 : 1) * (Cfg::A_STAGE + Cfg::B_STAGE));
+    auto load = [&](uint32_t dst, const CUtensorMap* m, int cx, int cy) {
+      if constexpr (PAIR)
+        tma_load_2d_pair(dst, m, fbc, cx, cy);
+      else
+        tma_load_2d(dst, m, fb, cx, cy);
+    };
+    if (!p.a_mn_major) {
+      load(sa, &tmA, k0, m0);  // 128 rows x 64 K
+    } else {
+      load(sa, &tmA, m0, k0);  // 64 K rows x 64 M, twice
+      load(sa + 64 * 128, &tmA, m0 + 64, k0);
+    }
+    if (!p.b_mn_major) {
+      load(sb, &tmB, k0, n0);  // BNC rows x 64 K
+    } else {
+#pragma unroll
+      for (int j = 0; j < BNC / 64; ++j) load(sb + j * 64 * 128, &tmB, n0 + 64 * j, k0);
+    }
+  };
+
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
@@ -339,6 +385,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   else
     __syncthreads();
   tc_fence_after();
+  // Launched as a programmatic dependent, the prologue above overlapped the
+  // previous kernel's tail; its results are needed from here on.
+  wait_prior_grid();
   const uint32_t tmem_base = *tmem_slot;
   // A dependent grid (the split-K reduction) may be scheduled now; it waits
   // for this grid's completion before it reads anything.
@@ -354,64 +403,21 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   auto wait_peer = [&](uint32_t bar, uint32_t parity, int code) {
     return wait_bar_cluster(bar, parity, w, code);
   };
-  // Units: a cluster walks tiles; a K pair's CTA r takes the r-th K half.
-  const int cta0 = CLUSTER ? int(blockIdx.x) / 2 : int(blockIdx.x);
-  const int ncta = CLUSTER ? int(gridDim.x) / 2 : int(gridDim.x);
-  auto unit_of = [&](int u) {
-    Unit x = decode_unit(u, p);
-    if constexpr (KPAIR) {
-      x.split = int(rank);
-      x.kb_begin = int(rank) * p.kb_per_split;
-      x.kb_end = min(p.k_blocks, x.kb_begin + p.kb_per_split);
-    }
-    return x;
-  };
-
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      constexpr int kbe = TF32 ? TC_BK_TF32 : TC_BK;
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
       bool ok = true;
       for (int u = cta0; u < p.units && ok; u += ncta) {
         const Unit x = unit_of(u);
-        // this CTA's rows of A and columns of B
-        const int m0 = x.m_blk * Cfg::TILE_M + (PAIR ? int(rank) * TC_BM : 0);
-        const int n0 = x.n_blk * BN + (PAIR ? int(rank) * BNC : 0);
         for (int kb = x.kb_begin; kb < x.kb_end; ++kb) {
           if (!wait(empty0 + 8 * stage, phase ^ 1u, WAIT_PRODUCER_EMPTY)) {
             ok = false;
             break;
           }
-          const uint32_t fb = full0 + 8 * stage;
-          const uint32_t sa = base + Cfg::OFF_A + stage * Cfg::A_STAGE;
-          const uint32_t sb = base + Cfg::OFF_B + stage * Cfg::B_STAGE;
-          const int k0 = kb * kbe;
-          // Pair: both CTAs' loads complete on the leader's barrier, which the
-          // leader arms with both CTAs' bytes.
-          uint32_t fbc = fb;
-          if constexpr (PAIR) fbc = mapa_shared(fb, 0);
-          if (leader) mbar_arrive_expect_tx(fb, (PAIR ? 2 : 1) * (Cfg::A_STAGE + Cfg::B_STAGE));
-          auto load = [&](uint32_t dst, const CUtensorMap* m, int cx, int cy) {
-            if constexpr (PAIR)
-              tma_load_2d_pair(dst, m, fbc, cx, cy);
-            else
-              tma_load_2d(dst, m, fb, cx, cy);
-          };
-          if (!p.a_mn_major) {
-            load(sa, &tmA, k0, m0);  // 128 rows x 64 K
-          } else {
-            load(sa, &tmA, m0, k0);  // 64 K rows x 64 M, twice
-            load(sa + 64 * 128, &tmA, m0 + 64, k0);
-          }
-          if (!p.b_mn_major) {
-            load(sb, &tmB, k0, n0);  // BNC rows x 64 K
-          } else {
-#pragma unroll
-            for (int j = 0; j < BNC / 64; ++j) load(sb + j * 64 * 128, &tmB, n0 + 64 * j, k0);
-          }
+          issue_loads(stage, x, kb);
           ++issued;
           if (++stage == S) {
             stage = 0;
@@ -662,7 +668,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (lane == 0) bulk_wait<0>();
+    // Every partial sum the peer sends this warp has arrived (or the warp gave
+    // up): its side of the exchange is over.
+    cluster_arrive();
+    // The stores must have read the staging buffers before the CTA exits; the
+    // grid's completion covers their writes to global memory.
+    if (lane == 0) bulk_wait_read<0>();
   } else {
     // ------------------------------------------------------------ epilogue
     const int e = warp - 2;  // staging buffers / C-load barrier of this warp
@@ -803,15 +814,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
-    if (lane == 0) bulk_wait<0>();
+    // The stores must have read the staging buffers before the CTA exits; the
+    // grid's completion covers their writes to global memory.
+    if (lane == 0) bulk_wait_read<0>();
   }
 
   // ------------------------------------------------------------- teardown
   // A cluster's CTAs stay until both are done: a pair leader's MMAs read the
-  // peer's shared memory and write its tensor memory; a K pair writes partial
-  // sums into the peer's shared memory and arrives on its barriers.
+  // peer's shared memory and write its tensor memory, so a pair synchronises
+  // before it frees tensor memory.  A K pair's CTAs write partial sums into
+  // each other's shared memory and arrive on each other's barriers: the
+  // producer and MMA warps, done with the peer from the start, and the
+  // epilogue warps, once their exchange is over, announce it; each CTA frees
+  // its own tensor memory and waits for the peer's announcement only before
+  // it exits.
+  if constexpr (KPAIR) {
+    if (warp < 2) cluster_arrive();
+  }
   tc_fence_before();
-  if constexpr (CLUSTER)
+  if constexpr (PAIR)
     cluster_sync();
   else
     __syncthreads();
@@ -823,6 +844,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     else
       tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
   }
+  if constexpr (KPAIR) cluster_wait();
 }
 
 template <int BN, int MODE, bool TF32 = false>
@@ -837,13 +859,22 @@ cudaError_t launch_gemm_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const 
   cfg.blockDim = dim3(TC_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = MODE != TC_SOLO ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (MODE != TC_SOLO) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = 2;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (p.pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = MODE != TC_SOLO ? 1 : 0;
+  cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, kern, a, b, c, ws, p);
 }
 

@@ -116,6 +116,7 @@ __device__ __forceinline__ uint4 load_x_vec(const uint16_t* x, const uint16_t* x
 template <bool F16, bool kXDirect>
 __global__ void __launch_bounds__(kRowdotThreads)
     gemv_rowdot_kernel(const GemvArgs g) {
+  wait_prior_grid();
   extern __shared__ __align__(16) uint16_t xs[];
   const uint16_t* x = static_cast<const uint16_t*>(g.x);
   const int K = g.K;
@@ -179,6 +180,7 @@ __device__ __forceinline__ void fma_row(float (&acc)[8], uint4 wv, float xf) {
 template <bool F16>
 __global__ void __launch_bounds__(kColThreads)
     gemv_colstream_kernel(const GemvArgs g, const ColstreamPlan cp, float* ws, unsigned* counters) {
+  wait_prior_grid();
   __shared__ float red[kColGroups][kColCols];
   __shared__ float xsl[kColMaxKc];
   __shared__ unsigned ticket;
@@ -302,6 +304,7 @@ __global__ void __launch_bounds__(kColThreads)
 // Any strides: one warp per output, lanes interleaved over K.
 template <bool F16>
 __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvArgs g) {
+  wait_prior_grid();
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
@@ -327,7 +330,7 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvArgs g) {
 __global__ void __launch_bounds__(256) tile_reduce_kernel(const TileReduceArgs a) {
   // Launched as a programmatic dependent of the GEMM that writes the partials:
   // this CTA may start before that grid ends, so wait for its results here.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  wait_prior_grid();
   const EpiParams& e = a.e;
   const int gpr = a.tile_n >> 2;
   const int64_t per_tile = static_cast<int64_t>(a.tile_m) * gpr;
@@ -492,16 +495,17 @@ cudaError_t launch_gemv_rowdot(const GemvArgs& g, cudaStream_t s, int sms) {
   const bool direct = g.incx == 1 && (reinterpret_cast<uintptr_t>(g.x) & 15u) == 0;
   const int smem = direct ? 0 : ((g.K + 7) & ~7) * 2;
   const int grid = grid_for(g.R, kRowdotThreads / 32, sms, 8);
+  cudaError_t err = cudaSuccess;
   auto go = [&](auto kern) {
     if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    kern<<<grid, kRowdotThreads, smem, s>>>(g);
+    err = launch_k(kern, dim3(grid), dim3(kRowdotThreads), smem, s, g.pdl != 0, g);
   };
   if (g.in_f16) {
     if (direct) go(gemv_rowdot_kernel<true, true>); else go(gemv_rowdot_kernel<true, false>);
   } else {
     if (direct) go(gemv_rowdot_kernel<false, true>); else go(gemv_rowdot_kernel<false, false>);
   }
-  return cudaGetLastError();
+  return err;
 }
 
 ColstreamPlan plan_gemv_colstream(int R, int K, int sms) {
@@ -527,20 +531,14 @@ cudaError_t launch_gemv_colstream(const GemvArgs& g, const ColstreamPlan& cp, vo
                                   unsigned* counters, cudaStream_t s) {
   float* part = static_cast<float*>(ws);
   const dim3 grid(cp.panels, cp.ksplit);
-  if (g.in_f16)
-    gemv_colstream_kernel<true><<<grid, kColThreads, 0, s>>>(g, cp, part, counters);
-  else
-    gemv_colstream_kernel<false><<<grid, kColThreads, 0, s>>>(g, cp, part, counters);
-  return cudaGetLastError();
+  auto kern = g.in_f16 ? gemv_colstream_kernel<true> : gemv_colstream_kernel<false>;
+  return launch_k(kern, grid, dim3(kColThreads), 0, s, g.pdl != 0, g, cp, part, counters);
 }
 
 cudaError_t launch_gemv_generic(const GemvArgs& g, cudaStream_t s, int sms) {
   const int grid = grid_for(g.R, 8, sms, 8);
-  if (g.in_f16)
-    gemv_generic_kernel<true><<<grid, 256, 0, s>>>(g);
-  else
-    gemv_generic_kernel<false><<<grid, 256, 0, s>>>(g);
-  return cudaGetLastError();
+  auto kern = g.in_f16 ? gemv_generic_kernel<true> : gemv_generic_kernel<false>;
+  return launch_k(kern, dim3(grid), dim3(256), 0, s, g.pdl != 0, g);
 }
 
 cudaError_t launch_tile_reduce(const TileReduceArgs& a, cudaStream_t s, int sms) {

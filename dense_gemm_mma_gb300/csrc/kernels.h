@@ -91,6 +91,7 @@ struct TcParams {
   int act;
   int* err;          // plan error word
   uint64_t timeout_ns;
+  int pdl;           // launch as a programmatic dependent of the stream's previous kernel
 };
 
 // Shared-memory footprint and ring depth of the tensor-core kernel for a tile
@@ -112,6 +113,32 @@ cudaError_t launch_gemm_tc(int bn, int mode, const CUtensorMap& a, const CUtenso
 
 
 #ifdef __CUDACC__
+// Programmatic dependent launch: a kernel launched with the programmatic
+// stream-serialization attribute may be scheduled before the previous kernel
+// in its stream has finished (once that kernel's CTAs have all started and
+// signalled, or exited), so its launch and prologue overlap that kernel's
+// tail.  It must call wait_prior_grid() before it reads or writes global
+// memory: that returns once the previous kernel has completed and its writes
+// are visible.  In a kernel launched normally it returns at once.
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// kern<<<grid, block, smem, s>>>(args...), as a programmatic dependent if pdl.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Output transform (gemm_act_t), in fp32: 1 LeakyReLU, 2 ReLU, 3 GELU
 // (x * Phi(x), Phi through erfc so the negative tail keeps its relative
 // accuracy), 4 SiLU; anything else is the identity.
@@ -176,6 +203,7 @@ struct GemvArgs {
   int64_t inc_cin;
   int in_f16;
   EpiParams e;
+  int pdl;  // launch as a programmatic dependent of the stream's previous kernel
 };
 
 int gemv_rowdot_max_k();

@@ -33,6 +33,15 @@
  * The plan owns its workspace (split-K partials, GEMV partials, the watchdog
  * word) and frees it in gemm_plan_destroy.  One plan must not be used by two
  * host threads, or on two streams whose work may overlap, at the same time.
+ * The GEMM and GEMV kernels launch as programmatic dependents of the previous
+ * kernel on the stream (CUDA programmatic dependent launch): their launch
+ * and setup may overlap that kernel's last moments, but they touch no memory
+ * before it has completed, so stream order holds as for a plain launch.  The
+ * GEMM kernel lets its own dependents start early; a caller's kernel launched
+ * after a gemm_run with the programmatic stream-serialization attribute must
+ * therefore call cudaGridDependencySynchronize() (griddepcontrol.wait) before
+ * it reads the result, as that attribute requires.  Set GEMM_PDL=0 in the
+ * environment before gemm_plan_create for plain launches.
  *
  * Errors: argument problems are reported synchronously, before anything is
  * launched, as a gemm_status_t; nothing aborts or throws across this ABI.
