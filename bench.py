@@ -414,9 +414,11 @@ def main():
     n = len(calls)
     infos = [None] * n
 
-    def one_step(events=None):
+    def one_step(events=None, flush_each=False):
         launches = 0
         for i, c in enumerate(calls):
+            if flush_each:
+                flush_l2()
             if events is not None:
                 events[i][0].record(stream)
             info = launch(c, devbuf[c.name])
@@ -437,8 +439,21 @@ def main():
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-           for _ in range(n)] for _ in range(args.steps)]
+    # A workload whose calls read buffers no other call touches is timed a step
+    # at a time (one event pair around its calls, which run back to back as a
+    # user's would); the calls of a sweep share A and B, so each is timed on
+    # its own with L2 flushed before it.
+    sweep = any(c.group for c in calls)
+    new_ev = lambda: torch.cuda.Event(enable_timing=True)
+    ev = [[[new_ev(), new_ev()] for _ in range(n)] for _ in range(args.steps)]
+    step_ev = [[new_ev(), new_ev()] for _ in range(args.steps)]
+
+    def restore_c():
+        # beta != 0 calls update C in place: restore it outside the timed events
+        for c in calls:
+            if devbuf[c.name]["C0"] is not None:
+                devbuf[c.name]["C"].copy_(devbuf[c.name]["C0"])
+
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
@@ -446,23 +461,36 @@ def main():
     gpu_launches = 0
     for s in range(args.steps):
         flush_l2()
-        # beta != 0 calls update C in place: restore it outside the timed events
-        for c in calls:
-            if devbuf[c.name]["C0"] is not None:
-                devbuf[c.name]["C"].copy_(devbuf[c.name]["C0"])
-        gpu_launches += one_step(ev[s])
+        restore_c()
+        if sweep:
+            gpu_launches += one_step(ev[s], flush_each=True)
+        else:
+            step_ev[s][0].record(stream)
+            gpu_launches += one_step()
+            step_ev[s][1].record(stream)
     torch.cuda.synchronize(dev)
     t_end = time.time()
     if dist is not None:
         dist.barrier()
+    if sweep:
+        call_ms = np.array([[ev[s][i][0].elapsed_time(ev[s][i][1]) for i in range(n)]
+                            for s in range(args.steps)])
+        step_ms = call_ms.sum(axis=1)
+    else:
+        step_ms = np.array([step_ev[s][0].elapsed_time(step_ev[s][1]) for s in range(args.steps)])
+        # Per-call breakdown (parts, roofline): the same steps again, each call
+        # between its own events.
+        for s in range(args.steps):
+            flush_l2()
+            restore_c()
+            one_step(ev[s])
+        torch.cuda.synchronize(dev)
+        call_ms = np.array([[ev[s][i][0].elapsed_time(ev[s][i][1]) for i in range(n)]
+                            for s in range(args.steps)])
     time.sleep(0.3)
     sampler.stop()
     if plan.poll_error() != gemm.GEMM_OK:
         raise RuntimeError("watchdog fired during the timed region")
-
-    call_ms = np.array([[ev[s][i][0].elapsed_time(ev[s][i][1]) for i in range(n)]
-                        for s in range(args.steps)])
-    step_ms = call_ms.sum(axis=1)
     total_ms = max_over_ranks(float(step_ms.sum()), dist, dev)
     step_bytes = sum(c.bytes for c in calls)
     step_flops = sum(c.flops for c in calls)
@@ -528,10 +556,14 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": calls[0].in_fmt, "data": "synthetic",
             "config": {"workload": wl_name, "calls": [c.desc() for c in calls],
                        "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                       "l2": "flushed between steps (512 MiB read, untimed); each call reads "
-                             "device buffers no other call of the step touches"
-                             + ("" if not any(c.group for c in calls) else
-                                " (except the calls of one sweep, which share A and B)"),
+                       "l2": ("flushed before every call (512 MiB read, untimed); the calls of a sweep "
+                              "share A and B" if sweep else
+                              "flushed between steps (512 MiB read, untimed); each call reads "
+                              "device buffers no other call of the step touches"),
+                       "timing": ("each call between its own CUDA events; ms_per_step is their sum" if sweep
+                                  else "one CUDA event pair around each step's calls, which run back "
+                                       "to back; parts and roofline from a second pass with events "
+                                       "around each call"),
                        "planner": "benchmark mode (timed once per shape in warm-up)" if args.autotune
                                   else "cost model",
                        "step_bytes": step_bytes, "step_flops": step_flops,
