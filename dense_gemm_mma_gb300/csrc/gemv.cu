@@ -13,6 +13,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 
 #include "kernels.h"
@@ -27,6 +28,7 @@ constexpr int kRowdotMaxK = 32768;  // x staged in shared memory: 64 KB of 16-bi
 constexpr int kColThreads = 256;
 constexpr int kColGroups = 4;             // K-interleaved thread groups per CTA
 constexpr int kColCols = 8 * (kColThreads / kColGroups);  // 512 columns per CTA
+static_assert(kColCols / 4 * 2 == kColThreads, "the last-CTA reduction gives each half of the threads one column quad");
 constexpr int kColMaxKc = 2048;           // rows of x staged in shared memory at a time
 
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
@@ -487,6 +489,33 @@ int grid_for(int64_t items, int per_block, int sms, int blocks_per_sm) {
   return g < 1 ? 1 : static_cast<int>(g);
 }
 
+// Grid of a kernel whose warps take rows r, r + (warps in the grid), ...:
+// one wave, every warp the same number of rows (within one).  A CTA that has
+// to wait for a slot runs its rows after the others have finished, at a
+// fraction of the bandwidth: in a 1 x 8192 x 8192 row-dot GEMV a second wave
+// of 11% of the CTAs took 40% of the time.  `occ` caches the resident CTAs
+// per SM of the kernel as smem << 16 | count (one word, so that threads see a
+// matching pair).
+template <typename Kern>
+int one_wave_grid(Kern kern, std::atomic<int64_t>& occ, int threads, int smem, int64_t rows, int sms) {
+  int64_t c = occ.load(std::memory_order_relaxed);
+  if (c < 0 || (c >> 16) != smem) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = 1;
+    }
+    c = (static_cast<int64_t>(smem) << 16) | n;
+    occ.store(c, std::memory_order_relaxed);
+  }
+  const int wpb = threads / 32;
+  const int64_t resident_warps = static_cast<int64_t>(sms) * static_cast<int>(c & 0xffff) * wpb;
+  const int64_t rows_per_warp = (rows + resident_warps - 1) / resident_warps;
+  const int64_t warps = (rows + rows_per_warp - 1) / rows_per_warp;
+  const int64_t grid = (warps + wpb - 1) / wpb;
+  return grid < 1 ? 1 : static_cast<int>(grid);
+}
+
 }  // namespace
 
 int gemv_rowdot_max_k() { return kRowdotMaxK; }
@@ -494,10 +523,11 @@ int gemv_rowdot_max_k() { return kRowdotMaxK; }
 cudaError_t launch_gemv_rowdot(const GemvArgs& g, cudaStream_t s, int sms) {
   const bool direct = g.incx == 1 && (reinterpret_cast<uintptr_t>(g.x) & 15u) == 0;
   const int smem = direct ? 0 : ((g.K + 7) & ~7) * 2;
-  const int grid = grid_for(g.R, kRowdotThreads / 32, sms, 8);
   cudaError_t err = cudaSuccess;
   auto go = [&](auto kern) {
     if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    static std::atomic<int64_t> occ{-1};
+    const int grid = one_wave_grid(kern, occ, kRowdotThreads, smem, g.R, sms);
     err = launch_k(kern, dim3(grid), dim3(kRowdotThreads), smem, s, g.pdl != 0, g);
   };
   if (g.in_f16) {
@@ -510,6 +540,7 @@ cudaError_t launch_gemv_rowdot(const GemvArgs& g, cudaStream_t s, int sms) {
 
 ColstreamPlan plan_gemv_colstream(int R, int K, int sms) {
   ColstreamPlan cp;
+  cp.cols = kColCols;
   cp.panels = (R + kColCols - 1) / kColCols;
   const int target = sms * 4;  // four 256-thread CTAs per SM, each with 8 rows in flight per thread
   int ksplit = (target + cp.panels - 1) / cp.panels;
@@ -536,8 +567,9 @@ cudaError_t launch_gemv_colstream(const GemvArgs& g, const ColstreamPlan& cp, vo
 }
 
 cudaError_t launch_gemv_generic(const GemvArgs& g, cudaStream_t s, int sms) {
-  const int grid = grid_for(g.R, 8, sms, 8);
   auto kern = g.in_f16 ? gemv_generic_kernel<true> : gemv_generic_kernel<false>;
+  static std::atomic<int64_t> occ[2] = {{-1}, {-1}};
+  const int grid = one_wave_grid(kern, occ[g.in_f16 ? 1 : 0], 256, 0, g.R, sms);
   return launch_k(kern, dim3(grid), dim3(256), 0, s, g.pdl != 0, g);
 }
 

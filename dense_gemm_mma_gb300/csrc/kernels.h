@@ -211,10 +211,11 @@ cudaError_t launch_gemv_rowdot(const GemvArgs& g, cudaStream_t s, int sms);
 
 // Plan of the column-stream kernel: `ksplit` K slices of `kc` rows each.
 struct ColstreamPlan {
-  int panels;  // ceil(R / 512)
+  int cols;    // columns per CTA (panel width)
+  int panels;  // ceil(R / cols)
   int ksplit;
   int kc;
-  int64_t ws_bytes;  // fp32 partials, ksplit x panels x 512 (0 when ksplit == 1)
+  int64_t ws_bytes;  // fp32 partials, ksplit x panels x cols (0 when ksplit == 1)
 };
 ColstreamPlan plan_gemv_colstream(int R, int K, int sms);
 // counters: `panels` words that are zero on entry and are left zero on exit.

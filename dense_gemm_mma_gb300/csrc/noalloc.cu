@@ -33,7 +33,6 @@
 
 namespace {
 
-constexpr int kColCols = 512;                      // columns per CTA of the column-stream kernel
 constexpr int kMaxPanels = 4096;                   // => N (or M) <= 2,097,152
 constexpr size_t kScratchBytes = size_t(4) << 20;  // 4 MiB per device
 constexpr size_t kCounterBytes = size_t(kMaxPanels) * sizeof(unsigned);
@@ -130,7 +129,7 @@ extern "C" gemm_status_t gemm_gemv_noalloc(int64_t M, int64_t N, int64_t K, cons
 
   dg::ColstreamPlan cp = dg::plan_gemv_colstream(g.R, g.K, sms);
   if (cp.panels > kMaxPanels) return GEMM_ERR_UNSUPPORTED;  // R beyond the fixed scratch
-  const int64_t per_split = int64_t(cp.panels) * kColCols;
+  const int64_t per_split = int64_t(cp.panels) * cp.cols;
   const int64_t max_split = int64_t(kPartialFloats) / per_split;
   if (cp.ksplit > 1 && max_split < 2) {
     cp.ksplit = 1;  // no room for two slices: one slice, no partials

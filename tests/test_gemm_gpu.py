@@ -474,6 +474,84 @@ def test_cuda_graph_capture_and_replay(plan):
     assert plan.poll_error() == gemm.GEMM_OK
 
 
+def _check_link(got_bits, A, B, M, N, K, lda, ldb, out_fmt, tb=False, what=""):
+    """One call's output against the oracle on the inputs it should have seen."""
+    import oracle
+    from tests.gemm_case import decode, ulp
+    exact, rounded = oracle.gemm(M, N, K, A, B, lda=lda, ldb=ldb, in_fmt="bf16", out_fmt=out_fmt,
+                                 transB=tb)
+    amax = float(np.abs(decode(A, "bf16")).max())
+    bmax = float(np.abs(decode(B, "bf16")).max())
+    tol = 1e-5 * K * amax * bmax + 2.0 ** -21 * np.abs(exact) + ulp(exact, out_fmt)
+    err = np.abs(decode(got_bits, out_fmt) - decode(rounded, out_fmt))
+    assert (err <= tol).all(), f"{what}: {int((~(err <= tol)).sum())} outputs off"
+
+
+def test_back_to_back_calls_keep_stream_order(plan):
+    """Calls enqueued back to back with no synchronisation between them (the
+    kernels launch as programmatic dependents of their predecessor): a chain
+    in which every call reads the previous call's output, across the K-pair,
+    one-CTA tile, split-K and both GEMV kernels, sees finished inputs; and a
+    call that overwrites a matrix the previous call is still streaming does
+    not disturb that call.  Each output is checked against the oracle on the
+    inputs it should have read."""
+    torch = pytest.importorskip("torch")
+    from dense_gemm_mma_gb300 import gemm, inputs
+    from tests.gemm_case import from_device, to_device
+    s = torch.cuda.current_stream().cuda_stream
+    BF32 = gemm.DTYPES[("bf16", "f32")]
+    BB = gemm.DTYPES[("bf16", "bf16")]
+    torch.cuda.synchronize()
+    # read after write: X0 -> X1 -> X2 -> X3 -> y -> z
+    links = [  # (M, N, K, out) of each link; the input is the previous output
+        (1024, 256, 2048, "bf16"), (1024, 1024, 256, "bf16"), (1024, 128, 1024, "bf16"),
+        (1, 4096, 128, "bf16"), (1, 2048, 4096, "f32")]
+    X0 = inputs.matrix(1024, 2048, 61, inputs.TENSOR_A, "bf16")
+    Ws = [inputs.matrix(K, N, 62 + i, inputs.TENSOR_B, "bf16") if i < 4 else
+          inputs.matrix(N, K, 62 + i, inputs.TENSOR_B, "bf16")  # the last B is given transposed
+          for i, (M, N, K, _) in enumerate(links)]
+    dev_in = to_device(X0, "bf16")
+    dev_w = [to_device(W, "bf16") for W in Ws]
+    outs, paths = [], []
+    for i, (M, N, K, fmt) in enumerate(links):
+        out = torch.empty((M, N), device="cuda", dtype=torch.float32 if fmt == "f32" else torch.bfloat16)
+        tb = i == 4
+        st = gemm.gemm_run(plan.handle, M, N, K, dev_in.data_ptr(), dev_in.shape[1] if dev_in.dim() == 2 else K,
+                           dev_w[i].data_ptr(), K if tb else N, out.data_ptr(), N, 1.0, 0.0,
+                           BF32 if fmt == "f32" else BB, 0, int(tb), 0, 0.0, s)
+        assert st == gemm.GEMM_OK
+        paths.append(plan.last_config()["path"])
+        outs.append(out)
+        # the next link reads this output (its first row only, for the GEMVs)
+        dev_in = out[:1] if i == 2 else out
+    # write after read: P @ Q streams P while the next call writes its result into P
+    P = inputs.matrix(8192, 1024, 71, inputs.TENSOR_A, "bf16")
+    Q = inputs.matrix(1024, 128, 72, inputs.TENSOR_B, "bf16")
+    R = inputs.matrix(8192, 64, 73, inputs.TENSOR_A, "bf16")
+    T = inputs.matrix(64, 1024, 74, inputs.TENSOR_B, "bf16")
+    Pd, Qd, Rd, Td = (to_device(X, "bf16") for X in (P, Q, R, T))
+    Y = torch.empty((8192, 128), device="cuda", dtype=torch.float32)
+    assert gemm.gemm_run(plan.handle, 8192, 128, 1024, Pd.data_ptr(), 1024, Qd.data_ptr(), 128,
+                         Y.data_ptr(), 128, 1.0, 0.0, BF32, 0, 0, 0, 0.0, s) == gemm.GEMM_OK
+    paths.append(plan.last_config()["path"])
+    assert gemm.gemm_run(plan.handle, 8192, 1024, 64, Rd.data_ptr(), 64, Td.data_ptr(), 1024,
+                         Pd.data_ptr(), 1024, 1.0, 0.0, BB, 0, 0, 0, 0.0, s) == gemm.GEMM_OK
+    paths.append(plan.last_config()["path"])
+    torch.cuda.synchronize()
+    assert plan.poll_error() == gemm.GEMM_OK
+    assert "tc_splitk_cluster" in paths and "gemv_colstream" in paths and "gemv_rowdot" in paths, paths
+
+    host_in = X0
+    for i, (M, N, K, fmt) in enumerate(links):
+        got = from_device(outs[i], fmt)
+        A = host_in if i != 3 else host_in[:1]
+        _check_link(got, A, Ws[i], M, N, K, A.shape[1], Ws[i].shape[1], fmt, tb=(i == 4),
+                    what=f"link {i} ({paths[i]})")
+        host_in = got
+    _check_link(from_device(Y, "f32"), P, Q, 8192, 128, 1024, 1024, 128, "f32", what=f"P @ Q ({paths[5]})")
+    _check_link(from_device(Pd, "bf16"), R, T, 8192, 1024, 64, 64, 1024, "bf16", what=f"R @ T into P ({paths[6]})")
+
+
 # ----------------------------------------------------------- benchmark mode
 
 def test_autotune_benchmark_mode():
