@@ -272,7 +272,7 @@ double estimate(int64_t M, int64_t N, int64_t K, int bn, int mode, int splitk, i
                        std::max(0.0, 1.0 - unique / (double(units) * (pair ? 2 : 1) * unit_bytes));
   const double feed = md.feed * (1.0 + md.reuse_gain * reuse);
   const double makespan = waves * std::max(t_mma, unit_bytes / feed) + md.fixed +
-                          (pair ? kPairFixed : 0.0) + (kpair ? kKPairRound * (bn / 128) : 0.0);
+                          (pair ? kPairFixed : 0.0) + (kpair ? kKPairRound * (bn / 128) * waves : 0.0);
   double bytes = unique + double(M) * N * c_es * (beta ? 2.0 : 1.0);
   double t = 0.0;
   if (s_eff > 1 && !kpair) {
@@ -389,9 +389,19 @@ void tc_candidates(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta
     if (force_bn && (c.bn != force_bn || (c.mode == dg::TC_PAIR) != force_pair)) continue;
     if (kpair ? kpair_env == 0 : kpair_env == 1) continue;
     if (kpair && (only_tail || (c.bn == 256 && force_bn != 256))) continue;
-    // A K pair pays its exchange on every tile; it measured faster only where
-    // the tiles fit one wave of clusters (then it replaces a reduction launch).
-    if (kpair && kpair_env != 1 && ceil_div(M, dg::TC_BM) * ceil_div(N, c.bn) > sms / 2) continue;
+    // A K pair pays its exchange on every tile.  Where its tiles take more
+    // than one wave of clusters it measured faster only when the best other
+    // choice needs more than one wave as well (27648 x 128 x 4096: 45.7
+    // against 53.9 us); against a one-wave choice it lost by up to 32%.
+    if (kpair && kpair_env != 1 && ceil_div(M, dg::TC_BM) * ceil_div(N, c.bn) > sms / 2) {
+      bool pick_multi_wave = pick.tail || pick.t >= 1e300;  // (or nothing else was possible)
+      if (!pick_multi_wave) {
+        const int p_tm = pick.mode == dg::TC_PAIR ? 2 * dg::TC_BM : dg::TC_BM;
+        const int p_slots = pick.mode == dg::TC_PAIR ? sms / 2 : sms;
+        pick_multi_wave = ceil_div(M, p_tm) * ceil_div(N, pick.bn) * pick.s > p_slots;
+      }
+      if (!pick_multi_wave) continue;
+    }
     const int tile_m = c.mode == dg::TC_PAIR ? 2 * dg::TC_BM : dg::TC_BM;
     const int slots = c.mode == dg::TC_PAIR ? sms / 2 : sms;
     if (c.mode != dg::TC_SOLO && sms < 2) continue;
