@@ -468,25 +468,20 @@ def main():
             step_ev[s][0].record(stream)
             gpu_launches += one_step()
             step_ev[s][1].record(stream)
+            # the per-call breakdown (parts, roofline): the same step again,
+            # each call between its own events, right after the timed step so
+            # that both see the same clocks and power state
+            flush_l2()
+            restore_c()
+            gpu_launches += one_step(ev[s])
     torch.cuda.synchronize(dev)
     t_end = time.time()
     if dist is not None:
         dist.barrier()
-    if sweep:
-        call_ms = np.array([[ev[s][i][0].elapsed_time(ev[s][i][1]) for i in range(n)]
-                            for s in range(args.steps)])
-        step_ms = call_ms.sum(axis=1)
-    else:
-        step_ms = np.array([step_ev[s][0].elapsed_time(step_ev[s][1]) for s in range(args.steps)])
-        # Per-call breakdown (parts, roofline): the same steps again, each call
-        # between its own events.
-        for s in range(args.steps):
-            flush_l2()
-            restore_c()
-            one_step(ev[s])
-        torch.cuda.synchronize(dev)
-        call_ms = np.array([[ev[s][i][0].elapsed_time(ev[s][i][1]) for i in range(n)]
-                            for s in range(args.steps)])
+    call_ms = np.array([[ev[s][i][0].elapsed_time(ev[s][i][1]) for i in range(n)]
+                        for s in range(args.steps)])
+    step_ms = call_ms.sum(axis=1) if sweep else \
+        np.array([step_ev[s][0].elapsed_time(step_ev[s][1]) for s in range(args.steps)])
     time.sleep(0.3)
     sampler.stop()
     if plan.poll_error() != gemm.GEMM_OK:
@@ -562,8 +557,8 @@ def main():
                               "device buffers no other call of the step touches"),
                        "timing": ("each call between its own CUDA events; ms_per_step is their sum" if sweep
                                   else "one CUDA event pair around each step's calls, which run back "
-                                       "to back; parts and roofline from a second pass with events "
-                                       "around each call"),
+                                       "to back; every timed step is followed by the same step with "
+                                       "events around each call, for parts and roofline"),
                        "planner": "benchmark mode (timed once per shape in warm-up)" if args.autotune
                                   else "cost model",
                        "step_bytes": step_bytes, "step_flops": step_flops,

@@ -797,6 +797,7 @@ gemm_status_t launch_entry(gemm_plan* plan, TcEntry* e, int64_t M, int64_t N, vo
     r.Cin = e->p.cin;
     r.ldcin = e->p.ldcin;
     r.e = dg::EpiParams{alpha, beta, epi.slope, epi.act, out_kind(dtype), e->p.cin_kind};
+    r.pdl = plan->pdl;
     if (dg::launch_tile_reduce(r, s, plan->sms) != cudaSuccess) return GEMM_ERR_CUDA;
   }
   return GEMM_OK;

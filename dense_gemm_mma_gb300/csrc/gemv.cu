@@ -509,7 +509,7 @@ int grid_for(int64_t items, int per_block, int sms, int blocks_per_sm) {
 // per SM of the kernel as smem << 16 | count (one word, so that threads see a
 // matching pair).
 template <typename Kern>
-int one_wave_grid(Kern kern, std::atomic<int64_t>& occ, int threads, int smem, int64_t rows, int sms) {
+int resident_per_sm(Kern kern, std::atomic<int64_t>& occ, int threads, int smem) {
   int64_t c = occ.load(std::memory_order_relaxed);
   if (c < 0 || (c >> 16) != smem) {
     int n = 0;
@@ -520,8 +520,13 @@ int one_wave_grid(Kern kern, std::atomic<int64_t>& occ, int threads, int smem, i
     c = (static_cast<int64_t>(smem) << 16) | n;
     occ.store(c, std::memory_order_relaxed);
   }
+  return static_cast<int>(c & 0xffff);
+}
+
+template <typename Kern>
+int one_wave_grid(Kern kern, std::atomic<int64_t>& occ, int threads, int smem, int64_t rows, int sms) {
   const int wpb = threads / 32;
-  const int64_t resident_warps = static_cast<int64_t>(sms) * static_cast<int>(c & 0xffff) * wpb;
+  const int64_t resident_warps = static_cast<int64_t>(sms) * resident_per_sm(kern, occ, threads, smem) * wpb;
   const int64_t rows_per_warp = (rows + resident_warps - 1) / resident_warps;
   const int64_t warps = (rows + rows_per_warp - 1) / rows_per_warp;
   const int64_t grid = (warps + wpb - 1) / wpb;
@@ -590,8 +595,11 @@ cudaError_t launch_tile_reduce(const TileReduceArgs& a, cudaStream_t s, int sms)
   const int64_t items = static_cast<int64_t>(a.tail_tiles) * a.tile_m * (a.tile_n / 4);
   // Programmatic dependent launch: the reduction's launch overlaps the tail of
   // the GEMM; its griddepcontrol.wait orders it after the GEMM's writes.
+  // (a grid-stride kernel: no more CTAs than are resident at once, so none
+  // waits for a slot and runs its share after the others)
+  static std::atomic<int64_t> occ{-1};
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid_for(items, 256, sms, 8));
+  cfg.gridDim = dim3(grid_for(items, 256, sms, resident_per_sm(tile_reduce_kernel, occ, 256, 0)));
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
@@ -599,9 +607,7 @@ cudaError_t launch_tile_reduce(const TileReduceArgs& a, cudaStream_t s, int sms)
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (const char* v = std::getenv("GEMM_PDL"))  // GEMM_PDL=0: ordinary launch, for comparison
-    if (v[0] == '0') cfg.numAttrs = 0;
+  cfg.numAttrs = a.pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, tile_reduce_kernel, a);
 }
 
@@ -618,7 +624,9 @@ cudaError_t launch_transpose32(const void* in, int64_t ld_in, int rows, int cols
 cudaError_t launch_scale(int M, int N, void* D, int64_t ldd, const void* C, int64_t ldc, EpiParams e,
                          cudaStream_t s, int sms) {
   const int64_t items = static_cast<int64_t>(M) * N;
-  scale_kernel<<<grid_for(items, 256, sms, 8), 256, 0, s>>>(M, N, D, ldd, C, ldc, e);
+  static std::atomic<int64_t> occ{-1};
+  scale_kernel<<<grid_for(items, 256, sms, resident_per_sm(scale_kernel, occ, 256, 0)), 256, 0, s>>>(
+      M, N, D, ldd, C, ldc, e);
   return cudaGetLastError();
 }
 

@@ -174,6 +174,7 @@ struct TileReduceArgs {
   const void* Cin;  // the C that beta scales (may be the output)
   int64_t ldcin;
   EpiParams e;
+  int pdl;  // launch as a programmatic dependent of the GEMM that writes the partials
 };
 cudaError_t launch_tile_reduce(const TileReduceArgs& a, cudaStream_t s, int sms);
 

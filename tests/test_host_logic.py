@@ -306,6 +306,35 @@ def test_planner_kpair_switch(monkeypatch):
     assert c.path in (1, 2) and c.splitk == 1
 
 
+def test_planner_kpair_over_several_waves():
+    """A K pair whose tiles take more than one wave of clusters is chosen only
+    where the best other choice needs more than one wave too: the three
+    shapes where it measured faster on GB300 take it, shapes where a one-wave
+    tile measured faster keep that tile."""
+    for shape in [(27648, 128, 4096), (1024, 2048, 1024), (2048, 1024, 1024)]:
+        c = g.gemm_choose_config(*shape, 0, 0, 0, 152)
+        assert g.PATH_NAMES[c.path] == "tc_splitk_cluster", shape
+        assert c.tiles > 76 and c.waves > 1.0
+    for shape in [(1536, 1536, 1536), (1280, 1280, 1280), (4096, 512, 4096), (2048, 1024, 4096),
+                  (1024, 4096, 1024), (2048, 2048, 1024)]:
+        c = g.gemm_choose_config(*shape, 0, 0, 0, 152)
+        assert g.PATH_NAMES[c.path] == "tc" and c.waves <= 1.0, (shape, c.as_dict())
+
+
+def test_gemv_colstream_grid_is_one_wave():
+    """The column-stream GEMV's K split never asks for more CTAs than four per
+    SM: a split rounded up left a few CTAs to run alone in a second wave
+    (1 x 5000 x 8192: 610 CTAs for 608 slots)."""
+    for sms in (152, 148, 132):
+        for n in (5000, 8192, 3000, 16384, 777, 4096 + 512, 40000):
+            for k in (8192, 4096, 1000):
+                c = g.gemm_choose_config(1, n, k, 0, 0, 0, sms)
+                assert g.PATH_NAMES[c.path] == "gemv_colstream"
+                panels = -(-n // 512)
+                assert c.grid <= max(4 * sms, panels), (sms, n, k, c.grid)
+                assert c.grid == panels * c.splitk
+
+
 def test_planner_tail_split(monkeypatch):
     """Config 5's second-wave shapes: 2304 x 2176 x 4096 has 81 tiles of
     256 x 256 for 76 CTA pairs, so 5 tiles would run alone in a second wave;
