@@ -26,10 +26,10 @@ namespace {
 constexpr int kRowdotThreads = 256;
 constexpr int kRowdotCtasPerSm = 8;
 constexpr int kRowdotMaxK = 32768;  // x staged in shared memory: 64 KB of 16-bit values
-constexpr int kColThreads = 384;  // 48 warps per SM at four CTAs per SM
-constexpr int kColGroups = 6;             // K-interleaved thread groups per CTA
+constexpr int kColThreads = 512;  // 64 warps per SM at four CTAs per SM
+constexpr int kColGroups = 8;             // K-interleaved thread groups per CTA
 constexpr int kColCols = 8 * (kColThreads / kColGroups);  // 512 columns per CTA
-constexpr int kColMaxKc = 1536;           // rows of x staged in shared memory at a time
+constexpr int kColMaxKc = 2048;           // rows of x staged in shared memory at a time
 static_assert(kColThreads % (kColCols / 4) == 0, "the last-CTA reduction gives every thread one column quad");
 static_assert(kColMaxKc % kColGroups == 0, "a chunk of x keeps every row with its group");
 
@@ -163,17 +163,18 @@ __global__ void __launch_bounds__(kRowdotThreads, kRowdotCtasPerSm)
 
 // --------------------------------------------------------------- colstream
 // W is K x R with R contiguous.  CTA (panel, z) covers columns
-// [panel*512, panel*512+512) and K rows [z*kc, z*kc+kc); its 384 threads form
-// 6 groups of 64, each thread owning 8 adjacent columns (one 16-byte load per
-// row, kColU rows in flight) and every 6th row of the slice; the slice of x is
+// [panel*512, panel*512+512) and K rows [z*kc, z*kc+kc); its 512 threads form
+// 8 groups of 64, each thread owning 8 adjacent columns (one 16-byte load per
+// row, kColU rows in flight) and every 8th row of the slice; the slice of x is
 // staged in shared memory as fp32.  The groups are summed in shared memory in
 // a fixed order.  With ksplit > 1 each CTA writes its 512 partial sums to the
 // workspace; the CTA that finishes a panel last (per-panel arrival counter,
-// zero on entry) sums the slices -- three fixed ranges in slice order, then the
-// ranges -- applies the epilogue and sets the counter back to zero.  (384
-// threads rather than 256: the same four CTAs per SM then keep 48 warps of
-// loads in flight, 29.3 instead of 30.1-31.3 us for 1 x 8192 x 8192.)
-constexpr int kColU = 8;
+// zero on entry) sums the slices -- four fixed ranges in slice order, then the
+// ranges -- applies the epilogue and sets the counter back to zero.  Four CTAs
+// of 512 threads at 32 registers fill an SM with 64 warps of loads for the
+// same K split as 256-thread CTAs: 1 x 8192 x 8192 29.3 us (30.1-31.3 with
+// 256 threads), 1 x 4096 x 4096 15.0 us (17.0 with 384).
+constexpr int kColU = 4;
 
 template <bool F16>
 __device__ __forceinline__ void fma_row(float (&acc)[8], uint4 wv, float xf) {
@@ -187,7 +188,7 @@ __device__ __forceinline__ void fma_row(float (&acc)[8], uint4 wv, float xf) {
 }
 
 template <bool F16>
-__global__ void __launch_bounds__(kColThreads)
+__global__ void __launch_bounds__(kColThreads, 4)
     gemv_colstream_kernel(const GemvArgs g, const ColstreamPlan cp, float* ws, unsigned* counters) {
   wait_prior_grid();
   __shared__ float red[kColGroups][kColCols];
@@ -559,7 +560,7 @@ ColstreamPlan plan_gemv_colstream(int R, int K, int sms) {
   ColstreamPlan cp;
   cp.cols = kColCols;
   cp.panels = (R + kColCols - 1) / kColCols;
-  const int target = sms * 4;  // four CTAs per SM, each thread with 8 rows in flight
+  const int target = sms * 4;  // four CTAs per SM, each thread with kColU rows in flight
   // at most `target` CTAs: more would leave a few of them for a second wave
   int ksplit = target / cp.panels;
   const int max_split = (K + 63) / 64;  // at least 64 rows (16 per thread) per slice

@@ -474,6 +474,30 @@ def test_cuda_graph_capture_and_replay(plan):
     assert plan.poll_error() == gemm.GEMM_OK
 
 
+def test_plain_launches_without_programmatic_dependence(monkeypatch):
+    """A plan created with GEMM_PDL=0 launches every kernel plainly (no
+    programmatic stream serialization); each path still matches the oracle."""
+    torch = pytest.importorskip("torch")
+    from dense_gemm_mma_gb300 import gemm
+    monkeypatch.setenv("GEMM_PDL", "0")
+    p = gemm.Plan(0)
+    try:
+        cases = [((1024, 1024, 1024), {}, "tc_splitk_cluster"),
+                 ((2304, 2176, 4096), {}, "tc_tail_split"),
+                 ((256, 256, 8192), {"GEMM_FORCE_SPLITK": "8", "GEMM_SPLITK_CLUSTER": "0"}, "tc_splitk"),
+                 ((300, 520, 200), {}, None),
+                 ((1, 4096, 2048), {}, "gemv_colstream")]
+        for (M, N, K), env, path in cases:
+            r = run_case(p, M, N, K, env=env, sample=2048 if M * N > 2_000_000 else None,
+                         in_fmt="f16" if M == 2304 else "bf16")
+            if path:
+                assert r.info["path"] == path, (M, N, K, r.info["path"])
+        r = run_case(p, 1, 4096, 2048, tb=True)
+        assert r.info["path"] == "gemv_rowdot"
+    finally:
+        p.close()
+
+
 def _check_link(got_bits, A, B, M, N, K, lda, ldb, out_fmt, tb=False, what=""):
     """One call's output against the oracle on the inputs it should have seen."""
     import oracle
