@@ -704,6 +704,82 @@ def test_gemv_deterministic(plan):
     assert all(np.array_equal(r.outputs[0], o) for o in r.outputs[1:])
 
 
+# ------------------------------------------------ offsets past 2^31 and 2^32
+
+@pytest.mark.parametrize("case", ["tc_a", "tc_c", "gemv_colstream", "gemv_rowdot"])
+def test_operands_spanning_8_gib(plan, case):
+    """Leading dimensions of 65536 (or 32768 for fp32 C) put the last rows of
+    an operand 8 GiB past its base, so every address of the path needs more
+    than 32 bits, while the matrices hold only a few MB of data: sampled
+    outputs against the oracle on compact host copies, and sentinels in the
+    padding that the call must not touch."""
+    torch = pytest.importorskip("torch")
+    from dense_gemm_mma_gb300 import gemm, inputs
+    from tests.gemm_case import decode, sample_positions, ulp
+    import oracle
+    BIG = 65536
+    # (M, N, K, transB, which operand is padded, its leading dimension)
+    M, N, K, tb, padded, ld = {"tc_a": (BIG, 128, 64, False, "A", BIG),
+                               "tc_c": (BIG, 64, 64, False, "C", BIG // 2),
+                               "gemv_colstream": (1, 64, BIG, False, "B", BIG),
+                               "gemv_rowdot": (1, BIG, 64, True, "B", BIG)}[case]
+    A = inputs.matrix(M, K, 101, inputs.TENSOR_A, "bf16")
+    B = inputs.matrix(N, K, 102, inputs.TENSOR_B, "bf16") if tb else inputs.matrix(K, N, 102, inputs.TENSOR_B, "bf16")
+
+    def place(host, ld_big, dtype, fill):
+        rows, cols = host.shape
+        full = torch.full((rows * ld_big,), fill, dtype=dtype, device="cuda")
+        view = full.view(rows, ld_big)[:, :cols]
+        src = torch.from_numpy(host.view(np.int16) if host.dtype == np.uint16 else host)
+        view.copy_(src.view(dtype).cuda() if host.dtype == np.uint16 else src.cuda())
+        return full, view
+
+    bf = torch.bfloat16
+    nan = float("nan")
+    big = {}  # the 8 GiB buffers, freed at the end
+    if padded == "A":
+        big["A"], Ad = place(A, ld, bf, nan)
+        Bd = torch.from_numpy(B.view(np.int16)).view(bf).cuda()
+        lda, ldb = ld, B.shape[1]
+    else:
+        Ad = torch.from_numpy(A.view(np.int16)).view(bf).cuda()
+        lda = K
+        if padded == "B":
+            big["B"], Bd = place(B, ld, bf, nan)
+            ldb = ld
+        else:
+            Bd = torch.from_numpy(B.view(np.int16)).view(bf).cuda()
+            ldb = B.shape[1]
+    if padded == "C":
+        big["C"], Cd = place(np.zeros((M, N), np.float32), ld, torch.float32, nan)
+        ldc = ld
+    else:
+        Cd = torch.full((M, N), nan, dtype=torch.float32, device="cuda")
+        ldc = N
+    st = gemm.gemm_run(plan.handle, M, N, K, Ad.data_ptr(), lda, Bd.data_ptr(), ldb, Cd.data_ptr(), ldc,
+                       1.0, 0.0, gemm.DTYPES[("bf16", "f32")], 0, int(tb), 0, 0.0,
+                       torch.cuda.current_stream().cuda_stream)
+    assert st == gemm.GEMM_OK
+    torch.cuda.synchronize()
+    assert plan.poll_error() == gemm.GEMM_OK
+    path = plan.last_config()["path"]
+    assert path == ("tc" if case.startswith("tc") else case), path
+    rows, cols = sample_positions(M, N, 4096, seed=7)
+    got = Cd.cpu().numpy()[rows, cols].astype(np.float64)
+    exact, rounded = oracle.sample(rows, cols, K, A, B, lda=K, ldb=B.shape[1], in_fmt="bf16", out_fmt="f32",
+                                   transB=tb)
+    amax = float(np.abs(decode(A, "bf16")).max())
+    bmax = float(np.abs(decode(B, "bf16")).max())
+    tol = 1e-5 * K * amax * bmax + 2.0 ** -21 * np.abs(exact) + ulp(exact, "f32")
+    assert (np.abs(got - decode(rounded, "f32")) <= tol).all(), case
+    if padded == "C":  # padding of C's rows, including the far end, still holds its sentinel
+        pad = big["C"].view(M, ld)[[0, M // 2, M - 1], N:N + 64].cpu().numpy()
+        assert np.isnan(pad).all()
+    del Ad, Bd, Cd
+    big.clear()
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------- full-size workloads
 
 SAMPLE = 4096
