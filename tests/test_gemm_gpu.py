@@ -706,11 +706,12 @@ def test_gemv_deterministic(plan):
 
 # ------------------------------------------------ offsets past 2^31 and 2^32
 
-@pytest.mark.parametrize("case", ["tc_a", "tc_c", "gemv_colstream", "gemv_rowdot"])
+@pytest.mark.parametrize("case", ["tc_a", "tc_c", "kpair_a", "pair_a", "gemv_colstream", "gemv_rowdot"])
 def test_operands_spanning_8_gib(plan, case):
-    """Leading dimensions of 65536 (or 32768 for fp32 C) put the last rows of
-    an operand 8 GiB past its base, so every address of the path needs more
-    than 32 bits, while the matrices hold only a few MB of data: sampled
+    """Leading dimensions of 65536 (or 32768 for fp32 C; 262144 for the K
+    pair's A, 4 GiB) put the last rows of an operand 8 GiB past its base, so
+    every address of the path needs more than 32 bits, while the matrices
+    hold little data: sampled
     outputs against the oracle on compact host copies, and sentinels in the
     padding that the call must not touch."""
     torch = pytest.importorskip("torch")
@@ -718,11 +719,16 @@ def test_operands_spanning_8_gib(plan, case):
     from tests.gemm_case import decode, sample_positions, ulp
     import oracle
     BIG = 65536
-    # (M, N, K, transB, which operand is padded, its leading dimension)
-    M, N, K, tb, padded, ld = {"tc_a": (BIG, 128, 64, False, "A", BIG),
-                               "tc_c": (BIG, 64, 64, False, "C", BIG // 2),
-                               "gemv_colstream": (1, 64, BIG, False, "B", BIG),
-                               "gemv_rowdot": (1, BIG, 64, True, "B", BIG)}[case]
+    # (M, N, K, transB, which operand is padded, its leading dimension, planner switches, path)
+    M, N, K, tb, padded, ld, env, want = {
+        "tc_a": (BIG, 128, 64, False, "A", BIG, {}, "tc"),
+        "tc_c": (BIG, 64, 64, False, "C", BIG // 2, {}, "tc"),
+        "kpair_a": (8192, 128, 8192, False, "A", 4 * BIG, {}, "tc_splitk_cluster"),   # 4 GiB
+        "pair_a": (BIG, 256, 64, False, "A", BIG, {"GEMM_FORCE_TILE": "256x256"}, "tc"),
+        "gemv_colstream": (1, 64, BIG, False, "B", BIG, {}, "gemv_colstream"),
+        "gemv_rowdot": (1, BIG, 64, True, "B", BIG, {}, "gemv_rowdot")}[case]
+    for k, v in env.items():
+        os.environ[k] = v
     A = inputs.matrix(M, K, 101, inputs.TENSOR_A, "bf16")
     B = inputs.matrix(N, K, 102, inputs.TENSOR_B, "bf16") if tb else inputs.matrix(K, N, 102, inputs.TENSOR_B, "bf16")
 
@@ -756,14 +762,20 @@ def test_operands_spanning_8_gib(plan, case):
     else:
         Cd = torch.full((M, N), nan, dtype=torch.float32, device="cuda")
         ldc = N
-    st = gemm.gemm_run(plan.handle, M, N, K, Ad.data_ptr(), lda, Bd.data_ptr(), ldb, Cd.data_ptr(), ldc,
-                       1.0, 0.0, gemm.DTYPES[("bf16", "f32")], 0, int(tb), 0, 0.0,
-                       torch.cuda.current_stream().cuda_stream)
+    try:
+        st = gemm.gemm_run(plan.handle, M, N, K, Ad.data_ptr(), lda, Bd.data_ptr(), ldb, Cd.data_ptr(), ldc,
+                           1.0, 0.0, gemm.DTYPES[("bf16", "f32")], 0, int(tb), 0, 0.0,
+                           torch.cuda.current_stream().cuda_stream)
+    finally:
+        for k in env:
+            os.environ.pop(k, None)
     assert st == gemm.GEMM_OK
     torch.cuda.synchronize()
     assert plan.poll_error() == gemm.GEMM_OK
-    path = plan.last_config()["path"]
-    assert path == ("tc" if case.startswith("tc") else case), path
+    info = plan.last_config()
+    assert info["path"] == want, info["path"]
+    if case == "pair_a":
+        assert info["cta_per_tile"] == 2
     rows, cols = sample_positions(M, N, 4096, seed=7)
     got = Cd.cpu().numpy()[rows, cols].astype(np.float64)
     exact, rounded = oracle.sample(rows, cols, K, A, B, lda=K, ldb=B.shape[1], in_fmt="bf16", out_fmt="f32",
