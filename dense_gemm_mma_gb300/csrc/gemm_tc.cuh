@@ -53,6 +53,8 @@
 //    two-slice reduction kernel's.
 #pragma once
 
+#include <atomic>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -852,8 +854,17 @@ cudaError_t launch_gemm_tc_bn(const CUtensorMap& a, const CUtensorMap& b, const 
                               const CUtensorMap& ws, const TcParams& p, int grid, cudaStream_t s) {
   constexpr int smem = TcCfg<BN, MODE>::SMEM_BYTES;
   auto kern = gemm_tc_kernel<BN, MODE, TF32>;
-  cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (err != cudaSuccess) return err;
+  // The shared-memory limit is set once per device (bit d of `ready`), not on
+  // every launch: it is host time in front of every call.
+  static std::atomic<uint64_t> ready{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaGetLastError();
+  const uint64_t bit = dev < 64 ? uint64_t(1) << dev : 0;
+  if (bit == 0 || (ready.load(std::memory_order_acquire) & bit) == 0) {
+    const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    ready.fetch_or(bit, std::memory_order_release);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(TC_THREADS);
