@@ -498,6 +498,51 @@ def test_plain_launches_without_programmatic_dependence(monkeypatch):
         p.close()
 
 
+@pytest.mark.parametrize("first,second", [((8192, 128, 2048), (8192, 128, 64)),     # K pair -> tile
+                                          ((1, 4096, 2048), (1, 4096, 512)),        # GEMV -> GEMV
+                                          ((2304, 2176, 512), (2304, 2176, 4096))])  # pair tile -> tail split
+def test_back_to_back_beta_reads_the_previous_output(plan, first, second):
+    """A call that reads C (beta = 1) right after the call that wrote it, with
+    no synchronisation between them: its result matches the oracle applied to
+    the first call's output (the first call is deterministic, so running it
+    again alone gives the bits the second call must have read)."""
+    torch = pytest.importorskip("torch")
+    from dense_gemm_mma_gb300 import gemm, inputs
+    from tests.gemm_case import decode, from_device, to_device, ulp
+    import oracle
+    s = torch.cuda.current_stream().cuda_stream
+    BF32 = gemm.DTYPES[("bf16", "f32")]
+    (M, N, K1), (_, _, K2) = first, second
+    A1 = inputs.matrix(M, K1, 131, inputs.TENSOR_A, "bf16")
+    B1 = inputs.matrix(K1, N, 132, inputs.TENSOR_B, "bf16")
+    A2 = inputs.matrix(M, K2, 133, inputs.TENSOR_A, "bf16")
+    B2 = inputs.matrix(K2, N, 134, inputs.TENSOR_B, "bf16")
+    A1d, B1d, A2d, B2d = (to_device(X, "bf16") for X in (A1, B1, A2, B2))
+    C = torch.full((M, N), float("nan"), device="cuda")
+
+    def run(A, B, K, Cd, beta):
+        assert gemm.gemm_run(plan.handle, M, N, K, A.data_ptr(), K, B.data_ptr(), N, Cd.data_ptr(), N,
+                             1.0, beta, BF32, 0, 0, 0, 0.0, s) == gemm.GEMM_OK
+        return plan.last_config()["path"]
+
+    torch.cuda.synchronize()
+    p1 = run(A1d, B1d, K1, C, 0.0)
+    p2 = run(A2d, B2d, K2, C, 1.0)
+    torch.cuda.synchronize()
+    second_out = from_device(C, "f32")
+    X = torch.full((M, N), float("nan"), device="cuda")
+    run(A1d, B1d, K1, X, 0.0)
+    torch.cuda.synchronize()
+    assert plan.poll_error() == gemm.GEMM_OK
+    first_out = from_device(X, "f32")
+    exact, rounded = oracle.gemm(M, N, K2, A2, B2, C=first_out.copy(), alpha=1.0, beta=1.0,
+                                 in_fmt="bf16", out_fmt="f32")
+    amax, bmax = float(np.abs(decode(A2, "bf16")).max()), float(np.abs(decode(B2, "bf16")).max())
+    tol = 1e-5 * K2 * amax * bmax + 2.0 ** -21 * (np.abs(exact) + np.abs(first_out)) + ulp(exact, "f32")
+    err = np.abs(second_out.astype(np.float64) - decode(rounded, "f32"))
+    assert (err <= tol).all(), (p1, p2, int((~(err <= tol)).sum()))
+
+
 def _check_link(got_bits, A, B, M, N, K, lda, ldb, out_fmt, tb=False, what=""):
     """One call's output against the oracle on the inputs it should have seen."""
     import oracle
