@@ -635,7 +635,7 @@ gemm_status_t run_gemv(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const v
   info->launches = 1;
   if (row_major_w && (vec_ok || g.R == 1) && aligned(g.W, 16) && K <= dg::gemv_rowdot_max_k()) {
     info->path = GEMM_PATH_GEMV_ROWDOT;
-    err = dg::launch_gemv_rowdot(g, s, plan->sms);
+    err = dg::launch_gemv_rowdot(g, s, plan->sms, &info->grid);
   } else if (!row_major_w && (vec_ok || K == 1) && aligned(g.W, 16)) {
     const dg::ColstreamPlan cp = dg::plan_gemv_colstream(g.R, g.K, plan->sms);
     if (cp.ws_bytes > 0) {
@@ -649,7 +649,7 @@ gemm_status_t run_gemv(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const v
     info->workspace_bytes = cp.ws_bytes;
     err = dg::launch_gemv_colstream(g, cp, plan->ws, plan->counters, s);
   } else {
-    err = dg::launch_gemv_generic(g, s, plan->sms);
+    err = dg::launch_gemv_generic(g, s, plan->sms, &info->grid);
   }
   return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }

@@ -538,7 +538,7 @@ int one_wave_grid(Kern kern, std::atomic<int64_t>& occ, int threads, int smem, i
 
 int gemv_rowdot_max_k() { return kRowdotMaxK; }
 
-cudaError_t launch_gemv_rowdot(const GemvArgs& g, cudaStream_t s, int sms) {
+cudaError_t launch_gemv_rowdot(const GemvArgs& g, cudaStream_t s, int sms, int* grid_out) {
   const bool direct = g.incx == 1 && (reinterpret_cast<uintptr_t>(g.x) & 15u) == 0;
   const int smem = direct ? 0 : ((g.K + 7) & ~7) * 2;
   cudaError_t err = cudaSuccess;
@@ -546,6 +546,7 @@ cudaError_t launch_gemv_rowdot(const GemvArgs& g, cudaStream_t s, int sms) {
     if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     static std::atomic<int64_t> occ{-1};
     const int grid = one_wave_grid(kern, occ, kRowdotThreads, smem, g.R, sms);
+    if (grid_out) *grid_out = grid;
     err = launch_k(kern, dim3(grid), dim3(kRowdotThreads), smem, s, g.pdl != 0, g);
   };
   if (g.in_f16) {
@@ -585,10 +586,11 @@ cudaError_t launch_gemv_colstream(const GemvArgs& g, const ColstreamPlan& cp, vo
   return launch_k(kern, grid, dim3(kColThreads), 0, s, g.pdl != 0, g, cp, part, counters);
 }
 
-cudaError_t launch_gemv_generic(const GemvArgs& g, cudaStream_t s, int sms) {
+cudaError_t launch_gemv_generic(const GemvArgs& g, cudaStream_t s, int sms, int* grid_out) {
   auto kern = g.in_f16 ? gemv_generic_kernel<true> : gemv_generic_kernel<false>;
   static std::atomic<int64_t> occ[2] = {{-1}, {-1}};
   const int grid = one_wave_grid(kern, occ[g.in_f16 ? 1 : 0], 256, 0, g.R, sms);
+  if (grid_out) *grid_out = grid;
   return launch_k(kern, dim3(grid), dim3(256), 0, s, g.pdl != 0, g);
 }
 

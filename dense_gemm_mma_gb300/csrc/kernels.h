@@ -208,7 +208,8 @@ struct GemvArgs {
 };
 
 int gemv_rowdot_max_k();
-cudaError_t launch_gemv_rowdot(const GemvArgs& g, cudaStream_t s, int sms);
+// grid_out (optional): the CTAs launched (one wave, sized from the occupancy query).
+cudaError_t launch_gemv_rowdot(const GemvArgs& g, cudaStream_t s, int sms, int* grid_out = nullptr);
 
 // Plan of the column-stream kernel: `ksplit` K slices of `kc` rows each.
 struct ColstreamPlan {
@@ -223,7 +224,7 @@ ColstreamPlan plan_gemv_colstream(int R, int K, int sms);
 cudaError_t launch_gemv_colstream(const GemvArgs& g, const ColstreamPlan& cp, void* ws,
                                   unsigned* counters, cudaStream_t s);
 
-cudaError_t launch_gemv_generic(const GemvArgs& g, cudaStream_t s, int sms);
+cudaError_t launch_gemv_generic(const GemvArgs& g, cudaStream_t s, int sms, int* grid_out = nullptr);
 
 // One CTA waits on a barrier that nothing arrives on; gives up after timeout_ns.
 cudaError_t launch_watchdog_selftest(int* err, uint64_t timeout_ns, cudaStream_t s);

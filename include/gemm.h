@@ -11,10 +11,11 @@
  * Bounds); every output is a K-long dot product, 2*M*N*K floating-point
  * operations in all.  The guide's display formula for GEMM is lost in the
  * extracted text: the BLAS form above is the reading taken.  act is the
- * identity or LeakyReLU, the fused output transform motivated by "OpenAI
- * open-sources the Triton GPU language (part 2)", section Matrix
- * multiplication.  Operands are bf16 or fp16, products are accumulated in
- * fp32, C is fp32 or the operand type.
+ * identity, LeakyReLU (the fused output transform of "OpenAI open-sources the
+ * Triton GPU language (part 2)", section Matrix multiplication), ReLU, GELU
+ * or SiLU.  Operands are bf16, fp16 or TF32 (fp32 words), products are
+ * accumulated in fp32, C is fp32 or the operand type (gemm_run_ex: a separate
+ * D, and a C of its own type).
  *
  * Storage is row-major ("Learning Triton One Kernel at a Time: Matrix
  * Multiplication", section Memory coalescing: a row is contiguous, a
@@ -134,7 +135,9 @@ typedef struct {
   int32_t splitk;          /* K slices (1 = none)                                      */
   int32_t stages;          /* shared-memory pipeline depth                             */
   int32_t raster_group;    /* output-tile rows per rasterisation group                 */
-  int32_t grid;            /* CTAs launched for the main kernel                        */
+  int32_t grid;            /* CTAs launched for the main kernel (gemm_choose_config:  */
+                           /* 0 for the row-dot and generic GEMVs, whose grid comes   */
+                           /* from the device's occupancy at launch)                  */
   int32_t sms;             /* streaming multiprocessors used for the wave size         */
   int64_t tiles;           /* output tiles = ceil(M/tile_m) * ceil(N/tile_n)           */
   int64_t units;           /* work units = tiles - tail_tiles + tail_tiles * splitk    */

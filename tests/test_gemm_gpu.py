@@ -715,6 +715,11 @@ def test_plan_cache_survives_workspace_growth(plan):
 def test_gemv_m1_config(plan, tb):
     r = run_case(plan, 1, 8192, 8192, tb=tb, seed=1235)
     assert r.info["path"] == ("gemv_rowdot" if tb else "gemv_colstream")
+    # one wave: at most the CTAs that fit at once (row dot: eight per SM, one row per warp)
+    sms = r.info["sms"]
+    assert 0 < r.info["grid"] <= (8 if tb else 4) * sms
+    if tb:
+        assert r.info["grid"] == 8192 // 8
 
 
 @pytest.mark.parametrize("ta", [False, True])
