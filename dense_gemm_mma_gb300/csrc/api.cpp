@@ -124,6 +124,56 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // ------------------------------------------------------------- validation
 
+// Floor division for a positive divisor.
+int64_t floor_div(int64_t a, int64_t b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
+// A row-major matrix as memory: `rows` rows of `width` bytes, `pitch` bytes
+// apart, the first at byte address `base`.
+struct Region {
+  uint64_t base;
+  int64_t rows, pitch, width;
+};
+
+Region region(const void* p, int64_t rows, int64_t cols, int64_t ld, int64_t esize) {
+  return Region{uint64_t(reinterpret_cast<uintptr_t>(p)), rows, ld * esize, cols * esize};
+}
+
+// Do two matrices share a byte?  Row i of x and row k of y meet iff y's row
+// starts before x's ends and ends after x's starts: -wy < d + k*Ly - i*Lx < wx
+// with d = by - bx.  Exact in O(1) for equal pitches (row-interleaved slices
+// of one parent, or a single row), where only t = k - i matters; with
+// different pitches the rows of the shorter matrix are tested one by one, and
+// past 2^20 such rows overlapping byte spans count as overlap.
+bool overlaps(Region x, Region y) {
+  if (x.rows <= 0 || y.rows <= 0 || x.width <= 0 || y.width <= 0) return false;
+  const uint64_t xe = x.base + uint64_t(x.rows - 1) * uint64_t(x.pitch) + uint64_t(x.width);
+  const uint64_t ye = y.base + uint64_t(y.rows - 1) * uint64_t(y.pitch) + uint64_t(y.width);
+  if (xe <= y.base || ye <= x.base) return false;  // disjoint spans
+  if (x.rows == 1) x.pitch = y.pitch;  // a single row fits any pitch
+  if (y.rows == 1) y.pitch = x.pitch;
+  if (x.pitch == y.pitch) {
+    const int64_t L = x.pitch;
+    const int64_t d = int64_t(y.base - x.base);  // the spans overlap: |d| < 2^63
+    // integers t in the open interval ((-wy - d) / L, (wx - d) / L), and
+    // t = k - i in [1 - rows_x, rows_y - 1] (each such t has a valid i, k)
+    const int64_t lo = std::max<int64_t>(floor_div(-y.width - d, L) + 1, 1 - x.rows);
+    const int64_t hi = std::min<int64_t>(-floor_div(d - x.width, L) - 1, y.rows - 1);
+    return lo <= hi;
+  }
+  if (x.rows > y.rows) std::swap(x, y);
+  if (x.rows > (int64_t(1) << 20)) return true;
+  const int64_t d = int64_t(y.base - x.base);
+  for (int64_t i = 0; i < x.rows; ++i) {
+    // row i of x covers [s, s + wx) relative to y.base; rows k of y with
+    // k*Ly < s + wx and k*Ly + wy > s
+    const int64_t s = int64_t(i) * x.pitch - d;
+    const int64_t k_lo = std::max<int64_t>(floor_div(s - y.width, y.pitch) + 1, 0);
+    const int64_t k_hi = std::min<int64_t>(floor_div(s + x.width - 1, y.pitch), y.rows - 1);
+    if (k_lo <= k_hi) return true;
+  }
+  return false;
+}
+
 gemm_status_t check(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, const void* B,
                     int64_t ldb, const void* C, int64_t ldc, float alpha, gemm_dtype_t dtype,
                     gemm_op_t ta, gemm_op_t tb, gemm_epilogue_t epi) {
@@ -143,8 +193,14 @@ gemm_status_t check(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   const bool reads_ab = K > 0 && alpha != 0.f;
   if (reads_ab && (A == nullptr || B == nullptr)) return GEMM_ERR_INVALID_ARG;
   const size_t ces = out_is_f32(dtype) ? 4 : 2;
-  if (!aligned(C, ces)) return GEMM_ERR_ALIGNMENT;
   const int ies = in_bytes(dtype);
+  if (reads_ab) {  // C is written while A and B are read: they must not share a byte
+    const Region rc = region(C, M, N, ldc, int64_t(ces));
+    const Region ra = ta == GEMM_OP_N ? region(A, M, K, lda, ies) : region(A, K, M, lda, ies);
+    const Region rb = tb == GEMM_OP_N ? region(B, K, N, ldb, ies) : region(B, N, K, ldb, ies);
+    if (overlaps(rc, ra) || overlaps(rc, rb)) return GEMM_ERR_INVALID_ARG;
+  }
+  if (!aligned(C, ces)) return GEMM_ERR_ALIGNMENT;
   if (reads_ab && (!aligned(A, ies) || !aligned(B, ies))) return GEMM_ERR_ALIGNMENT;
   if (in_is_tf32(dtype)) {  // always the tensor-core path
     if (reads_ab && (!aligned(A, 16) || !aligned(B, 16) || (lda * 4) % 16 || (ldb * 4) % 16))
@@ -1020,10 +1076,9 @@ gemm_status_t check_ex(int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   const size_t c_es = c_type == GEMM_TYPE_F32 ? 4 : 2, d_es = f32 ? 4 : 2;
   if (!aligned(C, c_es)) return GEMM_ERR_ALIGNMENT;
   if (C == D) return ldc == ldd && c_type == d_type ? GEMM_OK : GEMM_ERR_INVALID_ARG;
-  const uintptr_t c0 = reinterpret_cast<uintptr_t>(C), d0 = reinterpret_cast<uintptr_t>(D);
-  const uintptr_t c1 = c0 + (uintptr_t(M - 1) * uintptr_t(ldc) + uintptr_t(N)) * c_es;
-  const uintptr_t d1 = d0 + (uintptr_t(M - 1) * uintptr_t(ldd) + uintptr_t(N)) * d_es;
-  if (c0 < d1 && d0 < c1) return GEMM_ERR_INVALID_ARG;  // a separate C must not overlap D
+  // a separate C must not share a byte with D (it may overlap A or B: all three are only read)
+  if (overlaps(region(C, M, N, ldc, int64_t(c_es)), region(D, M, N, ldd, int64_t(d_es))))
+    return GEMM_ERR_INVALID_ARG;
   return GEMM_OK;
 }
 

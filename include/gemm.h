@@ -177,7 +177,12 @@ gemm_status_t gemm_plan_create(gemm_plan_t* plan, int device);
  *  - M, N, K >= 0 and each < 2^31; lda >= stored columns of A (K for N, M
  *    for T), ldb >= stored columns of B (N for N, K for T), ldc >= N; all >= 1.
  *  - A and B may be NULL only if M*N == 0 or K == 0 or alpha == 0; C may be
- *    NULL only if M*N == 0.  C must not overlap A or B.
+ *    NULL only if M*N == 0.
+ *  - When A and B are read (M*N > 0, K > 0, alpha != 0), no byte of C (its
+ *    M rows of N elements, ldc apart) may lie in A or B (their stored rows,
+ *    lda / ldb apart).  Slices of one parent whose rows interleave without
+ *    sharing a byte are accepted; with different leading dimensions and more
+ *    than 2^20 rows on both sides, overlapping address ranges are rejected.
  *  - Every pointer is aligned to its element size.
  *  - Tensor-core path (M >= 2 and N >= 2): A, B and C are 16-byte aligned and
  *    lda, ldb, ldc times the element size are multiples of 16 bytes -- the
@@ -227,7 +232,8 @@ typedef enum { GEMM_TYPE_BF16 = 0, GEMM_TYPE_F16 = 1, GEMM_TYPE_F32 = 2,
  *            stride ldc >= N), read only when beta != 0 (it may then be NULL
  *            and ldc is ignored); it needs only its element alignment.  C may
  *            be D itself (same pointer, ldc == ldd, c_type == d_type: that is
- *            gemm_run); otherwise the two must not overlap.
+ *            gemm_run); otherwise the two must not share a byte.  C may
+ *            overlap A or B (all three are only read); D may not.
  * Violations return GEMM_ERR_INVALID_ARG or GEMM_ERR_ALIGNMENT before any
  * launch.  Paths, workspace, streams and errors as in gemm_run; the plan's
  * last configuration is updated the same way.  The pages fuse input and

@@ -70,7 +70,7 @@ def test_no_device_without_gpu():
 
 # -------------------------------------------------------------- argument checks
 
-A16, B16, C16 = 0x10000, 0x20000, 0x30000   # fake, 16-byte aligned addresses (never dereferenced)
+A16, B16, C16 = 1 << 32, 2 << 32, 3 << 32   # fake, 16-byte aligned, 4 GiB apart (never dereferenced)
 
 
 def chk(M, N, K, A=A16, lda=None, B=B16, ldb=None, C=C16, ldc=None, alpha=1.0, dtype=0,
@@ -111,6 +111,51 @@ def test_check_args_ex_separate_c():
     assert ex(c=D, c_type=TF) == E and ex(c=D, c_type=T16, ldc=72) == E
     assert ex(c=D + 64 * 64) == E                            # overlaps D (D spans 64*64*2 bytes)
     assert ex(c=D + 64 * 64 * 2) == OK                       # right after D
+
+
+def test_check_args_rejects_output_overlapping_operands():
+    """C is written while A and B are read: a C that shares a byte with A or B
+    is rejected before any launch (gemm_run), and so is a D of gemm_run_ex that
+    shares one with A or B.  Slices of one parent whose rows interleave without
+    sharing a byte are accepted."""
+    E, OK = g.GEMM_ERR_INVALID_ARG, g.GEMM_OK
+    M, N, K = 64, 32, 128                      # A 64 x 128 bf16 (16 KiB), B 128 x 32 (8 KiB), C fp32 8 KiB
+    a_bytes, b_bytes = M * K * 2, K * N * 2
+    assert chk(M, N, K) == OK
+    assert chk(M, N, K, C=A16 + 4096) == E                     # C inside A
+    assert chk(M, N, K, C=B16 + 1024) == E                     # C inside B
+    assert chk(M, N, K, C=A16 + a_bytes - 16) == E             # C straddles the end of A
+    assert chk(M, N, K, C=A16 - 16) == E                       # C's last row runs into A's first
+    assert chk(M, N, K, C=A16 + a_bytes) == OK                 # right after A
+    assert chk(M, N, K, C=B16 - M * N * 4) == OK               # right before B
+    for ta in (0, 1):                                          # stored K x M when transposed
+        for tb in (0, 1):
+            assert chk(M, N, K, ta=ta, tb=tb) == OK
+            assert chk(M, N, K, ta=ta, tb=tb, C=A16 + a_bytes // 2) == E
+            assert chk(M, N, K, ta=ta, tb=tb, C=B16 + b_bytes // 2) == E
+            assert chk(M, N, K, ta=ta, tb=tb, C=A16 + a_bytes) == OK
+    # A and C as column slices of one parent with 256 fp32-sized... (bf16 parent,
+    # ld 512 elements = 1 KiB rows): A in bytes [0, 256) of every row, C (bf16 out)
+    # in bytes [512, 576): rows interleave, no byte is shared
+    P, ld = A16, 512
+    assert chk(M, N, K, A=P, lda=ld, C=P + 512, ldc=ld, dtype=1) == OK
+    assert chk(M, N, K, A=P, lda=ld, C=P + 240, ldc=ld, dtype=1) == E      # C's rows start inside A's
+    assert chk(M, N, K, A=P, lda=ld, C=P + 1024 - 64, ldc=ld, dtype=1) == OK  # ends where A's next row starts
+    assert chk(M, N, K, A=P, lda=ld, C=P + 1024 - 62, ldc=ld, dtype=1) == E   # ... two bytes into it
+    # different leading dimensions: C's rows (ld 64 bf16 = 128 B) walk across A's (1 KiB apart)
+    assert chk(M, N, K, A=P, lda=ld, C=P + 256, ldc=64, dtype=1) == E
+    assert chk(2, N, K, A=P, lda=ld, C=P + 256, ldc=64, dtype=1) == OK       # two C rows in A's gap
+    # nothing of A or B is read: no rule (K == 0, alpha == 0)
+    assert chk(M, N, 0, C=A16) == OK
+    assert chk(M, N, K, C=A16, alpha=0.0) == OK
+    # gemm_run_ex: D against A and B
+    T16, TF = g.GEMM_TYPE_BF16, g.GEMM_TYPE_F32
+
+    def ex(d, c=None, beta=0.0):
+        return g.gemm_check_args_ex(M, N, K, A16, K, B16, N, c, N, TF, d, N, TF, 1.0, beta, T16, 0, 0)
+    assert ex(C16) == OK
+    assert ex(A16 + 1024) == E and ex(B16 + 1024) == E
+    assert ex(C16, c=A16, beta=1.0) == OK     # a separate C may overlap A: both are only read
 
 
 def test_check_args_rejects():
