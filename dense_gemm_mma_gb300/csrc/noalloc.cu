@@ -12,9 +12,14 @@
 // allocates, and a plan grows its workspace on demand.
 //
 // The scratch (arrival counters + fp32 partial sums of the K slices) is one
-// file-scope __device__ array of kScratchBytes.  Every GPU that loads this
-// library holds that array until the process exits.  All calls on a device
-// share it and it keeps the last call's contents, so:
+// file-scope __device__ array of kScratchBytes.  CUDA loads a library's
+// device code lazily, per device: this file's module, and with it the array,
+// is loaded on a device by the first call there (cudaGetSymbolAddress), which
+// takes the 4 MiB from that device's free memory and keeps it until the
+// process exits.  A caller whose pool allocator reserves the device's memory
+// should therefore make one call on each device before the pool takes the
+// rest; later calls allocate nothing.  All calls on a device share the array
+// and it keeps the last call's contents, so:
 //  - each call zeroes the counters it uses (cudaMemsetAsync on its stream)
 //    before the kernel, since the kernel needs them at zero on entry;
 //  - calls whose kernels may overlap on the GPU (different streams without
@@ -23,7 +28,8 @@
 // On the first call on a device the entry point looks the array's device
 // address up with cudaGetSymbolAddress (host code cannot use the symbol
 // itself: on the host it names a stand-in, not device memory).  That first
-// call should come before any stream capture.
+// call should come before any stream capture.  If the device has no room left
+// for the array at that point, the call returns GEMM_ERR_OUT_OF_MEMORY.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -59,9 +65,10 @@ gemm_status_t device_setup(int dev, void** addr, int* sms) {
       return GEMM_ERR_NO_DEVICE;
     }
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+    const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // loads the module here
+    if (err != cudaSuccess || p == nullptr) {
       cudaGetLastError();
-      return GEMM_ERR_CUDA;
+      return err == cudaErrorMemoryAllocation ? GEMM_ERR_OUT_OF_MEMORY : GEMM_ERR_CUDA;
     }
     g_sms[dev] = count;
     g_scratch_addr[dev] = p;

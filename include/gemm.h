@@ -338,11 +338,14 @@ gemm_status_t gemm_quantization(int64_t M, int64_t N, int32_t tile_m, int32_t ti
  * those of gemm_run.
  *
  * Runs on the calling thread's current device; `stream` must belong to it.
- * Its scratch is a fixed 4 MiB device array of the library, held by every
- * GPU that loads the library until the process exits; the call zeroes the
- * part that must start at zero.  The first call on a device looks up that
- * array's address (cudaGetSymbolAddress) and should come before any stream
- * capture.  All calls on a device share the array: calls whose kernels may
+ * Its scratch is a fixed 4 MiB device array of the library; the call zeroes
+ * the part that must start at zero.  CUDA loads the library's device code
+ * lazily: the first call on a device looks up that array's address
+ * (cudaGetSymbolAddress), which loads it there and takes its 4 MiB from the
+ * device's free memory until the process exits (GEMM_ERR_OUT_OF_MEMORY if no
+ * room is left).  Make that first call before a pool allocator reserves the
+ * device's memory, and before any stream capture; later calls allocate
+ * nothing.  All calls on a device share the array: calls whose kernels may
  * overlap on the GPU race and must be ordered by the caller (one stream, or
  * events).  No cudaMalloc, cudaFree or other allocating call is made. */
 gemm_status_t gemm_gemv_noalloc(int64_t M, int64_t N, int64_t K,
