@@ -19,7 +19,11 @@ CUDA events on the stream it is launched on; the step time is the sum.
 `e2e` repeats the step through the same C ABI with the inputs copied from
 pinned host memory and the outputs copied back inside the timed region.
 `cpu_baseline` times the CPU oracle (single thread) on a bounded sample of
-the same step's outputs.  `--impl reference` times that oracle as the
+the same step's outputs.  `other_configs` (default workload only) adds, outside
+the step, each call of the other configurations -- 8192^3 bf16 -> bf16, 8192^3
+with beta = 0.5 and LeakyReLU, 6912 x 2048 x 4096 and split-K 256 x 256 x 65536
+-- timed alone between its own events with L2 flushed, in TFLOP/s and as a
+fraction of the roofline.  `--impl reference` times that oracle as the
 reference arm.  Under torchrun (N > 1) every rank runs the same workload on
 its own GPU (replicas: the path needs no exchange between GPUs).
 """
@@ -314,6 +318,10 @@ def main():
                     help="fraction of each call's outputs the cpu_baseline oracle computes")
     ap.add_argument("--ref-fraction", type=float, default=1.0 / 512)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the per-call timing of the compute-bound and split-K configurations "
+                         "that the default run adds under `other_configs`")
+    ap.add_argument("--other-reps", type=int, default=20)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--autotune", action="store_true",
                     help="benchmark mode: time the planner's leading candidates once per shape "
@@ -542,6 +550,11 @@ def main():
                "sample": f"{desc} (fraction {frac:g} of each call's outputs; {secs:.1f} s)",
                "tflops": round(sum(c.flops for c in calls) * (byts / step_bytes) / secs / 1e12, 9)}
 
+    # ---- the other configurations, each call timed alone (outside the step)
+    others = None
+    if args.workload == "skinny" and not args.no_others:
+        others = measure_others(args, plan, launch, flush_l2, stream, dev, torch, peaks, n_sms, local)
+
     clocks = sampler.summary(t_begin, t_end)
     if rank == 0:
         line = {
@@ -565,13 +578,108 @@ def main():
                        "step_tflops": round(ws * args.steps * step_flops / (total_ms / 1e3) / 1e12, 2),
                        "input_generation_s": round(gen_s, 1)},
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": gpu_launches,
-            "clocks": clocks, "parts": parts,
+            "clocks": clocks, "parts": parts, "other_configs": others,
         }
         print(json.dumps(line), flush=True)
     plan.close()
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def other_calls():
+    """The compute-bound square GEMM (both runs), the 6912 x 2048 x 4096 tile case and
+    the 256 x 256 x 65536 split-K case, on their own configurations' seeds."""
+    s2, s3, s4 = inputs.config_seed(2), inputs.config_seed(3), inputs.config_seed(4)
+    return [
+        Call("square_bf16_out", 8192, 8192, 8192, out_fmt="bf16", seed=s2),
+        Call("square_beta_leaky", 8192, 8192, 8192, out_fmt="f32", beta=0.5, act=1, slope=0.01, seed=s2),
+        Call("tile_6912x2048x4096", 6912, 2048, 4096, seed=s3),
+        Call("splitk_256x256x65536", 256, 256, 65536, in_fmt="f16", seed=s4),
+    ]
+
+
+def measure_others(args, plan, launch, flush_l2, stream, dev, torch, peaks, n_sms, gpu_index):
+    """Each call of other_calls() between its own CUDA events on the launching
+    stream, L2 flushed before every call (untimed), C restored before a beta call
+    (untimed), after three untimed warm-up calls; reports the median, TFLOP/s and
+    the fraction of the roofline against the measured peaks, with the clocks
+    sampled while these calls ran."""
+    from dense_gemm_mma_gb300 import gemm
+    torch_dt = {"bf16": torch.bfloat16, "f16": torch.float16, "f32": torch.float32}
+
+    def to_dev(arr, fmt):
+        if arr.dtype == np.uint16:
+            return torch.from_numpy(arr.view(np.int16)).view(torch_dt[fmt]).to(dev)
+        return torch.from_numpy(arr).to(dev)
+
+    t_gen = time.time()
+    calls = other_calls()
+    host_cache, bufs = {}, {}
+    for c in calls:
+        (ar, ac), (br, bc) = stored_shapes(c)
+        key = (c.M, c.N, c.K, c.in_fmt, c.seed)
+        if key not in host_cache:
+            host_cache[key] = (to_dev(inputs.matrix(ar, ac, c.seed, inputs.TENSOR_A, c.in_fmt), c.in_fmt),
+                               to_dev(inputs.matrix(br, bc, c.seed, inputs.TENSOR_B, c.in_fmt), c.in_fmt))
+        Ad, Bd = host_cache[key]
+        if c.beta != 0.0:
+            Cd = to_dev(inputs.matrix(c.M, c.N, c.seed, inputs.TENSOR_C, c.out_fmt), c.out_fmt)
+            C0 = Cd.clone()
+        else:
+            Cd, C0 = torch.empty((c.M, c.N), dtype=torch_dt[c.out_fmt], device=dev), None
+        bufs[c.name] = {"A": Ad, "B": Bd, "C": Cd, "C0": C0}
+    gen_s = time.time() - t_gen
+    reps = max(3, args.other_reps)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)] for _ in calls]
+    infos = []
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    time.sleep(0.3)
+    t0 = time.time()
+    for i, c in enumerate(calls):
+        b = bufs[c.name]
+        for _ in range(3):  # warm-up
+            flush_l2()
+            launch(c, b)
+        for r in range(reps):
+            flush_l2()
+            if b["C0"] is not None:
+                b["C"].copy_(b["C0"])
+            ev[i][r][0].record(stream)
+            info = launch(c, b)
+            ev[i][r][1].record(stream)
+        infos.append(info)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    time.sleep(0.3)
+    sampler.stop()
+    if plan.poll_error() != gemm.GEMM_OK:
+        raise RuntimeError("watchdog fired while timing the other configurations")
+    out = []
+    for i, c in enumerate(calls):
+        ms = np.array([a.elapsed_time(z) for a, z in ev[i]])
+        med = float(np.median(ms)) / 1e3
+        ai = c.flops / c.bytes
+        tpk = tensor_peak(c, peaks) * 1e12
+        att = rl.attainable(ai, tpk, peaks["hbm_gbs"] * 1e9)
+        info = infos[i].as_dict()
+        out.append({
+            **c.desc(), "us_median": round(med * 1e6, 2), "us_min": round(float(ms.min()) * 1e3, 2),
+            "us_iqr": round(float(np.subtract(*np.percentile(ms, [75, 25]))) * 1e3, 2),
+            "tflops": round(c.flops / med / 1e12, 2), "gbs": round(c.bytes / med / 1e9, 1),
+            "intensity": round(ai, 1), "bound": rl.bound(ai, tpk, peaks["hbm_gbs"] * 1e9),
+            "frac_of_roofline": round(c.flops / med / att, 3),
+            "frac_of_nominal_roofline": round(c.flops / med / rl.attainable(ai, 2.25e15, 8e12), 3),
+            "path": info["path"], "tile": f"{info['tile_m']}x{info['tile_n']}", "splitk": info["splitk"],
+            "grid": info["grid"], "waves": round(info["waves"], 3), "launches": info["launches"]})
+    del bufs, host_cache
+    torch.cuda.empty_cache()
+    return {"timing": (f"each call alone between its own CUDA events, L2 flushed before every call, "
+                       f"3 warm-up + {reps} timed calls each; median; roofline = min(measured bf16 "
+                       f"burst peak, intensity x measured copy bandwidth)"),
+            "input_generation_s": round(gen_s, 1), "calls": out, "clocks": sampler.summary(t0, t1)}
 
 
 def traffic_for(kernel_name: str):
