@@ -255,7 +255,17 @@ struct Model {
   double hbm_bw = 6.8e12;       // B/s, copy bandwidth
   double fixed = 3.0e-6;        // launch, pipeline fill and last epilogue
   double reduce = 6.0e-6;       // split-K reduction launch and tail
+  double fused = 4.5e-6;        // split-K reduced in the GEMM kernel: arrival wait and tail
+  double l2_bw = 1.0e13;        // B/s of the partials' round trip through L2 in that case
 };
+
+// GEMM_FUSED_REDUCE=0 sends every split-K reduction to the tile reduction
+// kernel (for comparisons); otherwise K slices that all run at once are
+// summed inside the GEMM kernel.
+bool fused_enabled() {
+  const char* v = std::getenv("GEMM_FUSED_REDUCE");
+  return !(v && *v && std::atoi(v) == 0);
+}
 
 double tile_efficiency(int bn) { return bn >= 256 ? 1.0 : (bn >= 128 ? 0.85 : 0.5); }
 
@@ -333,8 +343,12 @@ double estimate(int64_t M, int64_t N, int64_t K, int bn, int mode, int splitk, i
   double t = 0.0;
   if (s_eff > 1 && !kpair) {
     const double part = double(s_eff) * double(mb * tile_m) * double(N) * 4.0;
-    bytes += part;                           // partials written
-    t += md.reduce + part / md.hbm_bw;       // and read back by the reduction
+    if (units <= slots && fused_enabled()) {  // reduced in the kernel, the partials stay in L2
+      t += md.fused + 2.0 * part / md.l2_bw;
+    } else {
+      bytes += part;                          // partials written
+      t += md.reduce + part / md.hbm_bw;      // and read back by the reduction kernel
+    }
   }
   if (pair) streams *= 2;  // each CTA of a pair streams its own half of A and of B
   const double t_mem = bytes / std::min(md.stream_bw, md.panel_bw * double(streams));
@@ -376,8 +390,10 @@ double estimate_tail(int64_t M, int64_t N, int64_t K, int bn, int mode, int S, i
   const double makespan = double(W) * std::max(t_mma_full, ub_full / feed) +
                           std::max(t_mma_tail, ub_tail / feed) + md.fixed + (pair ? kPairFixed : 0.0);
   const double part = double(S) * double(T) * tile_m * bn * 4.0;
-  const double bytes = unique + double(M) * N * c_es * (beta ? 2.0 : 1.0) + part;
+  const bool fused = fused_enabled();  // the tail's slices are one per CTA: reduced in the kernel
+  const double bytes = unique + double(M) * N * c_es * (beta ? 2.0 : 1.0) + (fused ? 0.0 : part);
   const double t_mem = bytes / std::min(md.stream_bw, md.panel_bw * double(streams));
+  if (fused) return std::max(makespan, t_mem) + md.fused + 2.0 * part / md.l2_bw;
   return std::max(makespan, t_mem) + md.reduce + kTailExtra + part / md.hbm_bw;
 }
 
@@ -503,6 +519,20 @@ void tc_candidates(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta
   *best = pick;
 }
 
+// Can a call's K slices be summed inside the GEMM kernel?  Every partial unit
+// must be the last unit of its CTA (or cluster) -- the last `ncta` units are --
+// and one share of every slice must fit the CTA's idle operand ring.
+bool fused_fits(const gemm_config_info_t& info, int mode, int grid) {
+  if (info.tail_tiles <= 0 || mode == dg::TC_KPAIR || !fused_enabled()) return false;
+  const int cpu = mode == dg::TC_PAIR ? 2 : 1;
+  const int64_t ncta = grid / cpu;
+  if (int64_t(info.tail_tiles) * info.splitk > ncta) return false;
+  const int64_t parts = int64_t(info.splitk) * cpu;
+  const int64_t f = int64_t(info.tile_m) * info.tile_n / 4;
+  const int64_t share = (f + parts - 1) / parts;
+  return int64_t(info.splitk) * share * 16 <= dg::tc_ring_bytes(info.tile_n, mode);
+}
+
 // The configuration record of one choice.
 void fill_info(int64_t M, int64_t N, int64_t K, int sms, const TcChoice& c, gemm_config_info_t* out,
                int eb) {
@@ -540,8 +570,8 @@ void fill_info(int64_t M, int64_t N, int64_t K, int sms, const TcChoice& c, gemm
     out->grid = int(2 * std::min<int64_t>(out->tiles, pairs));
   else
     out->grid = int(std::min<int64_t>(out->units, sms));
-  out->launches = out->tail_tiles > 0 ? 2 : 1;
   out->workspace_bytes = int64_t(out->tail_tiles) * best_s * tile_m * c.bn * 4;
+  out->launches = out->tail_tiles > 0 && !fused_fits(*out, c.mode, out->grid) ? 2 : 1;
 }
 
 void choose_tc(int64_t M, int64_t N, int64_t K, int sms, int c_es, bool beta, gemm_config_info_t* out,
@@ -718,7 +748,7 @@ int tc_mode(const gemm_config_info_t& info) {
 
 bool planner_overridden() {
   static const char* vars[] = {"GEMM_FORCE_TILE", "GEMM_FORCE_SPLITK", "GEMM_RASTER_GROUP",
-                               "GEMM_SPLITK_CLUSTER", "GEMM_TAIL_SPLIT"};
+                               "GEMM_SPLITK_CLUSTER", "GEMM_TAIL_SPLIT", "GEMM_FUSED_REDUCE"};
   for (const char* v : vars) {
     const char* x = std::getenv(v);
     if (x && *x) return true;
@@ -803,7 +833,8 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
   // fp32 partials, tile-major: [slice][tail tile][tile_m rows][bn columns]
   e->ws_bytes = size_t(tail) * size_t(S) * size_t(tile_m) * size_t(bn) * 4;
   info->workspace_bytes = int64_t(e->ws_bytes);
-  info->launches = tail > 0 ? 2 : 1;
+  p.fused_reduce = fused_fits(*info, mode, info->grid);
+  info->launches = tail > 0 && !p.fused_reduce ? 2 : 1;
   return ok ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
@@ -822,8 +853,11 @@ gemm_status_t launch_entry(gemm_plan* plan, TcEntry* e, int64_t M, int64_t N, vo
   const int mode = tc_mode(e->info);
   const int tail = e->p.tail_tiles;  // tiles whose K slices a second launch reduces
   if (tail > 0) {
-    const gemm_status_t st = ensure_ws(plan, e->ws_bytes, s);
+    gemm_status_t st = ensure_ws(plan, e->ws_bytes, s);
+    if (st == GEMM_OK && p.fused_reduce) st = ensure_counters(plan, size_t(tail), s);
     if (st != GEMM_OK) return st;
+    p.ws = static_cast<const float*>(plan->ws);
+    p.counters = plan->counters;
     if (e->ws_ptr != plan->ws) {  // (re-)encode the partial map for the current workspace
       const int64_t rows = int64_t(e->p.splitk) * tail * e->info.tile_m;
       if (!make_map(&e->mw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, plan->ws, e->info.tile_n, rows,
@@ -835,7 +869,7 @@ gemm_status_t launch_entry(gemm_plan* plan, TcEntry* e, int64_t M, int64_t N, vo
   if (dg::launch_gemm_tc(e->info.tile_n, mode, e->ma, e->mb, e->mc, e->mw, p, e->info.grid, s) !=
       cudaSuccess)
     return GEMM_ERR_CUDA;
-  if (tail > 0) {
+  if (tail > 0 && !p.fused_reduce) {
     dg::TileReduceArgs r{};
     r.ws = static_cast<const float*>(plan->ws);
     r.tail_tiles = tail;
@@ -1202,6 +1236,9 @@ gemm_status_t gemm_plan_poll_error(gemm_plan_t plan, void* stream) {
   if (cudaMemcpy(&h, plan->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
   if (h == 0) return GEMM_OK;
   if (cudaMemset(plan->err, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
+  // A kernel that gave up may have left arrival counters above zero.
+  if (plan->counters && cudaMemset(plan->counters, 0, plan->counter_count * sizeof(unsigned)) != cudaSuccess)
+    return GEMM_ERR_CUDA;
   return GEMM_ERR_TIMEOUT;
 }
 

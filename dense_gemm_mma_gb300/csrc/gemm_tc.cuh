@@ -249,6 +249,112 @@ __device__ __forceinline__ void epi32(float (&v)[32], const TcParams& p, int csr
   }
 }
 
+// D(row, col .. col+3) <- act(alpha * acc + beta * C) for the outputs inside
+// C, with the arithmetic of the tile reduction kernel (so both give the same
+// bits); one 16- or 8-byte store when the four lie in C and are aligned.
+__device__ __forceinline__ void finish4(const TcParams& p, int row, int col, float4 acc) {
+  if (row >= p.M || col >= p.N) return;
+  float v[4] = {acc.x, acc.y, acc.z, acc.w};
+  const bool has_beta = p.beta != 0.f;
+  const float4 cv = has_beta ? load_cin4(p, row, col) : make_float4(0.f, 0.f, 0.f, 0.f);
+  const float c[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float t = p.alpha * v[j];
+    if (has_beta) t = fmaf(p.beta, c[j], t);
+    v[j] = apply_act(t, p.act, p.slope);
+  }
+  const int nn = min(4, p.N - col);
+  if (p.out_kind == OUT_F32) {
+    float* dst = static_cast<float*>(p.c_ptr) + int64_t(row) * p.ldc + col;
+    if (nn == 4 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+      *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+      for (int j = 0; j < nn; ++j) dst[j] = v[j];
+    }
+  } else {
+    uint16_t* dst = static_cast<uint16_t*>(p.c_ptr) + int64_t(row) * p.ldc + col;
+    uint16_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = p.out_kind == OUT_BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v[j]))
+                                    : __half_as_ushort(__float2half_rn(v[j]));
+    if (nn == 4 && (reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(uint32_t(o[0]) | (uint32_t(o[1]) << 16), uint32_t(o[2]) | (uint32_t(o[3]) << 16));
+    } else {
+      for (int j = 0; j < nn; ++j) dst[j] = o[j];
+    }
+  }
+}
+
+// Split-K reduced inside the GEMM kernel ("Matrix Multiplication Background
+// User's Guide", section 2.3: K slices need a final reduction), run by the
+// four epilogue warps of a CTA after the last unit it computes, a K slice of
+// tail tile `tile`, whose raw fp32 partials it has stored (TMA) into the
+// workspace.  The CTA publishes them (their stores complete, a proxy fence,
+// a release add on the tile's counter), waits until all `parts` = slices x
+// CTAs per unit have done so, then takes share `part` of the tile's
+// elements: one bulk load per slice brings that share of every slice into
+// its idle operand ring, and each output is summed over slices 0 .. S-1 in
+// order -- the order of the tile reduction kernel -- before the epilogue.
+// The counter goes back to zero once all parts have seen it complete.
+// `gather` counts one arrival per epilogue warp; `bar` takes the bulk loads.
+// Both are fresh (phase 0) and every wait is bounded.
+template <int TILE_M, int BN>
+static __device__ __noinline__ void fused_split_reduce(const TcParams& p, int tile, int part, int parts,
+                                                       int m_blk, int n_blk, uint32_t ring,
+                                                       const uint8_t* ring_p, uint32_t gather, uint32_t bar,
+                                                       Watch w) {
+  const int ept = int(threadIdx.x) - 2 * 32;  // 0 .. 127 over the epilogue warps
+  const int lane = int(threadIdx.x) & 31;
+  if (lane == 0) {
+    bulk_wait<0>();              // this warp's partial stores have been written ...
+    fence_proxy_async_global();  // ... and come before the release below
+    mbar_arrive(gather);
+  }
+  if (!wait_bar(gather, 0, w, WAIT_SPLIT_PEERS)) return;  // all four warps' stores
+  unsigned* const cnt = p.counters + tile;
+  const unsigned target = unsigned(parts);
+  constexpr int F = TILE_M * BN / 4;  // float4s in the tile
+  const int share = (F + parts - 1) / parts;
+  const int f0 = min(F, part * share), f1 = min(F, f0 + share);
+  const uint32_t share_bytes = uint32_t(f1 - f0) * 16u;
+  const int splits = parts / (TILE_M / TC_BM);
+  if (ept == 0) {
+    __threadfence();
+    red_release_add(cnt, 1u);
+    if (wait_counter(cnt, target, w, WAIT_SPLIT_PEERS)) {
+      fence_proxy_async_global();  // the bulk loads read what the releases published
+      mbar_arrive_expect_tx(bar, share_bytes * uint32_t(splits));
+      if (share_bytes > 0) {
+        const int64_t slice = int64_t(p.tail_tiles) * TILE_M * BN;
+        const float* src = p.ws + int64_t(tile) * TILE_M * BN + int64_t(f0) * 4;
+        for (int sl = 0; sl < splits; ++sl) bulk_load_1d(ring + sl * share_bytes, src + sl * slice, share_bytes, bar);
+      }
+    }
+  }
+  if (!wait_bar(bar, 0, w, WAIT_SPLIT_LOAD)) return;  // (also when thread 0 gave up: it set the abort flag)
+  for (int f = f0 + ept; f < f1; f += TC_EPI_WARPS * 32) {
+    const uint8_t* src = ring_p + (f - f0) * 16;
+    float4 acc = *reinterpret_cast<const float4*>(src);
+    for (int sl = 1; sl < splits; ++sl) {
+      const float4 v = *reinterpret_cast<const float4*>(src + sl * share_bytes);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const int e = 4 * f;
+    const int r = e / BN;
+    finish4(p, m_blk * TILE_M + r, n_blk * BN + (e - r * BN), acc);
+  }
+  if (ept == 0) {
+    const unsigned old = atomicAdd(cnt, 1u);
+    if (old == 2u * target - 1u) atomicExch(cnt, 0u);  // every part has seen the count complete
+  }
+}
+
 // The TC_BK/16 MMAs of one ring stage (each reads 32 bytes of K per row:
 // 16 bf16/fp16 or 8 TF32 elements), accumulating unless this is the first
 // stage of the unit.
@@ -360,7 +466,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     for (int e = 0; e < TC_EPI_WARPS; ++e) {
       mbar_init(cload0 + 8 * e, 1);
       mbar_init(xfull0 + 8 * e, 1);  // own arrive.expect_tx; the peer's bytes complete it
-      mbar_init(xfree0 + 8 * e, 1);  // one arrival from the peer per exchange round
+      // one arrival from the peer per exchange round; outside a K pair, xfree[0]
+      // gathers the epilogue warps before an in-kernel split-K reduction
+      mbar_init(xfree0 + 8 * e, (KPAIR || e > 0) ? 1 : TC_EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -687,8 +795,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     int sbuf = 0;
     uint32_t cphase = 0;
     bool ok = true;
+    Unit fused{};  // the K slice this CTA reduces in the kernel (fused_reduce: its last unit)
+    fused.ws_tile = -1;
     for (int u = cta0; u < p.units && ok; u += ncta) {
       const Unit x = unit_of(u);
+      if (x.partial && p.fused_reduce) fused = x;
       // All lanes wait; the warp leaves together if any lane gave up, because the
       // tcgen05.ld below must be executed by the whole warp.
       if (!__all_sync(0xffffffffu, wait(tfull0 + 8 * acc, acc_phase, WAIT_EPI_TMEM_FULL)))
@@ -815,6 +926,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       }
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
+    }
+    if (ok && fused.ws_tile >= 0) {
+      constexpr int CPU = PAIR ? 2 : 1;  // CTAs per unit
+      // (the ring is idle: every MMA of this CTA's last unit has completed)
+      fused_split_reduce<Cfg::TILE_M, BN>(p, fused.ws_tile, fused.split * CPU + int(rank), p.splitk * CPU,
+                                          fused.m_blk, fused.n_blk, base + Cfg::OFF_A, sbase + Cfg::OFF_A,
+                                          xfree0, xfull0, w);
     }
     // The stores must have read the staging buffers before the CTA exits; the
     // grid's completion covers their writes to global memory.

@@ -42,6 +42,12 @@ int cfg_of(int bn, int mode, bool stages) {
 }  // namespace
 
 int tc_smem_bytes(int bn, int mode) { return cfg_of(bn, mode, false); }
+int tc_ring_bytes(int bn, int mode) {
+  const int st = cfg_of(bn, mode, true);
+  if (st <= 0) return -1;
+  const int b_cols = mode == TC_PAIR ? bn / 2 : bn;
+  return st * (TC_BM + b_cols) * TC_BK * 2;
+}
 int tc_stages(int bn, int mode) { return cfg_of(bn, mode, true); }
 
 int tc_max_clusters(int bn, int mode) {

@@ -24,7 +24,9 @@ enum WaitCode : int {
   WAIT_EPI_C_LOAD = 16,
   WAIT_DRAIN = 32,
   WAIT_SELFTEST = 64,
-  WAIT_EPI_EXCHANGE = 128  // K pair: the peer CTA's partial sums or its free buffers
+  WAIT_EPI_EXCHANGE = 128,  // K pair: the peer CTA's partial sums or its free buffers
+  WAIT_SPLIT_PEERS = 256,   // split-K reduced in the GEMM kernel: the tile's other K slices
+  WAIT_SPLIT_LOAD = 512     // ... or the bulk loads of the published slices
 };
 
 // Variants of the tensor-core kernel.
@@ -71,6 +73,16 @@ struct TcParams {
   int dp_units;
   int tail_tiles;
   int splitk;        // K slices of a tail tile
+  // fused_reduce: the slices are summed inside this kernel instead of by the
+  // tile reduction kernel.  Then every partial unit is the last unit of its
+  // CTA (tail_tiles * splitk <= CTAs or clusters) and all are resident at
+  // once; the unit publishes its partials, arrives on the tile's counter
+  // (counters[tail tile], zero on entry and left zero on exit), waits for
+  // all splitk * CTAs-per-unit arrivals, then sums one share of the tile's
+  // elements over slices 0 .. splitk-1 in order and applies the epilogue.
+  int fused_reduce;
+  unsigned* counters;
+  const float* ws;   // the partial workspace (the memory tmW maps)
   int kb_per_split;  // k-blocks per slice (the last one may be shorter); a K pair: per half
   int units;         // dp_units + tail_tiles * splitk (a K pair: tiles)
   int out_kind;      // OutKind of C
@@ -98,6 +110,8 @@ struct TcParams {
 // width and TcMode (TC_PAIR and TC_KPAIR exist for bn 128 and 256); -1 if none.
 int tc_smem_bytes(int bn, int mode);
 int tc_stages(int bn, int mode);
+// Bytes of the operand ring (A and B stages) of one CTA.
+int tc_ring_bytes(int bn, int mode);
 // Clusters of two CTAs of a TC_PAIR / TC_KPAIR kernel that fit on the device at once.
 int tc_max_clusters(int bn, int mode);
 

@@ -141,6 +141,47 @@ __device__ __forceinline__ void bulk_wait() {
   asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// 1-D bulk copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from global memory into this CTA's shared memory, counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Order this thread's async-proxy (TMA) accesses of global memory with its
+// generic-proxy accesses: after the writes of its completed bulk stores,
+// before a release that publishes them; after an acquire, before bulk loads
+// that must see what the release published.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Device-scope release add / acquire load of a global counter.
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Wait until *p >= target, bounded like wait_bar.
+static __device__ __noinline__ bool wait_counter(const unsigned* p, unsigned target, const Watch w, int code) {
+  const uint64_t t0 = global_timer_ns();
+  while (ld_acquire(p) < target) {
+    if (*w.abort) return false;
+    if (global_timer_ns() - t0 > w.limit_ns) {
+      *w.abort = 1;
+      atomicOr(w.err, code);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
 // ------------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
