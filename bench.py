@@ -322,6 +322,9 @@ def main():
                     help="skip the per-call timing of the compute-bound and split-K configurations "
                          "that the default run adds under `other_configs`")
     ap.add_argument("--other-reps", type=int, default=20)
+    ap.add_argument("--only", default=None,
+                    help="comma-separated call names: run only these calls of the workload "
+                         "(e.g. one call for a profiler capture)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--autotune", action="store_true",
                     help="benchmark mode: time the planner's leading candidates once per shape "
@@ -331,6 +334,12 @@ def main():
         args.warmup = 3  # at least three warm-up steps
     ws, rank, local = dist_env()
     wl_name, calls = workload(args.workload)
+    if args.only:
+        keep = set(args.only.split(","))
+        calls = [c for c in calls if c.name in keep]
+        if not calls:
+            raise SystemExit(f"--only matches no call of workload {args.workload}")
+        wl_name += "_only_" + "_".join(c.name for c in calls)
     if args.impl == "reference":
         return run_reference(args, wl_name, calls, rank)
 

@@ -249,42 +249,83 @@ __device__ __forceinline__ void epi32(float (&v)[32], const TcParams& p, int csr
   }
 }
 
-// D(row, col .. col+3) <- act(alpha * acc + beta * C) for the outputs inside
-// C, with the arithmetic of the tile reduction kernel (so both give the same
-// bits); one 16- or 8-byte store when the four lie in C and are aligned.
-__device__ __forceinline__ void finish4(const TcParams& p, int row, int col, float4 acc) {
-  if (row >= p.M || col >= p.N) return;
-  float v[4] = {acc.x, acc.y, acc.z, acc.w};
-  const bool has_beta = p.beta != 0.f;
-  const float4 cv = has_beta ? load_cin4(p, row, col) : make_float4(0.f, 0.f, 0.f, 0.f);
-  const float c[4] = {cv.x, cv.y, cv.z, cv.w};
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    float t = p.alpha * v[j];
-    if (has_beta) t = fmaf(p.beta, c[j], t);
-    v[j] = apply_act(t, p.act, p.slope);
+// The epilogue's inputs, read from the kernel parameters once into registers
+// (the in-kernel split-K reduction applies the epilogue to many outputs per
+// thread).
+struct Fin {
+  const void* cin;
+  int64_t ldcin;
+  int cin_kind;
+  void* c;
+  int64_t ldc;
+  int out_kind;
+  int M, N;
+  float alpha, beta, slope;
+  int act;
+};
+
+__device__ __forceinline__ Fin fin_of(const TcParams& p) {
+  return Fin{p.cin, p.ldcin, p.cin_kind, p.c_ptr, p.ldc, p.out_kind, p.M, p.N, p.alpha, p.beta, p.slope, p.act};
+}
+
+// The four values of the C that beta scales at (row, col .. col+3), zero
+// outside the matrix.
+__device__ __forceinline__ float4 fin_c4(const Fin& f, int row, int col) {
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
+  if (row < f.M && col < f.N) {
+    const int nn = min(4, f.N - col);
+    const int es = f.cin_kind == OUT_F32 ? 4 : 2;
+    const uint8_t* src = static_cast<const uint8_t*>(f.cin) + (int64_t(row) * f.ldcin + col) * es;
+    if (nn == 4 && (reinterpret_cast<uintptr_t>(src) & uintptr_t(4 * es - 1)) == 0) {
+      if (es == 4) return *reinterpret_cast<const float4*>(src);
+      const uint2 w = *reinterpret_cast<const uint2*>(src);
+      const float2 lo = unpack2(w.x, f.cin_kind), hi = unpack2(w.y, f.cin_kind);
+      return make_float4(lo.x, lo.y, hi.x, hi.y);
+    }
+    for (int j = 0; j < nn; ++j)
+      c[j] = es == 4 ? reinterpret_cast<const float*>(src)[j]
+                     : unpack2(reinterpret_cast<const uint16_t*>(src)[j], f.cin_kind).x;
   }
-  const int nn = min(4, p.N - col);
-  if (p.out_kind == OUT_F32) {
-    float* dst = static_cast<float*>(p.c_ptr) + int64_t(row) * p.ldc + col;
-    if (nn == 4 && (reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
-      *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-    } else {
-      for (int j = 0; j < nn; ++j) dst[j] = v[j];
+  return make_float4(c[0], c[1], c[2], c[3]);
+}
+
+// v <- act(alpha * v + beta * C) for 16 values (four groups of four columns),
+// with the arithmetic of the tile reduction kernel so that both give the same
+// bits.  Every run-time choice is taken once for the 16 values: with the
+// activation switch inside an unrolled per-value loop, the executed path was
+// spread over tens of KB of code and every batch missed the instruction cache.
+__device__ __forceinline__ void fin_epilogue16(float (&v)[16], const Fin& f, const int (&row)[4],
+                                               const int (&col)[4]) {
+  if (f.beta != 0.f) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 c = fin_c4(f, row[j], col[j]);
+      v[4 * j + 0] = fmaf(f.beta, c.x, f.alpha * v[4 * j + 0]);
+      v[4 * j + 1] = fmaf(f.beta, c.y, f.alpha * v[4 * j + 1]);
+      v[4 * j + 2] = fmaf(f.beta, c.z, f.alpha * v[4 * j + 2]);
+      v[4 * j + 3] = fmaf(f.beta, c.w, f.alpha * v[4 * j + 3]);
     }
   } else {
-    uint16_t* dst = static_cast<uint16_t*>(p.c_ptr) + int64_t(row) * p.ldc + col;
-    uint16_t o[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      o[j] = p.out_kind == OUT_BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(v[j]))
-                                    : __half_as_ushort(__float2half_rn(v[j]));
-    if (nn == 4 && (reinterpret_cast<uintptr_t>(dst) & 7u) == 0) {
-      *reinterpret_cast<uint2*>(dst) =
-          make_uint2(uint32_t(o[0]) | (uint32_t(o[1]) << 16), uint32_t(o[2]) | (uint32_t(o[3]) << 16));
-    } else {
-      for (int j = 0; j < nn; ++j) dst[j] = o[j];
-    }
+    for (int i = 0; i < 16; ++i) v[i] = f.alpha * v[i];
+  }
+  switch (f.act) {
+    case 0:
+      break;
+    case 1:
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = v[i] < 0.f ? v[i] * f.slope : v[i];
+      break;
+    case 2:
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = v[i] < 0.f ? 0.f : v[i];
+      break;
+    case 3:
+      for (int i = 0; i < 16; ++i) v[i] = apply_act(v[i], 3, 0.f);
+      break;
+    default:
+      for (int i = 0; i < 16; ++i) v[i] = apply_act(v[i], 4, 0.f);
+      break;
   }
 }
 
@@ -298,57 +339,146 @@ __device__ __forceinline__ void finish4(const TcParams& p, int row, int col, flo
 // elements: one bulk load per slice brings that share of every slice into
 // its idle operand ring, and each output is summed over slices 0 .. S-1 in
 // order -- the order of the tile reduction kernel -- before the epilogue.
-// The counter goes back to zero once all parts have seen it complete.
-// `gather` counts one arrival per epilogue warp; `bar` takes the bulk loads.
-// Both are fresh (phase 0) and every wait is bounded.
+// Each thread carries four outputs at a time (independent chains of shared
+// memory loads and adds).  The results, in the output's type, go back into
+// the ring (fp32 in place of slice 0, which each thread has read; 16-bit after
+// the slices) at addresses that share the 16-byte alignment of their place
+// in C, and one thread writes every row segment of the share with a 1-D bulk
+// store (plain stores for the unaligned ends): a few warps' plain global
+// stores, on an SM whose shared memory is almost all carved out, measured
+// ~5 GB/s per SM.  The counter goes back to zero once all parts have seen it
+// complete.  `gather` counts one arrival per epilogue warp (phase 0 before the
+// release, phase 1 once the results are in the ring); `bar` takes the bulk
+// loads.  Both are fresh and every wait is bounded.
 template <int TILE_M, int BN>
-static __device__ __noinline__ void fused_split_reduce(const TcParams& p, int tile, int part, int parts,
-                                                       int m_blk, int n_blk, uint32_t ring,
-                                                       const uint8_t* ring_p, uint32_t gather, uint32_t bar,
-                                                       Watch w) {
+__device__ __forceinline__ void fused_split_reduce(const TcParams& p, int tile, int part, int parts, int m_blk,
+                                                   int n_blk, uint32_t ring, uint32_t gather, uint32_t bar,
+                                                   const Watch& w) {
   const int ept = int(threadIdx.x) - 2 * 32;  // 0 .. 127 over the epilogue warps
   const int lane = int(threadIdx.x) & 31;
+  constexpr uint32_t kAll = 0xffffffffu;
+  // Every wait is taken by the whole warp through __all_sync (the lanes leave
+  // it together, converged), and single-lane work is followed by __syncwarp()
+  // before the warp waits: lanes that left a bounded wait at different times,
+  // or that spin while one lane works, make the warp run its lanes' paths one
+  // after another.
   if (lane == 0) {
     bulk_wait<0>();              // this warp's partial stores have been written ...
     fence_proxy_async_global();  // ... and come before the release below
     mbar_arrive(gather);
   }
-  if (!wait_bar(gather, 0, w, WAIT_SPLIT_PEERS)) return;  // all four warps' stores
+  __syncwarp();
+  const Fin fin = fin_of(p);
   unsigned* const cnt = p.counters + tile;
+  const float* const ws = p.ws;
+  const int tail_tiles = p.tail_tiles;
+  if (!__all_sync(kAll, wait_bar(gather, 0, w, WAIT_SPLIT_PEERS))) return;  // all four warps' stores
   const unsigned target = unsigned(parts);
   constexpr int F = TILE_M * BN / 4;  // float4s in the tile
   const int share = (F + parts - 1) / parts;
   const int f0 = min(F, part * share), f1 = min(F, f0 + share);
   const uint32_t share_bytes = uint32_t(f1 - f0) * 16u;
   const int splits = parts / (TILE_M / TC_BM);
-  if (ept == 0) {
-    __threadfence();
-    red_release_add(cnt, 1u);
-    if (wait_counter(cnt, target, w, WAIT_SPLIT_PEERS)) {
-      fence_proxy_async_global();  // the bulk loads read what the releases published
-      mbar_arrive_expect_tx(bar, share_bytes * uint32_t(splits));
-      if (share_bytes > 0) {
-        const int64_t slice = int64_t(p.tail_tiles) * TILE_M * BN;
-        const float* src = p.ws + int64_t(tile) * TILE_M * BN + int64_t(f0) * 4;
-        for (int sl = 0; sl < splits; ++sl) bulk_load_1d(ring + sl * share_bytes, src + sl * slice, share_bytes, bar);
+  if (ept < 32) {
+    if (lane == 0) {
+      __threadfence();
+      red_release_add(cnt, 1u);
+      if (wait_counter(cnt, target, w, WAIT_SPLIT_PEERS)) {
+        fence_proxy_async_global();  // the bulk loads read what the releases published
+        mbar_arrive_expect_tx(bar, share_bytes * uint32_t(splits));
+        if (share_bytes > 0) {
+          const int64_t slice = int64_t(tail_tiles) * TILE_M * BN;
+          const float* src = ws + int64_t(tile) * TILE_M * BN + int64_t(f0) * 4;
+          for (int sl = 0; sl < splits; ++sl) bulk_load_1d(ring + sl * share_bytes, src + sl * slice, share_bytes, bar);
+        }
+      }
+    }
+    __syncwarp();
+  }
+  if (!__all_sync(kAll, wait_bar(bar, 0, w, WAIT_SPLIT_LOAD))) return;  // (also when lane 0 gave up: abort flag)
+  const int es = fin.out_kind == OUT_F32 ? 4 : 2;
+  const int e0 = 4 * f0, e1 = 4 * f1;  // the share's tile elements
+  // results: element e of the tile at out + (e - e0) * es, out = e0 * es (mod 16)
+  const uint32_t out = (es == 4 ? ring : ((ring + uint32_t(splits) * share_bytes + 15u) & ~15u)) +
+                       (uint32_t(e0 * es) & 15u);
+  constexpr int T = TC_EPI_WARPS * 32;
+  for (int fb = f0 + ept; fb < f1; fb += 4 * T) {
+    float4 acc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int f = min(fb + j * T, f1 - 1);  // (a clamped duplicate is summed but not stored)
+      acc[j] = ld_shared_f4(ring + uint32_t(f - f0) * 16u);
+    }
+    for (int sl = 1; sl < splits; ++sl) {
+      const uint32_t src = ring + uint32_t(sl) * share_bytes;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int f = min(fb + j * T, f1 - 1);
+        const float4 v = ld_shared_f4(src + uint32_t(f - f0) * 16u);
+        acc[j].x += v.x;
+        acc[j].y += v.y;
+        acc[j].z += v.z;
+        acc[j].w += v.w;
+      }
+    }
+    float v[16];
+    int rows[4], cols[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = 4 * (fb + j * T);
+      const int r = e / BN;
+      rows[j] = m_blk * TILE_M + r;
+      cols[j] = n_blk * BN + (e - r * BN);
+      v[4 * j + 0] = acc[j].x;
+      v[4 * j + 1] = acc[j].y;
+      v[4 * j + 2] = acc[j].z;
+      v[4 * j + 3] = acc[j].w;
+    }
+    fin_epilogue16(v, fin, rows, cols);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int f = fb + j * T;
+      if (f < f1) {
+        const uint32_t dst = out + uint32_t(4 * f - e0) * uint32_t(es);
+        if (es == 4)
+          st_shared_f4(dst, make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+        else
+          st_shared_u2(dst, pack2(v[4 * j], v[4 * j + 1], fin.out_kind), pack2(v[4 * j + 2], v[4 * j + 3], fin.out_kind));
       }
     }
   }
-  if (!wait_bar(bar, 0, w, WAIT_SPLIT_LOAD)) return;  // (also when thread 0 gave up: it set the abort flag)
-  for (int f = f0 + ept; f < f1; f += TC_EPI_WARPS * 32) {
-    const uint8_t* src = ring_p + (f - f0) * 16;
-    float4 acc = *reinterpret_cast<const float4*>(src);
-    for (int sl = 1; sl < splits; ++sl) {
-      const float4 v = *reinterpret_cast<const float4*>(src + sl * share_bytes);
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+  fence_proxy_async_smem();  // the bulk stores read these results through the async proxy
+  __syncwarp();
+  if (lane == 0) mbar_arrive(gather);
+  __syncwarp();
+  if (!__all_sync(kAll, wait_bar(gather, 1, w, WAIT_SPLIT_LOAD))) return;  // every warp's results are in
+  // One row segment of C per tile row the share touches, rows spread over the
+  // 128 threads: a 1-D bulk store for its 16-byte aligned part, plain stores
+  // for the ends.
+  const int epb = 16 / es;  // elements per 16 bytes
+  for (int r = e0 / BN + ept; r * BN < e1; r += T) {
+    const int row = m_blk * TILE_M + r;
+    if (row >= fin.M) break;
+    const int c_lo = max(e0, r * BN) - r * BN, c_hi = min(e1, (r + 1) * BN) - r * BN;
+    const int g_lo = n_blk * BN + c_lo, g_hi = min(n_blk * BN + c_hi, fin.N);
+    if (g_lo >= g_hi) continue;
+    const int a_lo = min(g_hi, (g_lo + epb - 1) / epb * epb);
+    const int a_hi = max(a_lo, g_hi / epb * epb);
+    uint8_t* const crow = static_cast<uint8_t*>(fin.c) + int64_t(row) * fin.ldc * es;
+    auto src_of = [&](int g) { return out + uint32_t(r * BN + (g - n_blk * BN) - e0) * uint32_t(es); };
+    if (a_lo < a_hi) bulk_store_1d(crow + int64_t(a_lo) * es, src_of(a_lo), uint32_t(a_hi - a_lo) * uint32_t(es));
+    for (int g = g_lo; g < g_hi; ++g) {  // the unaligned ends, element by element
+      if (g == a_lo) g = a_hi;
+      if (g >= g_hi) break;
+      if (es == 4)
+        *reinterpret_cast<uint32_t*>(crow + int64_t(g) * 4) = ld_shared_u32(src_of(g));
+      else
+        *reinterpret_cast<uint16_t*>(crow + int64_t(g) * 2) = uint16_t(ld_shared_u16(src_of(g)));
     }
-    const int e = 4 * f;
-    const int r = e / BN;
-    finish4(p, m_blk * TILE_M + r, n_blk * BN + (e - r * BN), acc);
   }
+  bulk_commit();
+  bulk_wait_read<0>();  // this thread's bulk stores have read the ring before the CTA exits
+  __syncwarp();
   if (ept == 0) {
     const unsigned old = atomicAdd(cnt, 1u);
     if (old == 2u * target - 1u) atomicExch(cnt, 0u);  // every part has seen the count complete
@@ -621,8 +751,23 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     uint32_t acc_phase = 0;
     uint32_t xphase = 0;
     bool ok = true;
+    // My staging buffers are free once my earlier stores from them have read
+    // them: tell the peer and arm my receive.  (The peer can only send for the
+    // next round after this warp has waited for the peer's data of this one,
+    // so no arrival ever runs a phase ahead.)
+    auto free_and_arm = [&]() {
+      if (lane == 0) {
+        bulk_wait_read<0>();
+        mbar_arrive_cluster(peer_xfree);
+        mbar_arrive_expect_tx(xfull, 2 * Cfg::STG_BYTES);
+      }
+      __syncwarp();
+    };
     for (int u = cta0; u < p.units && ok; u += ncta) {
       const Unit x = unit_of(u);
+      // Round 0's handshake does not need the accumulator: it overlaps the
+      // tile's last MMAs instead of following them.
+      free_and_arm();
       if (!__all_sync(0xffffffffu, wait(tfull0 + 8 * acc, acc_phase, WAIT_EPI_TMEM_FULL))) break;
       tc_fence_after();
       const int y0 = x.m_blk * TC_BM + 32 * q;
@@ -632,12 +777,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       for (int rd = 0; rd < Cfg::KP_ROUNDS; ++rd) {
         const int own_c = int(rank) * (BN / 2) + rd * 64;  // tile columns finished here
         const int peer_c = int(peer) * (BN / 2) + rd * 64;
-        if (lane == 0) {
-          bulk_wait_read<0>();
-          mbar_arrive_cluster(peer_xfree);
-          mbar_arrive_expect_tx(xfull, 2 * Cfg::STG_BYTES);
-        }
-        __syncwarp();
+        if (rd > 0) free_and_arm();
         {
           uint32_t r0[32], r1[32];
           tmem_ld_32x32b_x32(t_row + peer_c, r0);
@@ -667,6 +807,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
           if (last) {
             if (lane == 0) bulk_copy_to_cluster(peer_stg0, snd, 2 * Cfg::STG_BYTES, peer_xfull);
+            __syncwarp();  // the copy is issued before any lane of this warp waits
           } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -775,6 +916,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      __syncwarp();
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -841,6 +983,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             mbar_arrive_expect_tx(cload0 + 8 * e, Cfg::STG_BYTES);
             tma_load_2d(stg, &tmC, cload0 + 8 * e, x0, y0);
           }
+          __syncwarp();  // the load is issued before any lane of this warp waits for it
           if (!__all_sync(0xffffffffu, wait(cload0 + 8 * e, cphase, WAIT_EPI_C_LOAD))) {
             ok = false;
             break;
@@ -924,6 +1067,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         else
           mbar_arrive(tempty0 + 8 * acc);
       }
+      __syncwarp();
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -931,8 +1075,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       constexpr int CPU = PAIR ? 2 : 1;  // CTAs per unit
       // (the ring is idle: every MMA of this CTA's last unit has completed)
       fused_split_reduce<Cfg::TILE_M, BN>(p, fused.ws_tile, fused.split * CPU + int(rank), p.splitk * CPU,
-                                          fused.m_blk, fused.n_blk, base + Cfg::OFF_A, sbase + Cfg::OFF_A,
-                                          xfree0, xfull0, w);
+                                          fused.m_blk, fused.n_blk, base + Cfg::OFF_A, xfree0, xfull0, w);
     }
     // The stores must have read the staging buffers before the CTA exits; the
     // grid's completion covers their writes to global memory.

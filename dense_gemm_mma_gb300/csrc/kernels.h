@@ -73,8 +73,8 @@ struct TcParams {
   int dp_units;
   int tail_tiles;
   int splitk;        // K slices of a tail tile
-  // fused_reduce: the slices are summed inside this kernel instead of by the
-  // tile reduction kernel.  Then every partial unit is the last unit of its
+  // fused_reduce (GEMM_FUSED_REDUCE=1): the slices are summed inside this
+  // kernel instead of by the tile reduction kernel.  Then every partial unit is the last unit of its
   // CTA (tail_tiles * splitk <= CTAs or clusters) and all are resident at
   // once; the unit publishes its partials, arrives on the tile's counter
   // (counters[tail tile], zero on entry and left zero on exit), waits for

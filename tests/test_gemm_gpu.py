@@ -174,16 +174,17 @@ FUSED_CASES = [
 @pytest.mark.parametrize("tile,shape,env,out_fmt", FUSED_CASES,
                          ids=[f"{c[0]}_{'x'.join(map(str, c[1]))}" for c in FUSED_CASES])
 def test_fused_reduction_bitwise_equals_reduction_kernel(plan, tile, shape, env, out_fmt):
-    """K slices that all run at once are summed inside the GEMM kernel: each
-    CTA publishes its slice's partials, waits for the tile's other slices and
-    sums its share of the tile over the slices in order.  The tile reduction
-    kernel (GEMM_FUSED_REDUCE=0) sums the same partials in the same order with
-    the same epilogue, so the two agree bit for bit; both match the oracle and
-    repeat bit for bit (the arrival counters are back at zero after a call)."""
+    """With GEMM_FUSED_REDUCE=1, K slices that all run at once are summed
+    inside the GEMM kernel: each CTA publishes its slice's partials, waits for
+    the tile's other slices and sums its share of the tile over the slices in
+    order.  The tile reduction kernel (the default) sums the same partials in
+    the same order with the same epilogue, so the two agree bit for bit; both
+    match the oracle and repeat bit for bit (the arrival counters are back at
+    zero after a call)."""
     env = {**env, "GEMM_FORCE_TILE": tile}
     kw = dict(beta=0.5, act=1, slope=0.2, out_fmt=out_fmt, seed=90 + shape[2] % 7, pad=(0, 0, 8))
-    a = run_case(plan, *shape, env=env, repeat=3, **kw)
-    b = run_case(plan, *shape, env={**env, "GEMM_FUSED_REDUCE": "0"}, **kw)
+    a = run_case(plan, *shape, env={**env, "GEMM_FUSED_REDUCE": "1"}, repeat=3, **kw)
+    b = run_case(plan, *shape, env=env, **kw)
     assert a.info["launches"] == 1 and b.info["launches"] == 2
     assert a.info["path"] == b.info["path"] and a.info["path"] in ("tc_splitk", "tc_tail_split")
     for out in a.outputs[1:] + b.outputs:
@@ -430,8 +431,7 @@ def test_tail_split_ragged(plan, tile, shape):
     r = run_case(plan, *shape, env={"GEMM_TAIL_SPLIT": "3", "GEMM_FORCE_TILE": tile}, seed=80 + len(tile))
     i = r.info
     assert i["path"] == "tc_tail_split" and i["splitk"] == 3 and 0 < i["tail_tiles"] < i["tiles"]
-    # the tail tiles' slices run one per CTA at the same time: reduced inside the GEMM kernel
-    assert i["units"] == i["tiles"] - i["tail_tiles"] + 3 * i["tail_tiles"] and i["launches"] == 1
+    assert i["units"] == i["tiles"] - i["tail_tiles"] + 3 * i["tail_tiles"] and i["launches"] == 2
 
 
 @pytest.mark.parametrize("out_fmt", ["f32", "bf16", "f16"])

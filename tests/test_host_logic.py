@@ -289,11 +289,7 @@ def test_planner_invariants(M, N, K):
         per = -(-kb // c.splitk)
         assert -(-kb // per) == c.splitk                  # no empty K slice
         assert (c.path in (2, 7, 8)) == (c.splitk > 1)
-        # K slices that all run at once (each the last unit of its CTA) are summed inside
-        # the GEMM kernel; more slices than CTAs take the reduction kernel
-        fused = c.path in (2, 8) and c.tail_tiles * c.splitk <= c.grid // c.cta_per_tile
-        assert c.launches == (2 if c.path in (2, 8) and not fused else 1)
-        assert c.path != 8 or fused
+        assert c.launches == (2 if c.path in (2, 8) else 1)
         assert c.workspace_bytes == c.tail_tiles * c.splitk * c.tile_m * c.tile_n * 4
 
 
@@ -390,7 +386,7 @@ def test_planner_tail_split(monkeypatch):
     the tail split runs 76 whole tiles and splits the 5 along K."""
     c = g.gemm_choose_config(2304, 2176, 4096, g.GEMM_F16_F32, 0, 0, 152)
     assert g.PATH_NAMES[c.path] == "tc_tail_split" and c.tiles == 81 and c.tail_tiles == 5
-    assert c.units == 76 + 5 * c.splitk and c.launches == 1   # the slices are reduced in the kernel
+    assert c.units == 76 + 5 * c.splitk and c.launches == 2
     # a full last wave has no tail to split
     assert g.gemm_choose_config(2304, 1984, 4096, g.GEMM_F16_F32, 0, 0, 152).path == 1
     monkeypatch.setenv("GEMM_TAIL_SPLIT", "0")
@@ -399,6 +395,21 @@ def test_planner_tail_split(monkeypatch):
     monkeypatch.setenv("GEMM_FORCE_TILE", "128x128")
     c = g.gemm_choose_config(300, 2000, 1000, g.GEMM_F16_F32, 0, 0, 20)
     assert c.path == 8 and c.splitk == 3 and c.tiles == 3 * 16 and c.tail_tiles == 48 % 20
+
+
+def test_fused_reduction_is_opt_in(monkeypatch):
+    """GEMM_FUSED_REDUCE=1 sums K slices that all run at once inside the GEMM
+    kernel (one launch); by default the tile reduction kernel does (two)."""
+    c = g.gemm_choose_config(256, 256, 65536, g.GEMM_F16_F32, 0, 0, 152)
+    assert c.path == 2 and c.launches == 2
+    monkeypatch.setenv("GEMM_FUSED_REDUCE", "1")
+    c = g.gemm_choose_config(256, 256, 65536, g.GEMM_F16_F32, 0, 0, 152)
+    assert c.path == 2 and c.launches == 1 and c.tail_tiles * c.splitk <= c.grid // c.cta_per_tile
+    # more slices than CTAs: the reduction kernel all the same
+    monkeypatch.setenv("GEMM_FORCE_SPLITK", "64")
+    monkeypatch.setenv("GEMM_FORCE_TILE", "128x64")
+    c = g.gemm_choose_config(256, 256, 65536, g.GEMM_F16_F32, 0, 0, 152)
+    assert c.units > 152 and c.launches == 2
 
 
 def test_planner_env_overrides(monkeypatch):
