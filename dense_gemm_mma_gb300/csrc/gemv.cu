@@ -342,7 +342,9 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvArgs g) {
 // One thread per 4 adjacent columns of a row of a tail tile: sums the tile's
 // slices s = 0..S-1 in order (16-byte loads from the tile-major workspace),
 // applies the epilogue and stores the outputs that lie inside C.
-__global__ void __launch_bounds__(256) tile_reduce_kernel(const TileReduceArgs a) {
+constexpr int kReduceThreads = 128;
+
+__global__ void __launch_bounds__(kReduceThreads) tile_reduce_kernel(const TileReduceArgs a) {
   // Launched as a programmatic dependent of the GEMM that writes the partials:
   // this CTA may start before that grid ends, so wait for its results here.
   wait_prior_grid();
@@ -368,7 +370,22 @@ __global__ void __launch_bounds__(256) tile_reduce_kernel(const TileReduceArgs a
     if (m >= a.M || n >= N) continue;
     const float* src = a.ws + (static_cast<int64_t>(t) * a.tile_m + r) * a.tile_n + c4 * 4;
     float4 s = __ldcs(reinterpret_cast<const float4*>(src));
-    for (int sp = 1; sp < a.splits; ++sp) {
+    int sp = 1;
+    // slices in order, eight loads in flight before their adds (the sum is
+    // s0 + s1 + s2 + ... whatever the batching)
+    for (; sp + 8 <= a.splits; sp += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcs(reinterpret_cast<const float4*>(src + (sp + u) * slice));
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        s.x += v[u].x;
+        s.y += v[u].y;
+        s.z += v[u].z;
+        s.w += v[u].w;
+      }
+    }
+    for (; sp < a.splits; ++sp) {
       const float4 v = __ldcs(reinterpret_cast<const float4*>(src + sp * slice));
       s.x += v.x;
       s.y += v.y;
@@ -600,10 +617,13 @@ cudaError_t launch_tile_reduce(const TileReduceArgs& a, cudaStream_t s, int sms)
   // the GEMM; its griddepcontrol.wait orders it after the GEMM's writes.
   // (a grid-stride kernel: no more CTAs than are resident at once, so none
   // waits for a slot and runs its share after the others)
+  // (128-thread CTAs: a split-K call has few tiles, and smaller CTAs spread
+  // its items over more SMs)
   static std::atomic<int64_t> occ{-1};
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid_for(items, 256, sms, resident_per_sm(tile_reduce_kernel, occ, 256, 0)));
-  cfg.blockDim = dim3(256);
+  cfg.gridDim = dim3(grid_for(items, kReduceThreads, sms,
+                              resident_per_sm(tile_reduce_kernel, occ, kReduceThreads, 0)));
+  cfg.blockDim = dim3(kReduceThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
