@@ -94,6 +94,8 @@ struct gemm_plan {
   // descriptor encoding (host time that would otherwise sit in front of the
   // kernels on the stream).
   std::unordered_map<TcKey, TcEntry, TcKeyHash> tc_cache;
+  // GEMM_LOG=1 (read at plan creation): one line per call on stderr.
+  bool log = false;
   // Benchmark mode: the fastest measured choice per shape (key without pointers).
   bool autotune = false;
   std::unordered_map<TcKey, TcChoice, TcKeyHash> tuned;
@@ -1054,6 +1056,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* plan, int device) {
   p->sms = prop.multiProcessorCount;
   p->autotune = env_int("GEMM_AUTOTUNE", 0) != 0;
   p->pdl = env_int("GEMM_PDL", 1) != 0;
+  p->log = env_int("GEMM_LOG", 0) != 0;
   if (const char* w = std::getenv("GEMM_WATCHDOG_NS")) {
     const unsigned long long v = std::strtoull(w, nullptr, 10);
     if (v >= 1000) p->watchdog_ns = v;
@@ -1088,6 +1091,22 @@ gemm_status_t gemm_check_args(int64_t M, int64_t N, int64_t K, const void* A, in
 }
 
 namespace {
+
+// GEMM_LOG=1: the decisions of a planned call, one line on stderr.
+void log_config(const char* who, int64_t M, int64_t N, int64_t K, int dtype, int ta, int tb,
+                const gemm_config_info_t& c) {
+  static const char* kPath[] = {"none", "tc", "tc_splitk", "gemv_rowdot", "gemv_colstream", "gemv_generic",
+                                "scale", "tc_splitk_cluster", "tc_tail_split"};
+  static const char* kType[] = {"bf16->f32", "bf16->bf16", "f16->f32", "f16->f16", "tf32->f32"};
+  const char* path = c.path >= 0 && c.path <= 8 ? kPath[c.path] : "?";
+  const char* type = dtype >= 0 && dtype <= 4 ? kType[dtype] : "?";
+  std::fprintf(stderr,
+               "gemm_log %s: %lldx%lldx%lld %s op(A)=%c op(B)=%c -> %s tile %dx%d cta/tile %d split %d tail "
+               "tiles %d grid %d sms %d tiles %lld waves %.3f tail fraction %.3f launches %d workspace %lld B\n",
+               who, (long long)M, (long long)N, (long long)K, type, ta ? 'T' : 'N', tb ? 'T' : 'N', path, c.tile_m,
+               c.tile_n, c.cta_per_tile, c.splitk, c.tail_tiles, c.grid, c.sms, (long long)c.tiles, c.waves,
+               c.tail_fraction, c.launches, (long long)c.workspace_bytes);
+}
 
 int type_kind(gemm_type_t t) {
   return t == GEMM_TYPE_F32 ? dg::OUT_F32 : (t == GEMM_TYPE_BF16 ? dg::OUT_BF16 : dg::OUT_F16);
@@ -1178,6 +1197,7 @@ gemm_status_t run_all(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, const v
   }
   if (r != GEMM_OK) cudaGetLastError();
   plan->last = info;
+  if (plan->log && r == GEMM_OK) log_config("gemm_run", M, N, K, dtype, transA, transB, info);
   return r;
 }
 
@@ -1275,9 +1295,22 @@ gemm_status_t gemm_plan_selftest_watchdog(gemm_plan_t plan, void* stream) {
   return gemm_plan_poll_error(plan, stream);
 }
 
+namespace {
+gemm_status_t choose_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, gemm_op_t transA,
+                            gemm_op_t transB, int32_t sms, gemm_config_info_t* out);
+}  // namespace
+
 gemm_status_t gemm_choose_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
                                  gemm_op_t transA, gemm_op_t transB, int32_t sms,
                                  gemm_config_info_t* out) {
+  const gemm_status_t st = choose_config(M, N, K, dtype, transA, transB, sms, out);
+  if (st == GEMM_OK && env_int("GEMM_LOG", 0) != 0) log_config("gemm_choose_config", M, N, K, dtype, transA, transB, *out);
+  return st;
+}
+
+namespace {
+gemm_status_t choose_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype, gemm_op_t transA,
+                            gemm_op_t transB, int32_t sms, gemm_config_info_t* out) {
   if (!out || sms <= 0 || M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
   if (dtype < GEMM_BF16_F32 || dtype > GEMM_TF32_F32) return GEMM_ERR_INVALID_ARG;
   if ((transA != GEMM_OP_N && transA != GEMM_OP_T) || (transB != GEMM_OP_N && transB != GEMM_OP_T))
@@ -1312,6 +1345,7 @@ gemm_status_t gemm_choose_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t d
   choose_tc(M, N, K, sms, out_is_f32(dtype) ? 4 : 2, false, out, in_bytes(dtype));
   return GEMM_OK;
 }
+}  // namespace
 
 gemm_status_t gemm_quantization(int64_t M, int64_t N, int32_t tile_m, int32_t tile_n,
                                 int32_t splitk, int32_t sms, int32_t ctas_per_sm,

@@ -155,7 +155,10 @@ typedef struct {
 /* Create a plan bound to CUDA device `device` (the caller's current device is
  * restored before returning).  Queries the SM count and allocates the
  * watchdog word.  Returns GEMM_ERR_NO_DEVICE if the device does not exist or
- * is not compute capability 10.x, GEMM_ERR_INVALID_ARG if plan is NULL. */
+ * is not compute capability 10.x, GEMM_ERR_INVALID_ARG if plan is NULL.
+ * With GEMM_LOG=1 in the environment at creation, every successful gemm_run /
+ * gemm_run_ex of the plan prints one line on stderr: the shape, the types and
+ * the decisions of gemm_config_info_t (gemm_choose_config does the same). */
 gemm_status_t gemm_plan_create(gemm_plan_t* plan, int device);
 
 /* C <- act(alpha * op(A) @ op(B) + beta * C), enqueued on `stream` (a

@@ -397,6 +397,26 @@ def test_planner_tail_split(monkeypatch):
     assert c.path == 8 and c.splitk == 3 and c.tiles == 3 * 16 and c.tail_tiles == 48 % 20
 
 
+def test_planner_log_lines():
+    """GEMM_LOG=1 prints one line per planned call on stderr: the shape, the types,
+    and the decisions (path, tile, split, grid, waves, tail, launches, workspace)."""
+    import subprocess
+    import sys
+    code = ("from dense_gemm_mma_gb300 import gemm as g; "
+            "g.gemm_choose_config(256, 256, 65536, g.GEMM_F16_F32, 0, 0, 152); "
+            "g.gemm_choose_config(1, 8192, 8192, g.GEMM_BF16_F32, 0, 1, 152)")
+    env = dict(os.environ, GEMM_LOG="1")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT)
+    lines = [l for l in r.stderr.splitlines() if l.startswith("gemm_log")]
+    assert len(lines) == 2, r.stderr
+    assert "256x256x65536 f16->f32 op(A)=N op(B)=N -> tc_splitk tile 128x" in lines[0]
+    assert "launches 2" in lines[0] and "workspace" in lines[0]
+    assert "1x8192x8192 bf16->f32 op(A)=N op(B)=T -> gemv_rowdot" in lines[1]
+    env.pop("GEMM_LOG")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, cwd=ROOT)
+    assert "gemm_log" not in r.stderr
+
+
 def test_fused_reduction_is_opt_in(monkeypatch):
     """GEMM_FUSED_REDUCE=1 sums K slices that all run at once inside the GEMM
     kernel (one launch); by default the tile reduction kernel does (two)."""
