@@ -54,6 +54,7 @@
 #pragma once
 
 #include <atomic>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -99,6 +100,9 @@ struct TcCfg {
   // On a cluster's last tile the A ring is idle once the accumulator is
   // complete: it holds the outgoing partials of every warp and round.
   static_assert(!KPAIR || KP_ROUNDS * TC_EPI_WARPS * 2 * STG_BYTES <= STAGES * A_STAGE, "send buffer");
+  // ... and it holds one staging buffer per fp32 chunk of every epilogue warp
+  // (the epilogue of a CTA's last unit).
+  static_assert(TC_EPI_WARPS * (BN / 32) * STG_BYTES <= STAGES * (A_STAGE + B_STAGE), "last-unit staging");
 };
 
 struct Unit {
@@ -185,18 +189,24 @@ enum CSource : int {
   C_DIRECT = 2   // a separate C (or a K pair's), read from global memory
 };
 
-// v <- act(alpha * v + beta * C) on the 32 consecutive columns [col0, col0+32)
-// of output row `row`.  C_STAGED: the 32 values start at 16-byte chunk
-// `chunk0` of the lane's swizzled 128-byte staging line, in the output's
-// format (esize bytes each).  Every run-time choice is taken once, outside
-// the unrolled loops, so the path a launch takes is straight-line code (the
-// epilogue shares the SM's instruction cache with the producer and MMA warps).
-__device__ __forceinline__ void epi32(float (&v)[32], const TcParams& p, int csrc, const uint8_t* row_p,
-                                      int sw, int chunk0, int esize, int row, int col0) {
-  if (csrc == C_NONE) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] *= p.alpha;
-  } else if (csrc == C_STAGED && esize == 4) {
+// Epilogue variants, compiled separately so that a tile's epilogue loop holds
+// only the code its call can take: EPI_PLAIN (beta == 0; identity, LeakyReLU
+// or ReLU), EPI_BETA (any C source; those activations), EPI_ALL (GELU, SiLU).
+// With every variant inlined into one loop, the fp32 path of a 256-column
+// chunk crossed tens of KB of code that it skipped, missed the instruction
+// cache on every chunk (~0.5 us a chunk) and evicted the producer's and MMA
+// issuer's code, which share the cache.
+enum EpiVariant : int { EPI_PLAIN = 0, EPI_BETA = 1, EPI_ALL = 2 };
+
+__device__ __forceinline__ int epi_variant(const TcParams& p, bool has_beta) {
+  if (p.act >= 3) return EPI_ALL;
+  return has_beta ? EPI_BETA : EPI_PLAIN;
+}
+
+// v <- alpha * v + beta * C (C_STAGED or C_DIRECT).
+__device__ __forceinline__ void epi_beta(float (&v)[32], const TcParams& p, int csrc, const uint8_t* row_p,
+                                         int sw, int chunk0, int esize, int row, int col0) {
+  if (csrc == C_STAGED && esize == 4) {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       const float4 c = *reinterpret_cast<const float4*>(row_p + (((chunk0 + j) ^ sw) << 4));
@@ -227,26 +237,43 @@ __device__ __forceinline__ void epi32(float (&v)[32], const TcParams& p, int csr
       v[4 * j + 3] = fmaf(p.beta, c.w, p.alpha * v[4 * j + 3]);
     }
   }
-  switch (p.act) {
-    case 0:
-      break;
-    case 1:
+}
+
+// v <- act(v): identity, LeakyReLU and ReLU in every variant, GELU and SiLU in EPI_ALL.
+template <int V>
+__device__ __forceinline__ void epi_act(float (&v)[32], const TcParams& p) {
+  if (p.act == 1) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = v[i] < 0.f ? v[i] * p.slope : v[i];
-      break;
-    case 2:
+    for (int i = 0; i < 32; ++i) v[i] = v[i] < 0.f ? v[i] * p.slope : v[i];
+  } else if (p.act == 2) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i) v[i] = v[i] < 0.f ? 0.f : v[i];
-      break;
-    case 3:
+    for (int i = 0; i < 32; ++i) v[i] = v[i] < 0.f ? 0.f : v[i];
+  } else if constexpr (V == EPI_ALL) {
+    if (p.act == 3) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = apply_act(v[i], 3, 0.f);
-      break;
-    default:
+    } else if (p.act == 4) {
 #pragma unroll
       for (int i = 0; i < 32; ++i) v[i] = apply_act(v[i], 4, 0.f);
-      break;
+    }
   }
+}
+
+// v <- act(alpha * v + beta * C) on the 32 consecutive columns [col0, col0+32)
+// of output row `row`.  C_STAGED: the 32 values start at 16-byte chunk
+// `chunk0` of the lane's swizzled 128-byte staging line, in the output's
+// format (esize bytes each).  Every run-time choice is taken once, outside
+// the unrolled loops, so the path a launch takes is straight-line code.
+template <int V>
+__device__ __forceinline__ void epi32(float (&v)[32], const TcParams& p, int csrc, const uint8_t* row_p,
+                                      int sw, int chunk0, int esize, int row, int col0) {
+  if (V == EPI_PLAIN || csrc == C_NONE) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] *= p.alpha;
+    return epi_act<V>(v, p);
+  }
+  if constexpr (V != EPI_PLAIN) epi_beta(v, p, csrc, row_p, sw, chunk0, esize, row, col0);
+  epi_act<V>(v, p);
 }
 
 // The epilogue's inputs, read from the kernel parameters once into registers
@@ -774,6 +801,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const int row = y0 + lane;
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc * BN);
+      // one compiled copy of the exchange rounds per epilogue variant, chosen per tile
+      auto rounds = [&](auto variant) {
+      constexpr int V = decltype(variant)::value;
       for (int rd = 0; rd < Cfg::KP_ROUNDS; ++rd) {
         const int own_c = int(rank) * (BN / 2) + rd * 64;  // tile columns finished here
         const int peer_c = int(peer) * (BN / 2) + rd * 64;
@@ -839,7 +869,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
               v[4 * j + 2] = __uint_as_float(r[4 * j + 2]) + pv.z;
               v[4 * j + 3] = __uint_as_float(r[4 * j + 3]) + pv.w;
             }
-            epi32(v, p, has_beta ? C_DIRECT : C_NONE, row_p, sw, 0, 4, row, x0);
+            epi32<V>(v, p, has_beta ? C_DIRECT : C_NONE, row_p, sw, 0, 4, row, x0);
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               *reinterpret_cast<float4*>(row_p + ((j ^ sw) << 4)) =
@@ -886,8 +916,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             v1[i] = __uint_as_float(r1[i]) + pv[32 + i];
           }
           const int csrc = has_beta ? C_DIRECT : C_NONE;
-          epi32(v0, p, csrc, row_p, sw, 0, 2, row, x0);
-          epi32(v1, p, csrc, row_p, sw, 4, 2, row, x0 + 32);
+          epi32<V>(v0, p, csrc, row_p, sw, 0, 2, row, x0);
+          epi32<V>(v1, p, csrc, row_p, sw, 4, 2, row, x0 + 32);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float* h = j < 4 ? &v0[8 * (j & 3)] : &v1[8 * (j & 3)];
@@ -911,6 +941,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           }
         }
       }
+      };
+      const int variant = epi_variant(p, has_beta);
+      if (variant == EPI_PLAIN)
+        rounds(std::integral_constant<int, EPI_PLAIN>{});
+      else if (variant == EPI_BETA)
+        rounds(std::integral_constant<int, EPI_BETA>{});
+      else
+        rounds(std::integral_constant<int, EPI_ALL>{});
       if (!ok) break;
       // this warp's reads of the accumulator are complete: release it
       tc_fence_before();
@@ -966,9 +1004,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       const uint32_t t_row = tmem_base + (static_cast<uint32_t>(32 * q) << 16) +
                              static_cast<uint32_t>(acc * BN);
       const int chunks = BN / cw;
+      // On the CTA's last unit the operand ring is idle (every MMA of the unit
+      // has completed, no load follows): each chunk gets a staging buffer of
+      // its own there, so no store waits for an earlier one to have been read
+      // (with one tile per CTA, two buffers per warp left the epilogue of a
+      // 256x256 pair tile at ~5.6 us).
+      const bool spread = u + ncta >= p.units;
+      // One compiled copy of the chunk loop per epilogue variant (EpiVariant),
+      // chosen once per tile.
+      auto chunk_loop = [&](auto variant) {
+      constexpr int V = decltype(variant)::value;
       for (int c = 0; c < chunks; ++c) {
-        const uint32_t stg = stg0 + sbuf * Cfg::STG_BYTES;
-        uint8_t* const stg_p = stg_p0 + sbuf * Cfg::STG_BYTES;
+        const uint32_t ring_buf = uint32_t(Cfg::OFF_A + (e * chunks + c) * Cfg::STG_BYTES);
+        const uint32_t stg = spread ? base + ring_buf : stg0 + sbuf * Cfg::STG_BYTES;
+        uint8_t* const stg_p = spread ? sbase + ring_buf : stg_p0 + sbuf * Cfg::STG_BYTES;
         const int x0 = n0 + c * cw;
         // A TMA store writes whole 16-byte pieces of a row, so columns past the
         // last 16-byte boundary inside C, [n_tma, N), are written by the threads.
@@ -976,9 +1025,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         const int tail_lo = max(x0, p.n_tma), tail_hi = min(x0 + cw, p.N);
         const int row = row0 + lane;
         const bool has_tail = !partial && tail_lo < tail_hi && row < p.M;
-        if (lane == 0) bulk_wait_read<1>();  // the store that last used this buffer has read it
+        if (lane == 0 && !spread) bulk_wait_read<1>();  // the store that last used this buffer has read it
         __syncwarp();
-        if (c_tma && tma_cols) {
+        if (V != EPI_PLAIN && c_tma && tma_cols) {
           if (lane == 0) {
             mbar_arrive_expect_tx(cload0 + 8 * e, Cfg::STG_BYTES);
             tma_load_2d(stg, &tmC, cload0 + 8 * e, x0, y0);
@@ -993,7 +1042,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         __syncwarp();
         uint8_t* const row_p = stg_p + lane * 128;
         const int sw = lane & 7;  // 128-byte swizzle: 16-byte chunk j lives at j ^ (row % 8)
-        if (c_tma && has_tail) {
+        if (V != EPI_PLAIN && c_tma && has_tail) {
           for (int col = tail_lo; col < tail_hi; ++col) {
             const int b = (col - x0) * esize;
             uint8_t* dst = row_p + ((((b >> 4) ^ sw)) << 4) + (b & 15);
@@ -1011,7 +1060,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           float v[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          if (!partial) epi32(v, p, csrc, row_p, sw, 0, 4, row, x0);  // partials stay raw
+          if (!partial) epi32<V>(v, p, csrc, row_p, sw, 0, 4, row, x0);  // partials stay raw
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             *reinterpret_cast<float4*>(row_p + ((j ^ sw) << 4)) =
@@ -1028,8 +1077,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             v0[i] = __uint_as_float(r0[i]);
             v1[i] = __uint_as_float(r1[i]);
           }
-          epi32(v0, p, csrc, row_p, sw, 0, 2, row, x0);  // (16-bit output: never a partial unit)
-          epi32(v1, p, csrc, row_p, sw, 4, 2, row, x0 + 32);
+          epi32<V>(v0, p, csrc, row_p, sw, 0, 2, row, x0);  // (16-bit output: never a partial unit)
+          epi32<V>(v1, p, csrc, row_p, sw, 4, 2, row, x0 + 32);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float* h = j < 4 ? &v0[8 * (j & 3)] : &v1[8 * (j & 3)];
@@ -1057,6 +1106,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         }
         sbuf ^= 1;
       }
+      };
+      const int variant = partial ? int(EPI_PLAIN) : epi_variant(p, has_beta);
+      if (variant == EPI_PLAIN)
+        chunk_loop(std::integral_constant<int, EPI_PLAIN>{});
+      else if (variant == EPI_BETA)
+        chunk_loop(std::integral_constant<int, EPI_BETA>{});
+      else
+        chunk_loop(std::integral_constant<int, EPI_ALL>{});
       // This warp's reads of the accumulator are complete: release it (to the
       // leader, whose MMA warp waits for both CTAs of a pair).
       tc_fence_before();
