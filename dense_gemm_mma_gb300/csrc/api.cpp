@@ -236,27 +236,37 @@ void quantization(int64_t M, int64_t N, int tm, int tn, int splitk, int sms, int
 
 // Cost model of the tensor-core path (seconds), calibrated on GB300 against
 // measured times of every tile shape (128 x {64,128,256} on one CTA, 256 x 256
-// on a CTA pair) and split for 24 shapes: 23 picks are the measured best, the
-// worst is within 9%.  Persistent CTAs take units round-robin,
-// so the busiest SM runs ceil(units/SMs) units ("Matrix Multiplication
-// Background User's Guide", section 3.2, wave quantization); every unit pays
-// for a full tile whatever part of it lies inside C (section 3.1, tile
-// quantization).  A unit is bound by its tensor-core time or by how fast one
-// SM's TMA ring is fed: ~80 GB/s when its blocks come from DRAM (a single
-// wave moves through K in lockstep, so every stage waits on DRAM), faster
-// when later waves find blocks that earlier waves left in L2.  The call is
-// also bound by streaming its unique bytes from DRAM at ~60 GB/s per distinct
-// A or B panel in flight (up to ~4.9 TB/s).  Split-K adds its partials and a
-// reduction launch.
+// on a CTA pair, the 128 x 128 K pair), K split and tail split for 204
+// shapes: skinny M x {64,128,256} x {4096,8192} (M = 1024 ... 32768), the
+// 2304 x N x 4096 and 27648 x N x 4096 sweeps and 14 cubes and long-K
+// shapes.  Persistent CTAs take units round-robin, so the busiest SM runs
+// ceil(units/SMs) units ("Matrix Multiplication Background User's Guide",
+// section 3.2, wave quantization); every unit pays for a full tile whatever
+// part of it lies inside C (section 3.1, tile quantization).
+//
+// A unit walks its k-blocks through a ring of `stages` shared-memory stages.
+// A stage is refilled only after the MMAs that read it have finished, and
+// its next block then arrives after the memory latency, so one k-block costs
+// max(MMA time, (latency + MMA time) / stages): a latency-bound ring when the
+// MMAs are short (skinny shapes), the tensor pipe when they are long.  The MMA
+// rate of one SM is its own peak while few SMs run, and the GPU's sustained
+// rate (power-limited) shared by the active SMs when many do.  The call is
+// also bound by streaming its unique bytes from DRAM at ~80 GB/s per distinct
+// A or B panel in flight, up to the copy bandwidth.  Split-K adds its partials
+// (written, then read by the reduction launch) and that launch, whose threads
+// load eight slices at a time, so every further eight slices add a round of
+// memory latency.
 struct Model {
-  double peak_flops = 1.7e15;   // sustained dense bf16 rate the kernel reaches per GPU
-  double feed = 8.0e10;         // B/s one SM's ring receives from DRAM
-  double reuse_gain = 0.25;      // feed speed-up at full cross-wave L2 reuse
-  double stream_bw = 4.9e12;    // B/s DRAM rate reachable by TMA box streams
-  double panel_bw = 5.0e10;     // B/s of one streamed panel
-  double hbm_bw = 6.8e12;       // B/s, copy bandwidth
-  double fixed = 3.0e-6;        // launch, pipeline fill and last epilogue
-  double reduce = 6.0e-6;       // split-K reduction launch and tail
+  double peak_flops = 2.0e15;   // dense bf16 rate with every SM busy (power-limited)
+  double peak_sm = 1.5e13;      // dense bf16 rate of one SM when the power limit does not bind
+  double latency = 2.1e-6;      // from a stage's release to its next block's arrival, under load
+  double stream_bw = 6.8e12;    // B/s DRAM rate reachable by TMA box streams (copy bandwidth)
+  double panel_bw = 8.0e10;     // B/s of one streamed panel
+  double part_bw = 4.5e12;      // B/s at which split-K partials are written and read back
+  double fixed = 6.0e-6;        // launch, pipeline fill and last epilogue
+  double wave = 3.0e-6;         // each further wave of units (refill after an epilogue)
+  double reduce = 7.0e-6;       // split-K reduction launch and tail
+  double reduce_round = 1.0e-6; // each further 8 K slices: the reduction's next round of dependent loads
   double fused = 4.5e-6;        // split-K reduced in the GEMM kernel (opt-in): arrival wait and tail
   double l2_bw = 1.0e13;        // B/s of the partials' round trip through L2 in that case
 };
@@ -272,10 +282,10 @@ bool fused_enabled() {
   return v && *v && std::atoi(v) != 0;
 }
 
-double tile_efficiency(int bn) { return bn >= 256 ? 1.0 : (bn >= 128 ? 0.85 : 0.5); }
+double tile_efficiency(int bn) { return bn >= 128 ? 1.0 : 0.5; }
 
 // Extra fixed cost of a CTA-pair (cluster) launch, fitted on GB300.
-constexpr double kPairFixed = 8.0e-6;
+constexpr double kPairFixed = 6.0e-6;
 // Cost of a K pair's on-chip exchange per 64-column round (bn/128 rounds):
 // 32 KB of fp32 partials each way between two SMs (distributed shared memory
 // moves ~15-27 GB/s per SM each way); fitted on GB300 to the K pair against
@@ -304,21 +314,31 @@ void distinct_panels(int64_t mb, int64_t nb, int64_t group, int64_t count, int64
   *db += dn;
 }
 
+// One k-block of one unit: the MMAs of a 128 x bn tile (a pair's SM does the
+// flops of 128 x bn as well) at the rate one SM gets while `active_sms` SMs
+// run, or, when the ring waits on memory, the latency plus those MMAs spread
+// over the ring's stages.
+double kblock_time(int bn, int mode, int eb, int sms, int64_t active_sms, const Model& md) {
+  const double scale = eb == 4 ? 0.5 : 1.0;  // TF32 runs at half the 16-bit rate
+  const double rate = std::min(md.peak_sm * scale, md.peak_flops * scale / double(std::max<int64_t>(1, active_sms)));
+  const double t_mma = 2.0 * dg::TC_BM * bn * double(128 / eb) / (rate * tile_efficiency(bn));
+  const int stages = std::max(1, dg::tc_stages(bn, mode));
+  return std::max(t_mma, (md.latency + t_mma) / stages);
+}
+
 // eb: operand element bytes (2: bf16/fp16, 4: TF32, whose tensor-core rate is
 // half of the 16-bit one); a k-block is one 128-byte row of every operand.
 double estimate(int64_t M, int64_t N, int64_t K, int bn, int mode, int splitk, int sms, int c_es,
                 bool beta, int raster_group, const Model& md, int* splitk_eff, int eb) {
   const bool pair = mode == dg::TC_PAIR, kpair = mode == dg::TC_KPAIR;
   const int kbe = 128 / eb;
-  const double peak = md.peak_flops * (eb == 4 ? 0.5 : 1.0);
   const int64_t kb = ceil_div(K, kbe);
   const int64_t kbps = ceil_div(kb, splitk);
   const int s_eff = int(ceil_div(kb, kbps));
   *splitk_eff = s_eff;
   // A pair unit (256 x bn) runs on two SMs; each SM stages 128 rows of A and
-  // bn/2 columns of B per k-block and does the flops of a 128 x bn tile, so it
-  // needs a third less feed per flop than a one-CTA 128 x 256 tile.  A K-pair
-  // tile is two CTA units (its K halves) that run side by side.
+  // bn/2 columns of B per k-block and does the flops of a 128 x bn tile.  A
+  // K-pair tile is two CTA units (its K halves) that run side by side.
   const int tile_m = pair ? 2 * dg::TC_BM : dg::TC_BM;
   const int slots = pair ? sms / 2 : sms;
   const int64_t mb = ceil_div(M, tile_m), nb = ceil_div(N, bn);
@@ -336,14 +356,11 @@ double estimate(int64_t M, int64_t N, int64_t K, int bn, int mode, int splitk, i
     distinct_panels(mb, nb, group, active, &da, &db);
   }
   int64_t streams = da + db;
-  const double t_mma = 2.0 * dg::TC_BM * bn * double(kbps * kbe) / (peak / sms * tile_efficiency(bn));
-  const double unit_bytes = double(dg::TC_BM + (pair ? bn / 2 : bn)) * double(kbps) * 128.0;
+  const int64_t active_sms = pair ? 2 * active : active;
+  const double makespan = waves * double(kbps) * kblock_time(bn, mode, eb, sms, active_sms, md) + md.fixed +
+                          (waves - 1.0) * md.wave + (pair ? kPairFixed : 0.0) +
+                          (kpair ? kKPairRound * (bn / 128) * waves : 0.0);
   const double unique = double(M * K + K * N) * eb;
-  const double reuse = (1.0 - 1.0 / waves) *
-                       std::max(0.0, 1.0 - unique / (double(units) * (pair ? 2 : 1) * unit_bytes));
-  const double feed = md.feed * (1.0 + md.reuse_gain * reuse);
-  const double makespan = waves * std::max(t_mma, unit_bytes / feed) + md.fixed +
-                          (pair ? kPairFixed : 0.0) + (kpair ? kKPairRound * (bn / 128) * waves : 0.0);
   double bytes = unique + double(M) * N * c_es * (beta ? 2.0 : 1.0);
   double t = 0.0;
   if (s_eff > 1 && !kpair) {
@@ -351,8 +368,8 @@ double estimate(int64_t M, int64_t N, int64_t K, int bn, int mode, int splitk, i
     if (units <= slots && fused_enabled()) {  // reduced in the kernel, the partials stay in L2
       t += md.fused + 2.0 * part / md.l2_bw;
     } else {
-      bytes += part;                          // partials written
-      t += md.reduce + part / md.hbm_bw;      // and read back by the reduction kernel
+      bytes += part;                          // partials written, read back by the reduction kernel
+      t += md.reduce + double(ceil_div(s_eff, 8)) * md.reduce_round + part / md.part_bw;
     }
   }
   if (pair) streams *= 2;  // each CTA of a pair streams its own half of A and of B
@@ -360,11 +377,9 @@ double estimate(int64_t M, int64_t N, int64_t K, int bn, int mode, int splitk, i
   return std::max(makespan, t_mem) + t;
 }
 
-// Extra cost of a tail split's reduction over the model's split-K reduction,
-// fitted on GB300 against the tail split on and off for the 673 shapes of the
-// 2304 x N x 4096 sweep and 8192^3: with it, 250 shapes take the tail split
-// and measure faster (up to 20%), 6 take it and measure at most 1.1% slower.
-constexpr double kTailExtra = 1.0e-6;
+// Extra cost of a tail split's reduction over the model's split-K reduction
+// (fitted on GB300 with the rest of the model, tail split on and off).
+constexpr double kTailExtra = 0.0;
 
 // Whole tiles for the W = tiles / slots full waves, then the T remaining
 // tiles in S K slices each (one more wave, T*S <= slots), whose partials a
@@ -382,24 +397,18 @@ double estimate_tail(int64_t M, int64_t N, int64_t K, int bn, int mode, int S, i
   int64_t da = 0, db = 0;
   distinct_panels(mb, nb, group, std::min<int64_t>(tiles, slots), &da, &db);
   const int64_t streams = (da + db) * (pair ? 2 : 1);
-  const double rate = md.peak_flops * (eb == 4 ? 0.5 : 1.0) / sms * tile_efficiency(bn);
-  const double t_mma_full = 2.0 * dg::TC_BM * bn * double(kb * kbe) / rate;
-  const double t_mma_tail = 2.0 * dg::TC_BM * bn * double(kbps * kbe) / rate;
-  const double row_bytes = double(dg::TC_BM + (pair ? bn / 2 : bn)) * 128.0;
-  const double ub_full = row_bytes * double(kb), ub_tail = row_bytes * double(kbps);
+  // every SM is busy in the full waves; the tail wave's slices fill the GPU as well
+  const double tk = kblock_time(bn, mode, eb, sms, sms, md);
+  const double makespan = double(W) * (double(kb) * tk + md.wave) + double(kbps) * tk + md.fixed +
+                          (pair ? kPairFixed : 0.0);
   const double unique = double(M * K + K * N) * eb;
-  const double waves = double(W + 1);
-  const double all_units = (double(W * slots) * ub_full + double(T * S) * ub_tail) * (pair ? 2 : 1);
-  const double reuse = (1.0 - 1.0 / waves) * std::max(0.0, 1.0 - unique / all_units);
-  const double feed = md.feed * (1.0 + md.reuse_gain * reuse);
-  const double makespan = double(W) * std::max(t_mma_full, ub_full / feed) +
-                          std::max(t_mma_tail, ub_tail / feed) + md.fixed + (pair ? kPairFixed : 0.0);
   const double part = double(S) * double(T) * tile_m * bn * 4.0;
   const bool fused = fused_enabled();  // the tail's slices are one per CTA: reduced in the kernel
   const double bytes = unique + double(M) * N * c_es * (beta ? 2.0 : 1.0) + (fused ? 0.0 : part);
   const double t_mem = bytes / std::min(md.stream_bw, md.panel_bw * double(streams));
   if (fused) return std::max(makespan, t_mem) + md.fused + 2.0 * part / md.l2_bw;
-  return std::max(makespan, t_mem) + md.reduce + kTailExtra + part / md.hbm_bw;
+  return std::max(makespan, t_mem) + md.reduce + double(ceil_div(S, 8)) * md.reduce_round + kTailExtra +
+         part / md.part_bw;
 }
 
 int env_int(const char* name, int dflt) {
