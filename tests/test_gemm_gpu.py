@@ -309,14 +309,19 @@ def test_tf32_layouts_ragged(plan, ta, tb):
     assert r.info["tile_k"] == 32 and r.info["launches"] >= 1 + int(ta) + int(not tb)
 
 
-def test_tf32_tile_widths_pair_kpair_splits(plan):
+@pytest.mark.parametrize("ta,tb", [(False, True), (True, False)])
+def test_tf32_tile_widths_pair_kpair_splits(plan, ta, tb):
+    """Every tile mode with K-major TF32 operands and with both operands
+    M/N-major (A stored K x M, B stored K x N, both transposed into
+    workspace first)."""
     envs = [{"GEMM_FORCE_TILE": "128x64"}, {"GEMM_FORCE_TILE": "128x128"}, {"GEMM_FORCE_TILE": "128x256"},
             {"GEMM_FORCE_TILE": "256x256"}, {"GEMM_SPLITK_CLUSTER": "1", "GEMM_FORCE_SPLITK": "2"},
             {"GEMM_FORCE_SPLITK": "5", "GEMM_SPLITK_CLUSTER": "0"},
             {"GEMM_TAIL_SPLIT": "3", "GEMM_FORCE_TILE": "128x128"}]
     for env in envs:
         M, N = (1300, 2000) if "GEMM_TAIL_SPLIT" in env else (257, 300)
-        run_case(plan, M, N, 515, in_fmt="tf32", tb=True, beta=0.5, act=1, slope=0.1, env=env, seed=150)
+        run_case(plan, M, N, 515, in_fmt="tf32", ta=ta, tb=tb, beta=0.5, act=1, slope=0.1, env=env,
+                 seed=150 + ta)
 
 
 def test_tf32_gemv_shapes_and_edges(plan):
