@@ -3,7 +3,11 @@
 Each translation unit is compiled in parallel into ``_build/`` and linked
 into ``dense_gemm_mma_gb300/libdgemm_gb300.so`` with the CUDA runtime linked
 statically, so the library loads on a machine without a GPU (the entry points
-then report GEMM_ERR_NO_DEVICE).
+then report GEMM_ERR_NO_DEVICE).  ``build(debug=True)`` compiles the same
+sources with DG_DEBUG into ``_build_debug/`` and
+``dense_gemm_mma_gb300/libdgemm_gb300_debug.so``: every kernel then checks its
+plain global accesses and TMA coordinates on the device and reports a failed
+check through the plan's error word (include/gemm.h, gemm_debug_build).
 """
 from __future__ import annotations
 
@@ -19,6 +23,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libdgemm_gb300.so")
+LIB_DEBUG = os.path.join(PKG, "libdgemm_gb300_debug.so")
 
 SOURCES = [
     "api.cpp",
@@ -52,15 +57,18 @@ def _newest_input() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    lib = LIB_DEBUG if debug else LIB
+    build_dir = BUILD + "_debug" if debug else BUILD
+    flags = FLAGS + (["-DDG_DEBUG"] if debug else [])
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _newest_input():
+        return lib
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
+        cmd = [nvcc, *ARCH, *flags, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose and src.endswith(".cu"):
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -72,14 +80,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -78,7 +78,8 @@ struct TcEntry {
 struct gemm_plan {
   int device = 0;
   int sms = 0;
-  int* err = nullptr;  // device word, OR of wait codes
+  int* err = nullptr;  // device word, OR of wait codes (and, debug build, failed-check sites)
+  int64_t last_err_bits = 0;  // the word the last gemm_plan_poll_error read
   void* ws = nullptr;  // workspace (split-K partials, GEMV partials)
   size_t ws_bytes = 0;
   unsigned* counters = nullptr;  // GEMV per-panel arrival counters: zero between calls
@@ -139,6 +140,53 @@ struct Region {
 Region region(const void* p, int64_t rows, int64_t cols, int64_t ld, int64_t esize) {
   return Region{uint64_t(reinterpret_cast<uintptr_t>(p)), rows, ld * esize, cols * esize};
 }
+
+// Byte ranges of a call's buffers for the debug build's device checks
+// (kernels.h, DbgSpans).  The release build passes them to no kernel.
+// GEMM_DEBUG_SHRINK=n (read by the debug build only, for its tests) makes the
+// output's range n bytes shorter, so that the checks of the last output
+// elements fail while every access stays inside the caller's buffer.
+struct Spans {
+  dg::DbgSpans s{};
+  int n = 0;
+  explicit Spans(int* err) { s.err = err; }
+  Spans& bytes(const void* p, int64_t len) {
+    if (p != nullptr && len > 0 && n < dg::kDbgSpans) {
+      s.lo[n] = uint64_t(reinterpret_cast<uintptr_t>(p));
+      s.hi[n] = s.lo[n] + uint64_t(len);
+      ++n;
+    }
+    return *this;
+  }
+  // rows x cols elements of esize bytes, rows ld elements apart
+  Spans& matrix(const void* p, int64_t rows, int64_t cols, int64_t ld, int64_t esize) {
+    if (rows <= 0 || cols <= 0) return *this;
+    return bytes(p, ((rows - 1) * ld + cols) * esize);
+  }
+  // count elements of esize bytes, inc elements apart
+  Spans& vector(const void* p, int64_t count, int64_t inc, int64_t esize) {
+    return count > 0 ? bytes(p, ((count - 1) * inc + 1) * esize) : *this;
+  }
+  // the output: its range less GEMM_DEBUG_SHRINK bytes
+  Spans& out_matrix(const void* p, int64_t rows, int64_t cols, int64_t ld, int64_t esize) {
+    const int at = n;
+    matrix(p, rows, cols, ld, esize);
+    return shrink(at);
+  }
+  Spans& out_vector(const void* p, int64_t count, int64_t inc, int64_t esize) {
+    const int at = n;
+    vector(p, count, inc, esize);
+    return shrink(at);
+  }
+  Spans& shrink(int at) {
+    static const int64_t cut = [] {
+      const char* v = std::getenv("GEMM_DEBUG_SHRINK");
+      return v ? std::max<int64_t>(0, std::atoll(v)) : int64_t(0);
+    }();
+    if (at < n) s.hi[at] -= std::min<uint64_t>(uint64_t(cut), s.hi[at] - s.lo[at]);
+    return *this;
+  }
+};
 
 // Do two matrices share a byte?  Row i of x and row k of y meet iff y's row
 // starts before x's ends and ends after x's starts: -wy < d + k*Ly - i*Lx < wx
@@ -730,12 +778,26 @@ gemm_status_t run_gemv(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const v
     g.w_cs = row_major_w ? 1 : ldb;
   }
   const bool vec_ok = aligned(g.W, 16) && (g.ldw * 2) % 16 == 0;
+  // (debug build) the output, beta's C, the matrix and the vector; the plan's
+  // workspace and counters once they exist
+  auto set_spans = [&]() {
+#ifdef DG_DEBUG
+    Spans sp(plan->err);
+    sp.out_vector(C, g.R, g.inc_out, e.out_kind == dg::OUT_F32 ? 4 : 2);
+    if (e.beta != 0.f) sp.vector(g.cin, g.R, g.inc_cin, e.cin_kind == dg::OUT_F32 ? 4 : 2);
+    sp.matrix(g.W, row_major_w ? g.R : K, row_major_w ? K : g.R, g.ldw, 2);
+    sp.vector(g.x, K, g.incx, 2);
+    sp.bytes(plan->ws, int64_t(plan->ws_bytes)).bytes(plan->counters, int64_t(plan->counter_count) * 4);
+    g.dbg = sp.s;
+#endif
+  };
   cudaError_t err;
   info->path = GEMM_PATH_GEMV_GENERIC;
   info->splitk = 1;
   info->launches = 1;
   if (row_major_w && (vec_ok || g.R == 1) && aligned(g.W, 16) && K <= dg::gemv_rowdot_max_k()) {
     info->path = GEMM_PATH_GEMV_ROWDOT;
+    set_spans();
     err = dg::launch_gemv_rowdot(g, s, plan->sms, &info->grid);
   } else if (!row_major_w && (vec_ok || K == 1) && aligned(g.W, 16)) {
     const dg::ColstreamPlan cp = dg::plan_gemv_colstream(g.R, g.K, plan->sms);
@@ -748,8 +810,10 @@ gemm_status_t run_gemv(gemm_plan* plan, int64_t M, int64_t N, int64_t K, const v
     info->splitk = cp.ksplit;
     info->grid = cp.panels * cp.ksplit;
     info->workspace_bytes = cp.ws_bytes;
+    set_spans();
     err = dg::launch_gemv_colstream(g, cp, plan->ws, plan->counters, s);
   } else {
+    set_spans();
     err = dg::launch_gemv_generic(g, s, plan->sms, &info->grid);
   }
   return err == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
@@ -881,6 +945,15 @@ gemm_status_t launch_entry(gemm_plan* plan, TcEntry* e, int64_t M, int64_t N, vo
       e->ws_ptr = plan->ws;
     }
   }
+#ifdef DG_DEBUG
+  {  // what the kernels touch with plain or bulk accesses: the output, beta's C, workspace, counters
+    Spans sp(plan->err);
+    sp.out_matrix(C, M, N, ldc, p.out_kind == dg::OUT_F32 ? 4 : 2);
+    if (beta != 0.f) sp.matrix(p.cin, M, N, p.ldcin, p.cin_kind == dg::OUT_F32 ? 4 : 2);
+    if (tail > 0) sp.bytes(plan->ws, int64_t(plan->ws_bytes)).bytes(plan->counters, int64_t(plan->counter_count) * 4);
+    p.dbg = sp.s;
+  }
+#endif
   if (dg::launch_gemm_tc(e->info.tile_n, mode, e->ma, e->mb, e->mc, e->mw, p, e->info.grid, s) !=
       cudaSuccess)
     return GEMM_ERR_CUDA;
@@ -903,6 +976,9 @@ gemm_status_t launch_entry(gemm_plan* plan, TcEntry* e, int64_t M, int64_t N, vo
     r.ldcin = e->p.ldcin;
     r.e = dg::EpiParams{alpha, beta, epi.slope, epi.act, out_kind(dtype), e->p.cin_kind};
     r.pdl = plan->pdl;
+#ifdef DG_DEBUG
+    r.dbg = p.dbg;
+#endif
     if (dg::launch_tile_reduce(r, s, plan->sms) != cudaSuccess) return GEMM_ERR_CUDA;
   }
   return GEMM_OK;
@@ -1041,6 +1117,7 @@ const char* gemm_status_string(gemm_status_t st) {
     case GEMM_ERR_OUT_OF_MEMORY: return "GEMM_ERR_OUT_OF_MEMORY: workspace allocation failed";
     case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: CUDA call or kernel launch failed";
     case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: a kernel wait ran out (watchdog)";
+    case GEMM_ERR_DEBUG_CHECK: return "GEMM_ERR_DEBUG_CHECK: a kernel's bounds or copy-rule check failed (debug build)";
   }
   return "unknown gemm_status_t";
 }
@@ -1168,7 +1245,16 @@ gemm_status_t run_all(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, const v
   if (K == 0 || alpha == 0.f) {
     info.path = GEMM_PATH_SCALE;
     info.launches = 1;
-    r = dg::launch_scale(int(M), int(N), D, ldd, cin.ptr, cin.ld, e, s, plan->sms) == cudaSuccess
+    dg::DbgSpans dbg{};
+#ifdef DG_DEBUG
+    {
+      Spans sp(plan->err);
+      sp.out_matrix(D, M, N, ldd, e.out_kind == dg::OUT_F32 ? 4 : 2);
+      if (beta != 0.f) sp.matrix(cin.ptr, M, N, cin.ld, cin.kind == dg::OUT_F32 ? 4 : 2);
+      dbg = sp.s;
+    }
+#endif
+    r = dg::launch_scale(int(M), int(N), D, ldd, cin.ptr, cin.ld, e, s, plan->sms, dbg) == cudaSuccess
             ? GEMM_OK
             : GEMM_ERR_CUDA;
   } else if ((M == 1 || N == 1) && !in_is_tf32(dtype)) {
@@ -1187,13 +1273,21 @@ gemm_status_t run_all(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, const v
     if (r == GEMM_OK && a_bytes) {  // A stored K x M -> M x K
       A2 = static_cast<char*>(plan->tws) + a_off;
       lda2 = lda_t;
-      if (dg::launch_transpose32(A, lda, int(K), int(M), const_cast<void*>(A2), lda2, s) != cudaSuccess)
+      dg::DbgSpans dbg{};
+#ifdef DG_DEBUG
+      dbg = Spans(plan->err).matrix(A, K, M, lda, 4).matrix(A2, M, K, lda2, 4).s;
+#endif
+      if (dg::launch_transpose32(A, lda, int(K), int(M), const_cast<void*>(A2), lda2, s, dbg) != cudaSuccess)
         r = GEMM_ERR_CUDA;
     }
     if (r == GEMM_OK && b_bytes) {  // B stored K x N -> N x K
       B2 = static_cast<char*>(plan->tws) + b_off;
       ldb2 = ldb_t;
-      if (dg::launch_transpose32(B, ldb, int(K), int(N), const_cast<void*>(B2), ldb2, s) != cudaSuccess)
+      dg::DbgSpans dbg{};
+#ifdef DG_DEBUG
+      dbg = Spans(plan->err).matrix(B, K, N, ldb, 4).matrix(B2, N, K, ldb2, 4).s;
+#endif
+      if (dg::launch_transpose32(B, ldb, int(K), int(N), const_cast<void*>(B2), ldb2, s, dbg) != cudaSuccess)
         r = GEMM_ERR_CUDA;
     }
     if (r == GEMM_OK)
@@ -1267,12 +1361,27 @@ gemm_status_t gemm_plan_poll_error(gemm_plan_t plan, void* stream) {
   }
   int h = 0;
   if (cudaMemcpy(&h, plan->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return GEMM_ERR_CUDA;
+  plan->last_err_bits = h;
   if (h == 0) return GEMM_OK;
   if (cudaMemset(plan->err, 0, sizeof(int)) != cudaSuccess) return GEMM_ERR_CUDA;
   // A kernel that gave up may have left arrival counters above zero.
   if (plan->counters && cudaMemset(plan->counters, 0, plan->counter_count * sizeof(unsigned)) != cudaSuccess)
     return GEMM_ERR_CUDA;
-  return GEMM_ERR_TIMEOUT;
+  return (h & dg::DBG_FLAG) ? GEMM_ERR_DEBUG_CHECK : GEMM_ERR_TIMEOUT;
+}
+
+gemm_status_t gemm_plan_last_error_bits(gemm_plan_t plan, int64_t* bits) {
+  if (!plan || !bits) return GEMM_ERR_INVALID_ARG;
+  *bits = plan->last_err_bits;
+  return GEMM_OK;
+}
+
+int gemm_debug_build(void) {
+#ifdef DG_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 gemm_status_t gemm_plan_set_watchdog(gemm_plan_t plan, uint64_t timeout_ns) {

@@ -161,6 +161,9 @@ __device__ __forceinline__ float4 load_cin4(const TcParams& p, int row, int col)
   if (row < p.M && col < p.N) {
     const int es = p.cin_kind == OUT_F32 ? 4 : 2;
     const uint8_t* src = static_cast<const uint8_t*>(p.cin) + (int64_t(row) * p.ldcin + col) * es;
+#ifdef DG_DEBUG
+    if (!DG_IN(p.dbg, src, min(4, p.N - col) * es, DBG_EPI_LOAD)) return make_float4(0.f, 0.f, 0.f, 0.f);
+#endif
     if (col + 4 <= p.N && (reinterpret_cast<uintptr_t>(src) & uintptr_t(4 * es - 1)) == 0) {
       if (es == 4) return *reinterpret_cast<const float4*>(src);
       const uint2 w = *reinterpret_cast<const uint2*>(src);
@@ -289,10 +292,17 @@ struct Fin {
   int M, N;
   float alpha, beta, slope;
   int act;
+#ifdef DG_DEBUG
+  const DbgSpans* dbg;
+#endif
 };
 
 __device__ __forceinline__ Fin fin_of(const TcParams& p) {
+#ifdef DG_DEBUG
+  return Fin{p.cin, p.ldcin, p.cin_kind, p.c_ptr, p.ldc, p.out_kind, p.M, p.N, p.alpha, p.beta, p.slope, p.act, &p.dbg};
+#else
   return Fin{p.cin, p.ldcin, p.cin_kind, p.c_ptr, p.ldc, p.out_kind, p.M, p.N, p.alpha, p.beta, p.slope, p.act};
+#endif
 }
 
 // The four values of the C that beta scales at (row, col .. col+3), zero
@@ -303,6 +313,9 @@ __device__ __forceinline__ float4 fin_c4(const Fin& f, int row, int col) {
     const int nn = min(4, f.N - col);
     const int es = f.cin_kind == OUT_F32 ? 4 : 2;
     const uint8_t* src = static_cast<const uint8_t*>(f.cin) + (int64_t(row) * f.ldcin + col) * es;
+#ifdef DG_DEBUG
+    if (!DG_IN(*f.dbg, src, nn * es, DBG_SPLIT)) return make_float4(0.f, 0.f, 0.f, 0.f);
+#endif
     if (nn == 4 && (reinterpret_cast<uintptr_t>(src) & uintptr_t(4 * es - 1)) == 0) {
       if (es == 4) return *reinterpret_cast<const float4*>(src);
       const uint2 w = *reinterpret_cast<const uint2*>(src);
@@ -406,6 +419,9 @@ __device__ __forceinline__ void fused_split_reduce(const TcParams& p, int tile, 
   const int f0 = min(F, part * share), f1 = min(F, f0 + share);
   const uint32_t share_bytes = uint32_t(f1 - f0) * 16u;
   const int splits = parts / (TILE_M / TC_BM);
+#ifdef DG_DEBUG
+  if (!DG_IN(p.dbg, cnt, 4, DBG_SPLIT)) return;  // (the peers' waits for this part run out)
+#endif
   if (ept < 32) {
     if (lane == 0) {
       __threadfence();
@@ -416,7 +432,9 @@ __device__ __forceinline__ void fused_split_reduce(const TcParams& p, int tile, 
         if (share_bytes > 0) {
           const int64_t slice = int64_t(tail_tiles) * TILE_M * BN;
           const float* src = ws + int64_t(tile) * TILE_M * BN + int64_t(f0) * 4;
-          for (int sl = 0; sl < splits; ++sl) bulk_load_1d(ring + sl * share_bytes, src + sl * slice, share_bytes, bar);
+          for (int sl = 0; sl < splits; ++sl)
+            if (DG_IN(p.dbg, src + sl * slice, share_bytes, DBG_SPLIT))
+              bulk_load_1d(ring + sl * share_bytes, src + sl * slice, share_bytes, bar);
         }
       }
     }
@@ -493,10 +511,12 @@ __device__ __forceinline__ void fused_split_reduce(const TcParams& p, int tile, 
     const int a_hi = max(a_lo, g_hi / epb * epb);
     uint8_t* const crow = static_cast<uint8_t*>(fin.c) + int64_t(row) * fin.ldc * es;
     auto src_of = [&](int g) { return out + uint32_t(r * BN + (g - n_blk * BN) - e0) * uint32_t(es); };
-    if (a_lo < a_hi) bulk_store_1d(crow + int64_t(a_lo) * es, src_of(a_lo), uint32_t(a_hi - a_lo) * uint32_t(es));
+    if (a_lo < a_hi && DG_IN(p.dbg, crow + int64_t(a_lo) * es, int64_t(a_hi - a_lo) * es, DBG_SPLIT))
+      bulk_store_1d(crow + int64_t(a_lo) * es, src_of(a_lo), uint32_t(a_hi - a_lo) * uint32_t(es));
     for (int g = g_lo; g < g_hi; ++g) {  // the unaligned ends, element by element
       if (g == a_lo) g = a_hi;
       if (g >= g_hi) break;
+      if (!DG_IN(p.dbg, crow + int64_t(g) * es, es, DBG_SPLIT)) continue;
       if (es == 4)
         *reinterpret_cast<uint32_t*>(crow + int64_t(g) * 4) = ld_shared_u32(src_of(g));
       else
@@ -592,6 +612,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
     if constexpr (PAIR) fbc = mapa_shared(fb, 0);
     if (leader) mbar_arrive_expect_tx(fb, (PAIR ? 2 : 1) * (Cfg::A_STAGE + Cfg::B_STAGE));
     auto load = [&](uint32_t dst, const CUtensorMap* m, int cx, int cy) {
+      if (!DG_TMA(p.dbg, cx, cy, TF32 ? 4 : 2, false)) return;  // (its barrier never completes)
       if constexpr (PAIR)
         tma_load_2d_pair(dst, m, fbc, cx, cy);
       else
@@ -878,14 +899,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             if (tail_lo < tail_hi && row < p.M) {
               for (int col = tail_lo; col < tail_hi; ++col) {
                 const int b = (col - x0) * 4;
-                *reinterpret_cast<float*>(static_cast<uint8_t*>(p.c_ptr) + (int64_t(row) * p.ldc + col) * 4) =
-                    *reinterpret_cast<const float*>(row_p + (((b >> 4) ^ sw) << 4) + (b & 15));
+                uint8_t* const dst = static_cast<uint8_t*>(p.c_ptr) + (int64_t(row) * p.ldc + col) * 4;
+                if (!DG_IN(p.dbg, dst, 4, DBG_EPI_STORE)) continue;
+                *reinterpret_cast<float*>(dst) = *reinterpret_cast<const float*>(row_p + (((b >> 4) ^ sw) << 4) + (b & 15));
               }
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              if (x0 < p.n_tma) tma_store_2d(&tmC, stg0 + c * Cfg::STG_BYTES, x0, y0);
+              if (x0 < p.n_tma && DG_TMA(p.dbg, x0, y0, 4, true)) tma_store_2d(&tmC, stg0 + c * Cfg::STG_BYTES, x0, y0);
               bulk_commit();
             }
           }
@@ -929,14 +951,15 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           if (tail_lo < tail_hi && row < p.M) {
             for (int col = tail_lo; col < tail_hi; ++col) {
               const int b = (col - x0) * 2;
-              *reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(p.c_ptr) + (int64_t(row) * p.ldc + col) * 2) =
-                  *reinterpret_cast<const uint16_t*>(row_p + (((b >> 4) ^ sw) << 4) + (b & 15));
+              uint8_t* const dst = static_cast<uint8_t*>(p.c_ptr) + (int64_t(row) * p.ldc + col) * 2;
+              if (!DG_IN(p.dbg, dst, 2, DBG_EPI_STORE)) continue;
+              *reinterpret_cast<uint16_t*>(dst) = *reinterpret_cast<const uint16_t*>(row_p + (((b >> 4) ^ sw) << 4) + (b & 15));
             }
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
-            if (x0 < p.n_tma) tma_store_2d(&tmC, stg0, x0, y0);
+            if (x0 < p.n_tma && DG_TMA(p.dbg, x0, y0, 2, true)) tma_store_2d(&tmC, stg0, x0, y0);
             bulk_commit();
           }
         }
@@ -1030,7 +1053,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         if (V != EPI_PLAIN && c_tma && tma_cols) {
           if (lane == 0) {
             mbar_arrive_expect_tx(cload0 + 8 * e, Cfg::STG_BYTES);
-            tma_load_2d(stg, &tmC, cload0 + 8 * e, x0, y0);
+            if (DG_TMA(p.dbg, x0, y0, esize, false)) tma_load_2d(stg, &tmC, cload0 + 8 * e, x0, y0);
           }
           __syncwarp();  // the load is issued before any lane of this warp waits for it
           if (!__all_sync(0xffffffffu, wait(cload0 + 8 * e, cphase, WAIT_EPI_C_LOAD))) {
@@ -1047,6 +1070,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int b = (col - x0) * esize;
             uint8_t* dst = row_p + ((((b >> 4) ^ sw)) << 4) + (b & 15);
             const uint8_t* src = static_cast<const uint8_t*>(p.c_ptr) + (int64_t(row) * p.ldc + col) * esize;
+            if (!DG_IN(p.dbg, src, esize, DBG_EPI_LOAD)) continue;
             if (esize == 4)
               *reinterpret_cast<float*>(dst) = *reinterpret_cast<const float*>(src);
             else
@@ -1092,6 +1116,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
             const int b = (col - x0) * esize;
             const uint8_t* src = row_p + ((((b >> 4) ^ sw)) << 4) + (b & 15);
             uint8_t* dst = static_cast<uint8_t*>(p.c_ptr) + (int64_t(row) * p.ldc + col) * esize;
+            if (!DG_IN(p.dbg, dst, esize, DBG_EPI_STORE)) continue;
             if (esize == 4)
               *reinterpret_cast<float*>(dst) = *reinterpret_cast<const float*>(src);
             else
@@ -1101,7 +1126,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          if (tma_cols) tma_store_2d(out_map, stg, x0, y0);
+          if (tma_cols && DG_TMA(p.dbg, x0, y0, esize, true)) tma_store_2d(out_map, stg, x0, y0);
           bulk_commit();  // one group per chunk (possibly empty) keeps the buffer accounting exact
         }
         sbuf ^= 1;

@@ -104,6 +104,18 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Output r of a GEMV: the epilogue of acc (reading C[r * inc_cin] when beta
+// != 0) stored at out[r * inc_out].
+__device__ __forceinline__ void gemv_store(const GemvArgs& g, int64_t r, float acc) {
+  const int64_t oi = r * g.inc_out, ci = r * g.inc_cin;
+#ifdef DG_DEBUG
+  const int os = g.e.out_kind == OUT_F32 ? 4 : 2, cs = g.e.cin_kind == OUT_F32 ? 4 : 2;
+  if (g.e.beta != 0.f && !DG_IN(g.dbg, static_cast<const char*>(g.cin) + ci * cs, cs, DBG_GEMV)) return;
+  if (!DG_IN(g.dbg, static_cast<char*>(g.out) + oi * os, os, DBG_GEMV)) return;
+#endif
+  store_c(g.out, oi, epilogue(acc, g.cin, ci, g.e), g.e.out_kind);
+}
+
 // ------------------------------------------------------------------ rowdot
 // One warp per row of W (row-contiguous, 16-byte aligned rows).  Each lane
 // keeps kRowU 16-byte loads of its row in flight; registers are held to 32 a
@@ -129,15 +141,25 @@ __global__ void __launch_bounds__(kRowdotThreads, kRowdotCtasPerSm)
   const int K = g.K;
   if (!kXDirect) {
     const int K8 = (K + 7) & ~7;
-    for (int k = threadIdx.x; k < K8; k += blockDim.x) xs[k] = k < K ? x[k * g.incx] : 0;
+    for (int k = threadIdx.x; k < K8; k += blockDim.x) {
+      uint16_t v = 0;
+      if (k < K && DG_IN(g.dbg, x + static_cast<int64_t>(k) * g.incx, 2, DBG_GEMV)) v = x[k * g.incx];
+      xs[k] = v;
+    }
     __syncthreads();
   }
+#ifdef DG_DEBUG
+  if (kXDirect && !DG_IN(g.dbg, x, int64_t(K) * 2, DBG_GEMV)) return;
+#endif
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wpb = kRowdotThreads / 32;
   const int nvec = K >> 3;
   for (int r = blockIdx.x * wpb + warp; r < g.R; r += gridDim.x * wpb) {
     const uint16_t* wrow = static_cast<const uint16_t*>(g.W) + static_cast<int64_t>(r) * g.ldw;
     const uint4* wv = reinterpret_cast<const uint4*>(wrow);
+#ifdef DG_DEBUG
+    if (!DG_IN(g.dbg, wrow, int64_t(K) * 2, DBG_GEMV)) continue;  // the whole row, once per warp
+#endif
     float a0 = 0.f, a1 = 0.f;
     int v = lane;
     for (; v + 32 * (kRowU - 1) < nvec; v += 32 * kRowU) {
@@ -154,10 +176,7 @@ __global__ void __launch_bounds__(kRowdotThreads, kRowdotCtasPerSm)
     for (int k = nvec * 8 + lane; k < K; k += 32)
       a1 = fmaf(to_f<F16>(wrow[k]), to_f<F16>(kXDirect ? x[k] : xs[k]), a1);
     const float acc = warp_sum(a0 + a1);
-    if (lane == 0) {
-      store_c(g.out, static_cast<int64_t>(r) * g.inc_out,
-              epilogue(acc, g.cin, static_cast<int64_t>(r) * g.inc_cin, g.e), g.e.out_kind);
-    }
+    if (lane == 0) gemv_store(g, r, acc);
   }
 }
 
@@ -211,9 +230,20 @@ __global__ void __launch_bounds__(kColThreads, 4)
   for (int cb = kb; cb < ke; cb += kColMaxKc) {
     const int ce = min(ke, cb + kColMaxKc);
     __syncthreads();  // the previous chunk's x is no longer read
-    for (int k = cb + threadIdx.x; k < ce; k += kColThreads)
-      xsl[k - cb] = to_f<F16>(x[static_cast<int64_t>(k) * g.incx]);
+    for (int k = cb + threadIdx.x; k < ce; k += kColThreads) {
+      float xv = 0.f;
+      if (DG_IN(g.dbg, x + static_cast<int64_t>(k) * g.incx, 2, DBG_GEMV)) xv = to_f<F16>(x[static_cast<int64_t>(k) * g.incx]);
+      xsl[k - cb] = xv;
+    }
     __syncthreads();
+#ifdef DG_DEBUG
+    // this thread's strip of the chunk: 8 columns of rows cb + grp, + 8, ... < ce
+    const int k_last = cb + grp + ((ce - 1 - cb - grp) / kColGroups) * kColGroups;
+    const bool strip_ok = col0 >= g.R || cb + grp >= ce ||
+                          (DG_IN(g.dbg, W + static_cast<int64_t>(cb + grp) * g.ldw + col0, min(8, g.R - col0) * 2, DBG_GEMV) &&
+                           DG_IN(g.dbg, W + static_cast<int64_t>(k_last) * g.ldw + col0, min(8, g.R - col0) * 2, DBG_GEMV));
+    if (!strip_ok) continue;
+#endif
     if (col0 + 8 <= g.R) {
       const uint16_t* wp = W + static_cast<int64_t>(cb + grp) * g.ldw + col0;
       const int64_t step = static_cast<int64_t>(kColGroups) * g.ldw;
@@ -251,9 +281,8 @@ __global__ void __launch_bounds__(kColThreads, 4)
     for (int q = 1; q < kColGroups; ++q) s += red[q][c];
     if (col < g.R) {
       if (cp.ksplit == 1) {
-        store_c(g.out, static_cast<int64_t>(col) * g.inc_out,
-                epilogue(s, g.cin, static_cast<int64_t>(col) * g.inc_cin, g.e), g.e.out_kind);
-      } else {
+        gemv_store(g, col, s);
+      } else if (DG_IN(g.dbg, ws + static_cast<int64_t>(z) * rpad + col, 4, DBG_GEMV)) {
         ws[static_cast<int64_t>(z) * rpad + col] = s;
       }
     }
@@ -262,7 +291,10 @@ __global__ void __launch_bounds__(kColThreads, 4)
 
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) ticket = atomicAdd(&counters[panel], 1u);
+  if (threadIdx.x == 0) {
+    ticket = 0u;  // (the debug build's skipped arrival: not the last CTA)
+    if (DG_IN(g.dbg, counters + panel, 4, DBG_GEMV)) ticket = atomicAdd(&counters[panel], 1u);
+  }
   __syncthreads();
   if (ticket != static_cast<unsigned>(cp.ksplit - 1)) return;
   __threadfence();
@@ -273,10 +305,16 @@ __global__ void __launch_bounds__(kColThreads, 4)
   const int q = threadIdx.x % kQuads;
   const int h = threadIdx.x / kQuads;
   const int per = (cp.ksplit + kParts - 1) / kParts;
-  const int z0 = min(cp.ksplit, h * per), z1 = min(cp.ksplit, z0 + per);
+  const int z0 = min(cp.ksplit, h * per);
+  int z1 = min(cp.ksplit, z0 + per);
   const float* src = ws + panel * kColCols + 4 * q;
   float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
   int zz = z0;
+#ifdef DG_DEBUG
+  if (z1 > z0 && !(DG_IN(g.dbg, src + static_cast<int64_t>(z0) * rpad, 16, DBG_GEMV) &&
+                   DG_IN(g.dbg, src + static_cast<int64_t>(z1 - 1) * rpad, 16, DBG_GEMV)))
+    z1 = z0;  // skip this thread's slices
+#endif
   for (; zz + 7 < z1; zz += 8) {
     float4 v[8];
 #pragma unroll
@@ -309,10 +347,9 @@ __global__ void __launch_bounds__(kColThreads, 4)
     float s = half[c];
 #pragma unroll
     for (int part = 1; part < kParts; ++part) s += half[part * kColCols + c];
-    store_c(g.out, static_cast<int64_t>(col) * g.inc_out,
-            epilogue(s, g.cin, static_cast<int64_t>(col) * g.inc_cin, g.e), g.e.out_kind);
+    gemv_store(g, col, s);
   }
-  if (threadIdx.x == 0) counters[panel] = 0u;
+  if (threadIdx.x == 0 && DG_IN(g.dbg, counters + panel, 4, DBG_GEMV)) counters[panel] = 0u;
 }
 
 // ----------------------------------------------------------------- generic
@@ -327,14 +364,14 @@ __global__ void __launch_bounds__(256) gemv_generic_kernel(const GemvArgs g) {
   const uint16_t* x = static_cast<const uint16_t*>(g.x);
   for (int r = gw; r < g.R; r += nw) {
     float acc = 0.f;
-    for (int k = lane; k < g.K; k += 32)
-      acc = fmaf(to_f<F16>(W[static_cast<int64_t>(r) * g.w_rs + static_cast<int64_t>(k) * g.w_cs]),
-                 to_f<F16>(x[static_cast<int64_t>(k) * g.incx]), acc);
-    acc = warp_sum(acc);
-    if (lane == 0) {
-      store_c(g.out, static_cast<int64_t>(r) * g.inc_out,
-              epilogue(acc, g.cin, static_cast<int64_t>(r) * g.inc_cin, g.e), g.e.out_kind);
+    for (int k = lane; k < g.K; k += 32) {
+      const uint16_t* wp = W + static_cast<int64_t>(r) * g.w_rs + static_cast<int64_t>(k) * g.w_cs;
+      const uint16_t* xp = x + static_cast<int64_t>(k) * g.incx;
+      if (DG_IN(g.dbg, wp, 2, DBG_GEMV) && DG_IN(g.dbg, xp, 2, DBG_GEMV))
+        acc = fmaf(to_f<F16>(*wp), to_f<F16>(*xp), acc);
     }
+    acc = warp_sum(acc);
+    if (lane == 0) gemv_store(g, r, acc);
   }
 }
 
@@ -369,6 +406,10 @@ __global__ void __launch_bounds__(kReduceThreads) tile_reduce_kernel(const TileR
     const int n = n_blk * a.tile_n + c4 * 4;
     if (m >= a.M || n >= N) continue;
     const float* src = a.ws + (static_cast<int64_t>(t) * a.tile_m + r) * a.tile_n + c4 * 4;
+#ifdef DG_DEBUG
+    // the first and the last slice of these four partial sums
+    if (!DG_IN(a.dbg, src, 16, DBG_REDUCE) || !DG_IN(a.dbg, src + (a.splits - 1) * slice, 16, DBG_REDUCE)) continue;
+#endif
     float4 s = __ldcs(reinterpret_cast<const float4*>(src));
     int sp = 1;
     // slices in order, eight loads in flight before their adds (the sum is
@@ -400,9 +441,19 @@ __global__ void __launch_bounds__(kReduceThreads) tile_reduce_kernel(const TileR
                      ((reinterpret_cast<uintptr_t>(C) + base * esz) & (4 * esz - 1)) == 0;
     if (!vec) {
       const int64_t cbase = static_cast<int64_t>(m) * a.ldcin + n;
-      for (int j = 0; j < nn; ++j) store_c(C, base + j, epilogue(sv[j], a.Cin, cbase + j, e), e.out_kind);
+      for (int j = 0; j < nn; ++j) {
+#ifdef DG_DEBUG
+        const int cs = e.cin_kind == OUT_F32 ? 4 : 2;
+        if (e.beta != 0.f && !DG_IN(a.dbg, static_cast<const char*>(a.Cin) + (cbase + j) * cs, cs, DBG_REDUCE)) continue;
+        if (!DG_IN(a.dbg, static_cast<char*>(C) + (base + j) * esz, esz, DBG_REDUCE)) continue;
+#endif
+        store_c(C, base + j, epilogue(sv[j], a.Cin, cbase + j, e), e.out_kind);
+      }
       continue;
     }
+#ifdef DG_DEBUG
+    if (!DG_IN(a.dbg, static_cast<char*>(C) + base * esz, 4 * esz, DBG_REDUCE)) continue;
+#endif
     // Four adjacent outputs with one 16-byte (fp32) or 8-byte (16-bit) access.
     if (e.out_kind == OUT_F32) {
       float4* cp = reinterpret_cast<float4*>(static_cast<float*>(C) + base);
@@ -449,7 +500,7 @@ __global__ void __launch_bounds__(kReduceThreads) tile_reduce_kernel(const TileR
 constexpr int kTrTile = 64;
 __global__ void __launch_bounds__(256) transpose32_kernel(const uint32_t* __restrict__ in, int64_t ld_in,
                                                           int rows, int cols, uint32_t* __restrict__ out,
-                                                          int64_t ld_out) {
+                                                          int64_t ld_out, const DbgSpans dbg) {
   __shared__ uint32_t tile[kTrTile][kTrTile + 1];
   const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 8 rows of 32 per pass
   for (int by = blockIdx.y * kTrTile; by < rows; by += gridDim.y * kTrTile) {
@@ -460,7 +511,9 @@ __global__ void __launch_bounds__(256) transpose32_kernel(const uint32_t* __rest
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int r = by + ty + 8 * j, c = bx + tx + 32 * h;
-          v[2 * j + h] = (r < rows && c < cols) ? in[static_cast<int64_t>(r) * ld_in + c] : 0u;
+          v[2 * j + h] = (r < rows && c < cols && DG_IN(dbg, in + static_cast<int64_t>(r) * ld_in + c, 4, DBG_TRANSPOSE))
+                             ? in[static_cast<int64_t>(r) * ld_in + c]
+                             : 0u;
         }
       }
 #pragma unroll
@@ -474,7 +527,8 @@ __global__ void __launch_bounds__(256) transpose32_kernel(const uint32_t* __rest
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int r = bx + ty + 8 * j, c = by + tx + 32 * h;  // row of out = column of in
-          if (r < cols && c < rows) out[static_cast<int64_t>(r) * ld_out + c] = tile[tx + 32 * h][ty + 8 * j];
+          if (r < cols && c < rows && DG_IN(dbg, out + static_cast<int64_t>(r) * ld_out + c, 4, DBG_TRANSPOSE))
+            out[static_cast<int64_t>(r) * ld_out + c] = tile[tx + 32 * h][ty + 8 * j];
         }
       }
       __syncthreads();
@@ -484,15 +538,19 @@ __global__ void __launch_bounds__(256) transpose32_kernel(const uint32_t* __rest
 
 // ------------------------------------------------------------------- scale
 __global__ void __launch_bounds__(256) scale_kernel(int M, int N, void* D, int64_t ldd, const void* C,
-                                                    int64_t ldc, const EpiParams e) {
+                                                    int64_t ldc, const EpiParams e, const DbgSpans dbg) {
   const int64_t total = static_cast<int64_t>(M) * N;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int m = static_cast<int>(i / N);
     const int n = static_cast<int>(i - static_cast<int64_t>(m) * N);
-    float v = e.beta != 0.f ? e.beta * load_c(C, static_cast<int64_t>(m) * ldc + n, e.cin_kind) : 0.f;
+    const int cs = e.cin_kind == OUT_F32 ? 4 : 2, ds = e.out_kind == OUT_F32 ? 4 : 2;
+    const int64_t ci = static_cast<int64_t>(m) * ldc + n, di = static_cast<int64_t>(m) * ldd + n;
+    float v = e.beta != 0.f && DG_IN(dbg, static_cast<const char*>(C) + ci * cs, cs, DBG_SCALE)
+                  ? e.beta * load_c(C, ci, e.cin_kind)
+                  : 0.f;
     v = apply_act(v, e.act, e.slope);
-    store_c(D, static_cast<int64_t>(m) * ldd + n, v, e.out_kind);
+    if (DG_IN(dbg, static_cast<char*>(D) + di * ds, ds, DBG_SCALE)) store_c(D, di, v, e.out_kind);
   }
 }
 
@@ -635,21 +693,21 @@ cudaError_t launch_tile_reduce(const TileReduceArgs& a, cudaStream_t s, int sms)
 }
 
 cudaError_t launch_transpose32(const void* in, int64_t ld_in, int rows, int cols, void* out, int64_t ld_out,
-                               cudaStream_t s) {
+                               cudaStream_t s, const DbgSpans& dbg) {
   if (rows <= 0 || cols <= 0) return cudaSuccess;
   const dim3 grid(static_cast<unsigned>(std::min(65535, (cols + kTrTile - 1) / kTrTile)),
                   static_cast<unsigned>(std::min(65535, (rows + kTrTile - 1) / kTrTile)));
   transpose32_kernel<<<grid, 256, 0, s>>>(static_cast<const uint32_t*>(in), ld_in, rows, cols,
-                                          static_cast<uint32_t*>(out), ld_out);
+                                          static_cast<uint32_t*>(out), ld_out, dbg);
   return cudaGetLastError();
 }
 
 cudaError_t launch_scale(int M, int N, void* D, int64_t ldd, const void* C, int64_t ldc, EpiParams e,
-                         cudaStream_t s, int sms) {
+                         cudaStream_t s, int sms, const DbgSpans& dbg) {
   const int64_t items = static_cast<int64_t>(M) * N;
   static std::atomic<int64_t> occ{-1};
   scale_kernel<<<grid_for(items, 256, sms, resident_per_sm(scale_kernel, occ, 256, 0)), 256, 0, s>>>(
-      M, N, D, ldd, C, ldc, e);
+      M, N, D, ldd, C, ldc, e, dbg);
   return cudaGetLastError();
 }
 

@@ -15,6 +15,40 @@ enum OutKind : int {
   OUT_F16 = 2
 };
 
+// Debug build (compiled with DG_DEBUG into libdgemm_gb300_debug.so): every
+// kernel checks each plain global load and store against the byte ranges of
+// the call's own buffers (operands, output, the C that beta scales, plan
+// workspace and counters), and each TMA copy's coordinates against the copy
+// rules (innermost coordinate times the element size a multiple of 16 bytes;
+// a store starts at non-negative coordinates), before the access.  A failed
+// check skips the access and ORs DBG_FLAG and the site's bit (bit
+// DBG_SITE_SHIFT + site) into the plan's error word, where
+// gemm_plan_poll_error finds it.  A skipped TMA load never completes its
+// barrier, so the waits behind it run out and add their own codes.  The
+// release build compiles every check out.
+enum DbgSite : int {
+  DBG_TMA = 0,        // a TMA copy's coordinates break the copy rules
+  DBG_EPI_STORE = 1,  // tensor-core epilogue: plain or bulk store of outputs
+  DBG_EPI_LOAD = 2,   // tensor-core epilogue: plain load of the C that beta scales
+  DBG_SPLIT = 3,      // K slices reduced inside the tensor-core kernel: partials, counters
+  DBG_REDUCE = 4,     // tile reduction kernel
+  DBG_GEMV = 5,       // GEMV kernels: matrix, vector, output, partials, counters
+  DBG_SCALE = 6,      // the K == 0 / alpha == 0 kernel
+  DBG_TRANSPOSE = 7   // the TF32 operand transpose
+};
+constexpr int DBG_SITE_SHIFT = 16;
+constexpr int DBG_FLAG = 1 << 30;
+constexpr int kDbgSpans = 6;
+struct DbgSpans {
+  uint64_t lo[kDbgSpans], hi[kDbgSpans];  // [lo, hi) byte ranges; unused entries have lo == hi
+  int* err;                               // the plan's error word
+};
+#ifdef DG_DEBUG
+#define DG_DEBUG_FIELD DbgSpans dbg;
+#else
+#define DG_DEBUG_FIELD
+#endif
+
 // Codes OR-ed into the plan's error word by a wait that ran out.
 enum WaitCode : int {
   WAIT_PRODUCER_EMPTY = 1,
@@ -104,6 +138,7 @@ struct TcParams {
   int* err;          // plan error word
   uint64_t timeout_ns;
   int pdl;           // launch as a programmatic dependent of the stream's previous kernel
+  DG_DEBUG_FIELD     // (debug build) the byte ranges this launch may touch
 };
 
 // Shared-memory footprint and ring depth of the tensor-core kernel for a tile
@@ -135,6 +170,28 @@ cudaError_t launch_gemm_tc(int bn, int mode, const CUtensorMap& a, const CUtenso
 // memory: that returns once the previous kernel has completed and its writes
 // are visible.  In a kernel launched normally it returns at once.
 __device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Debug-build checks (see DbgSite): true when the access may go ahead.
+#ifdef DG_DEBUG
+__device__ __forceinline__ bool dbg_in(const DbgSpans& d, const void* ptr, int64_t bytes, int site) {
+  const uint64_t a = reinterpret_cast<uint64_t>(ptr);
+#pragma unroll
+  for (int i = 0; i < kDbgSpans; ++i)
+    if (a >= d.lo[i] && a + uint64_t(bytes) <= d.hi[i]) return true;
+  atomicOr(d.err, DBG_FLAG | (1 << (DBG_SITE_SHIFT + site)));
+  return false;
+}
+__device__ __forceinline__ bool dbg_tma(const DbgSpans& d, int x, int y, int esize, bool store) {
+  if ((x * esize) % 16 == 0 && (!store || (x >= 0 && y >= 0))) return true;
+  atomicOr(d.err, DBG_FLAG | (1 << (DBG_SITE_SHIFT + DBG_TMA)));
+  return false;
+}
+#define DG_IN(spans, ptr, bytes, site) ::dg::dbg_in(spans, ptr, bytes, site)
+#define DG_TMA(spans, x, y, esize, store) ::dg::dbg_tma(spans, x, y, esize, store)
+#else
+#define DG_IN(spans, ptr, bytes, site) true
+#define DG_TMA(spans, x, y, esize, store) true
+#endif
 
 // kern<<<grid, block, smem, s>>>(args...), as a programmatic dependent if pdl.
 template <typename... KArgs, typename... Args>
@@ -189,17 +246,19 @@ struct TileReduceArgs {
   int64_t ldcin;
   EpiParams e;
   int pdl;  // launch as a programmatic dependent of the GEMM that writes the partials
+  DG_DEBUG_FIELD
 };
 cudaError_t launch_tile_reduce(const TileReduceArgs& a, cudaStream_t s, int sms);
 
 // out (cols x rows, row stride ld_out) <- transpose of in (rows x cols, row
 // stride ld_in), 32-bit elements: makes a TF32 operand K-major.
 cudaError_t launch_transpose32(const void* in, int64_t ld_in, int rows, int cols, void* out, int64_t ld_out,
-                               cudaStream_t s);
+                               cudaStream_t s, const DbgSpans& dbg);
 
 // D <- act(beta * C) (K == 0 or alpha == 0); C may be D.
+// dbg: the byte ranges the kernel may touch (checked by the debug build only).
 cudaError_t launch_scale(int M, int N, void* D, int64_t ldd, const void* C, int64_t ldc, EpiParams e,
-                         cudaStream_t s, int sms);
+                         cudaStream_t s, int sms, const DbgSpans& dbg);
 
 // GEMV, operand type in_f16 (0 = bf16, 1 = fp16).
 // rowdot:    out[r*inc_out] = epi(sum_k W[r*ldw + k] * x[k*incx]),  r < R
@@ -219,6 +278,7 @@ struct GemvArgs {
   int in_f16;
   EpiParams e;
   int pdl;  // launch as a programmatic dependent of the stream's previous kernel
+  DG_DEBUG_FIELD
 };
 
 int gemv_rowdot_max_k();

@@ -122,6 +122,11 @@ extern "C" gemm_status_t gemm_gemv_noalloc(int64_t M, int64_t N, int64_t K, cons
   }
   g.cin = C;
   g.inc_cin = g.inc_out;
+#ifdef DG_DEBUG
+  // (debug build) no plan to report through: every byte range is allowed
+  g.dbg.lo[0] = 0;
+  g.dbg.hi[0] = ~uint64_t(0);
+#endif
   if (!aligned16(g.W) || ((g.ldw * 2) % 16 != 0 && K != 1)) return GEMM_ERR_UNSUPPORTED;
 
   int dev = -1;

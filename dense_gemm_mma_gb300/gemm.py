@@ -11,7 +11,10 @@ import ctypes
 import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libdgemm_gb300.so")
+# GEMM_DEBUG=1 in the environment (read at the first load) selects the debug
+# build: device-side bounds and copy-rule checks (include/gemm.h, gemm_debug_build).
+LIB_PATH = os.path.join(_PKG, "libdgemm_gb300_debug.so" if os.environ.get("GEMM_DEBUG") == "1"
+                        else "libdgemm_gb300.so")
 
 GEMM_OK = 0
 GEMM_ERR_INVALID_ARG = 1
@@ -21,6 +24,11 @@ GEMM_ERR_NO_DEVICE = 4
 GEMM_ERR_OUT_OF_MEMORY = 5
 GEMM_ERR_CUDA = 6
 GEMM_ERR_TIMEOUT = 7
+GEMM_ERR_DEBUG_CHECK = 8
+# bits of the plan's error word (gemm_plan_last_error_bits)
+DBG_FLAG = 1 << 30
+DBG_SITES = {0: "tma", 1: "epilogue_store", 2: "epilogue_load", 3: "split_in_kernel", 4: "tile_reduce",
+             5: "gemv", 6: "scale", 7: "transpose"}
 
 GEMM_OP_N, GEMM_OP_T = 0, 1
 GEMM_TYPE_BF16, GEMM_TYPE_F16, GEMM_TYPE_F32, GEMM_TYPE_TF32 = 0, 1, 2, 3
@@ -89,6 +97,8 @@ _SIGNATURES = {
     "gemm_check_args_ex": (_I32, [_I64, _I64, _I64, _VP, _I64, _VP, _I64, _VP, _I64, _I32, _VP, _I64, _I32,
                                   _F, _F, _I32, _I32, _I32, gemm_epilogue_t]),
     "gemm_plan_tuned_count": (_I32, [_VP, ctypes.POINTER(_I64)]),
+    "gemm_plan_last_error_bits": (_I32, [_VP, ctypes.POINTER(_I64)]),
+    "gemm_debug_build": (ctypes.c_int, []),
 }
 
 
@@ -159,6 +169,23 @@ def gemm_plan_last_config(plan) -> gemm_config_info_t:
 
 def gemm_plan_poll_error(plan, stream=None) -> int:
     return load().gemm_plan_poll_error(plan, stream)
+
+
+def gemm_plan_last_error_bits(plan) -> int:
+    v = _I64()
+    st = load().gemm_plan_last_error_bits(plan, ctypes.byref(v))
+    if st != GEMM_OK:
+        raise GemmError(st, "gemm_plan_last_error_bits")
+    return v.value
+
+
+def gemm_debug_build() -> int:
+    return load().gemm_debug_build()
+
+
+def debug_sites(bits: int) -> list[str]:
+    """Names of the debug-build check sites set in an error word."""
+    return [name for s, name in DBG_SITES.items() if bits & (1 << (16 + s))]
 
 
 def gemm_plan_set_watchdog(plan, timeout_ns: int) -> int:

@@ -68,7 +68,9 @@ typedef enum {
   GEMM_ERR_NO_DEVICE = 4,     /* no CUDA device, or not compute capability 10.x      */
   GEMM_ERR_OUT_OF_MEMORY = 5, /* workspace allocation failed                         */
   GEMM_ERR_CUDA = 6,          /* a CUDA runtime/driver call or a launch failed       */
-  GEMM_ERR_TIMEOUT = 7        /* a kernel's bounded wait ran out (watchdog)          */
+  GEMM_ERR_TIMEOUT = 7,       /* a kernel's bounded wait ran out (watchdog)          */
+  GEMM_ERR_DEBUG_CHECK = 8    /* debug build: a kernel's bounds or copy-rule check
+                                 failed and the access was skipped (see below)    */
 } gemm_status_t;
 
 typedef enum { GEMM_OP_N = 0, GEMM_OP_T = 1 } gemm_op_t;
@@ -255,8 +257,36 @@ gemm_status_t gemm_plan_last_config(gemm_plan_t plan, gemm_config_info_t* out);
 
 /* Wait for `stream`, then read and clear the plan's watchdog word: returns
  * GEMM_ERR_TIMEOUT if any kernel of this plan gave up on a bounded wait since
- * the last poll, GEMM_OK otherwise, GEMM_ERR_CUDA if the stream failed. */
+ * the last poll, GEMM_ERR_DEBUG_CHECK if (debug build) a device-side check
+ * failed, GEMM_OK otherwise, GEMM_ERR_CUDA if the stream failed. */
 gemm_status_t gemm_plan_poll_error(gemm_plan_t plan, void* stream);
+
+/* The word the last gemm_plan_poll_error read, before it was cleared (0:
+ * nothing happened).  Bits 0-15: the bounded waits that ran out (producer,
+ * MMA, epilogue, exchange, ...); bit 30: a debug-build check failed, and bit
+ * 16 + s for each failing site s: 0 a TMA copy's coordinates (innermost
+ * coordinate times the element size not a multiple of 16 bytes, or a store
+ * starting at a negative coordinate), 1 an epilogue store, 2 an epilogue load
+ * of the C that beta scales, 3 the in-kernel split-K reduction, 4 the tile
+ * reduction kernel, 5 a GEMV kernel, 6 the K == 0 / alpha == 0 kernel, 7 the
+ * TF32 operand transpose.  GEMM_ERR_INVALID_ARG on NULL. */
+gemm_status_t gemm_plan_last_error_bits(gemm_plan_t plan, int64_t* bits);
+
+/* 1 in the debug build of the library (libdgemm_gb300_debug.so, compiled
+ * with DG_DEBUG), 0 in the release build.  The debug build checks, on the
+ * device, every plain global load and store of every kernel against the
+ * byte ranges of the call's own buffers (operands, output, the C that beta
+ * scales, plan workspace and counters; a GEMV matrix row or a column strip
+ * as a whole) and every TMA copy's coordinates against the copy rules,
+ * before the access; a failed check skips the access (no trap, no fault)
+ * and sets the plan's error word, which gemm_plan_poll_error reports as
+ * GEMM_ERR_DEBUG_CHECK.  A skipped TMA load leaves its barrier incomplete,
+ * so the bounded waits behind it run out as well.  gemm_gemv_noalloc has no
+ * plan to report through and is not checked.  For its own tests the debug
+ * build reads GEMM_DEBUG_SHRINK=n once per process: the output's byte
+ * range is taken n bytes shorter than it is, so that the checks of the last
+ * output elements fail while every access stays inside the buffer. */
+int gemm_debug_build(void);
 
 /* Limit, in nanoseconds, of every bounded wait inside this plan's kernels
  * (default 2e9; the environment variable GEMM_WATCHDOG_NS overrides the

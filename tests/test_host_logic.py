@@ -48,9 +48,27 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for s in range(8):
+    for s in range(9):
         assert g.gemm_status_string(s).startswith("GEMM_")
+    assert "debug" in g.gemm_status_string(g.GEMM_ERR_DEBUG_CHECK)
     assert "unknown" in g.gemm_status_string(99)
+
+
+def test_debug_build_exports_the_same_symbols():
+    """The debug build (device-side checks) is the same C ABI: the same
+    exported gemm_* functions; gemm_debug_build tells the two apart."""
+    import ctypes
+    import subprocess
+    from dense_gemm_mma_gb300 import build as b
+    path = b.build(debug=True)
+    assert path.endswith("libdgemm_gb300_debug.so")
+    names = declared_functions()
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    assert sorted(set(re.findall(r" T (gemm_\w+)", out))) == names
+    dbg = ctypes.CDLL(path)  # loaded beside the release library: no call touches a device
+    assert dbg.gemm_debug_build() == 1
+    assert g.gemm_debug_build() == 0
+    assert g.debug_sites(g.DBG_FLAG | (1 << 17) | (1 << 21)) == ["epilogue_store", "gemv"]
 
 
 def test_no_device_without_gpu():
