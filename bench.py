@@ -685,10 +685,78 @@ def measure_others(args, plan, launch, flush_l2, stream, dev, torch, peaks, n_sm
             "grid": info["grid"], "waves": round(info["waves"], 3), "launches": info["launches"]})
     del bufs, host_cache
     torch.cuda.empty_cache()
+    sweeps = measure_sweeps(args, plan, launch, flush_l2, stream, dev, torch, peaks, to_dev)
     return {"timing": (f"each call alone between its own CUDA events, L2 flushed before every call, "
                        f"3 warm-up + {reps} timed calls each; median; roofline = min(measured bf16 "
                        f"burst peak, intensity x measured copy bandwidth)"),
-            "input_generation_s": round(gen_s, 1), "calls": out, "clocks": sampler.summary(t0, t1)}
+            "input_generation_s": round(gen_s, 1), "calls": out, "clocks": sampler.summary(t0, t1),
+            "sweeps": sweeps}
+
+
+def sweep_calls():
+    """Samples of the two quantization sweeps: 2304 x N x 4096 fp16 for every
+    32nd N from 1024 to 6400 (169 of the 673 shapes; the tile count per wave
+    goes through every residue), and 27648 x N x 4096 bf16 for N = 128 ... 256
+    in steps of 8 (all 17)."""
+    s3, s4 = inputs.config_seed(3), inputs.config_seed(4)
+    wave = [Call(f"wave_2304xN{n}x4096", 2304, n, 4096, in_fmt="f16", seed=s4, ldb=6400, ldc=6400)
+            for n in range(1024, 6401, 32)]
+    tile = [Call(f"tile_27648xN{n}x4096", 27648, n, 4096, seed=s3, ldb=256, ldc=256)
+            for n in range(128, 257, 8)]
+    return {"wave_2304xNx4096_f16": wave, "tile_27648xNx4096_bf16": tile}
+
+
+def measure_sweeps(args, plan, launch, flush_l2, stream, dev, torch, peaks, to_dev):
+    """Each call of each sweep sample alone between its own CUDA events, L2
+    flushed before every call, one warm-up and 5 timed calls (median); the
+    calls of a sweep share A, B (the widest N) and C.  Reported per sweep:
+    the median, the range and the fraction of the roofline, and every call's
+    time."""
+    from dense_gemm_mma_gb300 import gemm
+    out = {}
+    for name, calls in sweep_calls().items():
+        c0 = calls[0]
+        n_max = max(c.N for c in calls)
+        A = to_dev(inputs.matrix(c0.M, c0.K, c0.seed, inputs.TENSOR_A, c0.in_fmt), c0.in_fmt)
+        B = to_dev(inputs.matrix(c0.K, n_max, c0.seed, inputs.TENSOR_B, c0.in_fmt), c0.in_fmt)
+        C = torch.empty((c0.M, n_max), dtype=torch.float32, device=dev)
+        b = {"A": A, "B": B, "C": C, "C0": None}
+        reps = 5
+        ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(reps)] for _ in calls]
+        infos = []
+        for i, c in enumerate(calls):
+            flush_l2()
+            launch(c, b)
+            for r in range(reps):
+                flush_l2()
+                ev[i][r][0].record(stream)
+                info = launch(c, b)
+                ev[i][r][1].record(stream)
+            infos.append(info.as_dict())
+        torch.cuda.synchronize(dev)
+        if plan.poll_error() != gemm.GEMM_OK:
+            raise RuntimeError(f"watchdog fired in sweep {name}")
+        us = np.array([float(np.median([a.elapsed_time(z) for a, z in ev[i]])) * 1e3 for i in range(len(calls))])
+        tfl = np.array([c.flops / (u * 1e-6) / 1e12 for c, u in zip(calls, us)])
+        gbs = np.array([c.bytes / (u * 1e-6) / 1e9 for c, u in zip(calls, us)])
+        frac = []
+        for c, u in zip(calls, us):
+            ai = c.flops / c.bytes
+            att = rl.attainable(ai, tensor_peak(c, peaks) * 1e12, peaks["hbm_gbs"] * 1e9)
+            frac.append(c.flops / (u * 1e-6) / att)
+        frac = np.array(frac)
+        bound = rl.bound(c0.flops / c0.bytes, tensor_peak(c0, peaks) * 1e12, peaks["hbm_gbs"] * 1e9)
+        out[name] = {
+            "shapes": len(calls), "bound": bound, "N": [c.N for c in calls], "us": [round(float(u), 2) for u in us],
+            "tflops_median": round(float(np.median(tfl)), 1), "tflops_min": round(float(tfl.min()), 1),
+            "tflops_max": round(float(tfl.max()), 1), "gbs_median": round(float(np.median(gbs)), 1),
+            "gbs_min": round(float(gbs.min()), 1), "gbs_max": round(float(gbs.max()), 1),
+            "frac_of_roofline_median": round(float(np.median(frac)), 3),
+            "paths": {p: sum(1 for i in infos if i["path"] == p) for p in sorted({i["path"] for i in infos})}}
+        del A, B, C, b
+        torch.cuda.empty_cache()
+    return out
 
 
 def traffic_for(kernel_name: str):

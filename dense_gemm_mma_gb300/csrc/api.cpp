@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cmath>
@@ -97,6 +98,9 @@ struct gemm_plan {
   std::unordered_map<TcKey, TcEntry, TcKeyHash> tc_cache;
   // GEMM_LOG=1 (read at plan creation): one line per call on stderr.
   bool log = false;
+  // GEMM_NVTX=1 (read at plan creation): every gemm_run / gemm_run_ex is an
+  // NVTX range named after its shape and types, for profilers' timelines.
+  bool nvtx = false;
   // Benchmark mode: the fastest measured choice per shape (key without pointers).
   bool autotune = false;
   std::unordered_map<TcKey, TcChoice, TcKeyHash> tuned;
@@ -1143,6 +1147,7 @@ gemm_status_t gemm_plan_create(gemm_plan_t* plan, int device) {
   p->autotune = env_int("GEMM_AUTOTUNE", 0) != 0;
   p->pdl = env_int("GEMM_PDL", 1) != 0;
   p->log = env_int("GEMM_LOG", 0) != 0;
+  p->nvtx = env_int("GEMM_NVTX", 0) != 0;
   if (const char* w = std::getenv("GEMM_WATCHDOG_NS")) {
     const unsigned long long v = std::strtoull(w, nullptr, 10);
     if (v >= 1000) p->watchdog_ns = v;
@@ -1230,6 +1235,19 @@ gemm_status_t run_all(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, const v
                       const void* B, int64_t ldb, void* D, int64_t ldd, const CinRef& cin, float alpha,
                       float beta, gemm_dtype_t dtype, gemm_op_t transA, gemm_op_t transB,
                       gemm_epilogue_t epilogue, void* stream) {
+  struct NvtxRange {  // pops the range on every return
+    bool on;
+    ~NvtxRange() {
+      if (on) nvtxRangePop();
+    }
+  } range{plan->nvtx};
+  if (plan->nvtx) {
+    static const char* kType[] = {"bf16->f32", "bf16->bf16", "f16->f32", "f16->f16", "tf32->f32"};
+    char name[96];
+    std::snprintf(name, sizeof name, "gemm %lldx%lldx%lld %s %c%c", (long long)M, (long long)N, (long long)K,
+                  kType[int(dtype)], transA == GEMM_OP_T ? 'T' : 'N', transB == GEMM_OP_T ? 'T' : 'N');
+    nvtxRangePushA(name);
+  }
   gemm_config_info_t info{};
   info.sms = plan->sms;
   info.splitk = 1;

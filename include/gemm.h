@@ -160,7 +160,10 @@ typedef struct {
  * is not compute capability 10.x, GEMM_ERR_INVALID_ARG if plan is NULL.
  * With GEMM_LOG=1 in the environment at creation, every successful gemm_run /
  * gemm_run_ex of the plan prints one line on stderr: the shape, the types and
- * the decisions of gemm_config_info_t (gemm_choose_config does the same). */
+ * the decisions of gemm_config_info_t (gemm_choose_config does the same).
+ * With GEMM_NVTX=1 at creation, every gemm_run / gemm_run_ex of the plan is
+ * an NVTX range ("gemm MxNxK types opA opB") on the calling thread, for a
+ * profiler's timeline (no cost beyond the range calls; none without a tool). */
 gemm_status_t gemm_plan_create(gemm_plan_t* plan, int device);
 
 /* C <- act(alpha * op(A) @ op(B) + beta * C), enqueued on `stream` (a

@@ -78,3 +78,18 @@ def test_reference_tiling_matches_the_guides_tail_wave_example():
     tail = bench.ref_tiling(bench.Call("x", 2304, 1544, 4096), 108)
     assert tail["tiles"] == 117 and tail["tail_fraction"] == round(9 / 108, 4)
     assert bench.ref_tiling(bench.Call("gemv", 1, 8192, 8192), 152) is None
+
+
+def test_sweep_samples_on_the_default_line():
+    """The default bench line carries samples of both quantization sweeps:
+    every 32nd N of 2304 x N x 4096 fp16 (169 shapes, all inside the shared
+    6400-column B and C) and all 17 N of 27648 x N x 4096 bf16."""
+    import bench
+    sw = bench.sweep_calls()
+    wave, tile = sw["wave_2304xNx4096_f16"], sw["tile_27648xNx4096_bf16"]
+    assert [c.N for c in wave] == list(range(1024, 6401, 32)) and len(wave) == 169
+    assert [c.N for c in tile] == list(range(128, 257, 8)) and len(tile) == 17
+    for calls, ld in ((wave, 6400), (tile, 256)):
+        for c in calls:
+            assert c.ldb_override == ld and c.ldc_override == ld and c.N <= ld and not c.tb
+    assert {c.in_fmt for c in wave} == {"f16"} and {c.in_fmt for c in tile} == {"bf16"}

@@ -915,3 +915,19 @@ def test_full_config5_wave_sweep_points_and_splitk(plan):
     r = run_case(plan, 256, 256, 65536, in_fmt="f16", seed=1238, sample=SAMPLE, repeat=2)
     assert r.info["path"] == "tc_splitk"
     assert np.array_equal(r.outputs[0].view(np.uint8), r.outputs[1].view(np.uint8))
+
+
+def test_nvtx_ranges_do_not_change_results(monkeypatch):
+    """GEMM_NVTX=1 at plan creation wraps every call in an NVTX range; without
+    a profiler attached the ranges are inert and the results are the oracle's."""
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_gemm_mma_gb300 import gemm
+    monkeypatch.setenv("GEMM_NVTX", "1")
+    p = gemm.Plan(0)
+    try:
+        run_case(p, 300, 260, 333, seed=501)
+        run_case(p, 1, 3000, 1000, seed=502)
+    finally:
+        p.close()
