@@ -668,7 +668,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // `ld` elements between rows; boxes of box_inner x box_outer with 128-byte
 // swizzling (box_inner * esize == 128).  Out-of-range reads give zero.
 bool make_map(CUtensorMap* m, CUtensorMapDataType t, int esize, const void* ptr, int64_t inner,
-              int64_t outer, int64_t ld, int box_inner, int box_outer) {
+              int64_t outer, int64_t ld, int box_inner, int box_outer,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
@@ -676,8 +677,47 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType t, int esize, const void* ptr,
   cuuint32_t box[2] = {cuuint32_t(box_inner), cuuint32_t(box_outer)};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, t, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// TF32 operands stored M/N-major: read by the MMAs where they are (tiles
+// swizzled in 32-byte units), or first copied K-major into plan workspace?
+// Measured on GB300 (8192^3 ... 512^3, skinny and GEMV-like shapes, L2
+// flushed): in place, the MMAs of a call run ~10% longer with one such
+// operand and ~44% longer with both; a copy reads and writes the operand at
+// the copy bandwidth plus ~3 us of launch.  Each choice (copy none, the
+// smaller, or both) is estimated and the cheapest taken: copies pay off only
+// for large, compute-bound calls (8192^3 and 4096^3 with both operands
+// M/N-major).  GEMM_TF32_TRANSPOSE=1 (read at every call) copies every
+// M/N-major operand, =0 none.
+void tf32_copies(int64_t M, int64_t N, int64_t K, gemm_op_t ta, gemm_op_t tb, bool* copy_a, bool* copy_b) {
+  const bool a_mn = ta == GEMM_OP_T, b_mn = tb == GEMM_OP_N;
+  *copy_a = *copy_b = false;
+  const int force = env_int("GEMM_TF32_TRANSPOSE", -1);
+  if (force >= 0) {
+    *copy_a = a_mn && force != 0;
+    *copy_b = b_mn && force != 0;
+    return;
+  }
+  const double t_mma = 2.0 * double(M) * double(N) * double(K) / 1.0e15;  // TF32 at ~1 PFLOP/s
+  const double copy_a_t = 2.0 * double(M) * double(K) * 4.0 / 6.8e12 + 3e-6;
+  const double copy_b_t = 2.0 * double(N) * double(K) * 4.0 / 6.8e12 + 3e-6;
+  auto penalty = [&](bool a_in_place, bool b_in_place) {
+    const int n = int(a_in_place) + int(b_in_place);
+    return t_mma * (n == 2 ? 0.44 : n == 1 ? 0.10 : 0.0);
+  };
+  double best = penalty(a_mn, b_mn);
+  for (int c = 1; c < 4; ++c) {  // bit 0: copy A, bit 1: copy B
+    const bool ca = (c & 1) != 0, cb = (c & 2) != 0;
+    if ((ca && !a_mn) || (cb && !b_mn)) continue;
+    const double t = penalty(a_mn && !ca, b_mn && !cb) + (ca ? copy_a_t : 0.0) + (cb ? copy_b_t : 0.0);
+    if (t < best) {
+      best = t;
+      *copy_a = ca;
+      *copy_b = cb;
+    }
+  }
 }
 
 // tcgen05 instruction descriptor, kind::f16 with fp32 accumulation:
@@ -867,10 +907,13 @@ gemm_status_t build_tc_entry(gemm_plan* plan, int64_t M, int64_t N, int64_t K, c
                                          : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int kbe = 128 / eb;  // K elements in one 128-byte swizzle row
   const bool a_mn = ta == GEMM_OP_T, b_mn = tb == GEMM_OP_N;
-  if (tf32 && (a_mn || b_mn)) return GEMM_ERR_UNSUPPORTED;  // the caller transposes TF32 operands first
-  bool ok = a_mn ? make_map(&e->ma, in_t, eb, A, M, K, lda, 64, 64)
+  // K-major: boxes of tile rows x one 128-byte row of K; M/N-major: boxes of
+  // kbe K rows x one 128-byte row of M or N (kbe elements), swizzled in
+  // 32-byte units for TF32, as the M/N-major kind::tf32 MMAs read them
+  const CUtensorMapSwizzle mn_sw = tf32 ? CU_TENSOR_MAP_SWIZZLE_128B_ATOM_32B : CU_TENSOR_MAP_SWIZZLE_128B;
+  bool ok = a_mn ? make_map(&e->ma, in_t, eb, A, M, K, lda, kbe, kbe, mn_sw)
                  : make_map(&e->ma, in_t, eb, A, K, M, lda, kbe, dg::TC_BM);
-  ok = ok && (b_mn ? make_map(&e->mb, in_t, eb, B, N, K, ldb, 64, 64)
+  ok = ok && (b_mn ? make_map(&e->mb, in_t, eb, B, N, K, ldb, kbe, kbe, mn_sw)
                    : make_map(&e->mb, in_t, eb, B, K, N, ldb, kbe, pair ? bn / 2 : bn));
   dg::TcParams& p = e->p;
   p = dg::TcParams{};
@@ -1260,6 +1303,7 @@ gemm_status_t run_all(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, const v
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const dg::EpiParams e{alpha, beta, epilogue.slope, epilogue.act, out_kind(dtype), cin.kind};
   gemm_status_t r;
+  bool copy_a = false, copy_b = false;  // TF32 operands copied K-major first (tf32_copies)
   if (K == 0 || alpha == 0.f) {
     info.path = GEMM_PATH_SCALE;
     info.launches = 1;
@@ -1277,12 +1321,13 @@ gemm_status_t run_all(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, const v
             : GEMM_ERR_CUDA;
   } else if ((M == 1 || N == 1) && !in_is_tf32(dtype)) {
     r = run_gemv(plan, M, N, K, A, lda, B, ldb, D, ldd, dtype, transA, transB, e, cin, s, &info);
-  } else if (in_is_tf32(dtype) && (transA == GEMM_OP_T || transB == GEMM_OP_N)) {
-    // The TF32 MMAs read K-major tiles: transpose an M/N-major operand into
-    // plan workspace first (row stride rounded to 4 elements, 16 bytes).
+  } else if (in_is_tf32(dtype) && (transA == GEMM_OP_T || transB == GEMM_OP_N) &&
+             (tf32_copies(M, N, K, transA, transB, &copy_a, &copy_b), copy_a || copy_b)) {
+    // Copy the chosen M/N-major TF32 operands K-major into plan workspace
+    // (row stride rounded to 4 elements, 16 bytes); the others stay in place.
     const int64_t lda_t = (K + 3) & ~int64_t(3), ldb_t = lda_t;
-    const size_t a_bytes = transA == GEMM_OP_T ? size_t(M) * size_t(lda_t) * 4 : 0;
-    const size_t b_bytes = transB == GEMM_OP_N ? size_t(N) * size_t(ldb_t) * 4 : 0;
+    const size_t a_bytes = copy_a ? size_t(M) * size_t(lda_t) * 4 : 0;
+    const size_t b_bytes = copy_b ? size_t(N) * size_t(ldb_t) * 4 : 0;
     const size_t a_off = 0, b_off = (a_bytes + 255) & ~size_t(255);
     r = ensure_buffer(&plan->tws, &plan->tws_bytes, b_off + b_bytes, s);
     const void* A2 = A;
@@ -1309,8 +1354,8 @@ gemm_status_t run_all(gemm_plan_t plan, int64_t M, int64_t N, int64_t K, const v
         r = GEMM_ERR_CUDA;
     }
     if (r == GEMM_OK)
-      r = run_tc(plan, M, N, K, A2, lda2, B2, ldb2, D, ldd, cin, alpha, beta, dtype, GEMM_OP_N, GEMM_OP_T,
-                 epilogue, s, &info);
+      r = run_tc(plan, M, N, K, A2, lda2, B2, ldb2, D, ldd, cin, alpha, beta, dtype,
+                 copy_a ? GEMM_OP_N : transA, copy_b ? GEMM_OP_T : transB, epilogue, s, &info);
     info.launches += int(a_bytes > 0) + int(b_bytes > 0);
   } else {
     r = run_tc(plan, M, N, K, A, lda, B, ldb, D, ldd, cin, alpha, beta, dtype, transA, transB, epilogue,

@@ -537,12 +537,13 @@ __device__ __forceinline__ void fused_split_reduce(const TcParams& p, int tile, 
 // stage of the unit.
 template <bool PAIR, bool TF32>
 __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint32_t sa, uint32_t sb, uint32_t lbo_a,
-                                            uint32_t lbo_b, uint32_t kstep_a, uint32_t kstep_b, uint32_t idesc,
-                                            bool first) {
+                                            uint32_t lbo_b, uint32_t kstep_a, uint32_t kstep_b, uint32_t lay_a,
+                                            uint32_t lay_b, uint32_t idesc, bool first) {
 #pragma unroll
   for (int kk = 0; kk < TC_BK / 16; ++kk) {
-    const uint64_t ad = smem_desc_sw128(sa + kk * kstep_a, lbo_a, 1024);
-    const uint64_t bd = smem_desc_sw128(sb + kk * kstep_b, lbo_b, 1024);
+    // (32-byte swizzle atoms are four 128-byte rows deep, 16-byte ones eight)
+    const uint64_t ad = smem_desc_sw128(sa + kk * kstep_a, lbo_a, lay_a == SMEM_SW128_ATOM32 ? 512 : 1024, lay_a);
+    const uint64_t bd = smem_desc_sw128(sb + kk * kstep_b, lbo_b, lay_b == SMEM_SW128_ATOM32 ? 512 : 1024, lay_b);
     const uint32_t accum = (!first || kk > 0) ? 1u : 0u;
     if constexpr (PAIR && TF32)
       tc_mma_tf32_pair(d_tmem, ad, bd, idesc, accum);
@@ -618,17 +619,20 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
       else
         tma_load_2d(dst, m, fb, cx, cy);
     };
+    // K-major: one box of the tile's rows x one 128-byte row of K.  M/N-major:
+    // boxes of kbe K rows x kbe elements of M or N (128 bytes), one per
+    // 128-byte piece of the tile's rows, each a column of swizzle atoms.
     if (!p.a_mn_major) {
-      load(sa, &tmA, k0, m0);  // 128 rows x 64 K
-    } else {
-      load(sa, &tmA, m0, k0);  // 64 K rows x 64 M, twice
-      load(sa + 64 * 128, &tmA, m0 + 64, k0);
-    }
-    if (!p.b_mn_major) {
-      load(sb, &tmB, k0, n0);  // BNC rows x 64 K
+      load(sa, &tmA, k0, m0);  // 128 rows x kbe K
     } else {
 #pragma unroll
-      for (int j = 0; j < BNC / 64; ++j) load(sb + j * 64 * 128, &tmB, n0 + 64 * j, k0);
+      for (int j = 0; j < TC_BM / kbe; ++j) load(sa + j * kbe * 128, &tmA, m0 + kbe * j, k0);
+    }
+    if (!p.b_mn_major) {
+      load(sb, &tmB, k0, n0);  // BNC rows x kbe K
+    } else {
+#pragma unroll
+      for (int j = 0; j < BNC / kbe; ++j) load(sb + j * kbe * 128, &tmB, n0 + kbe * j, k0);
     }
   };
 
@@ -724,10 +728,19 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
-      const uint32_t lbo_a = p.a_mn_major ? 64 * 128 : 16;
-      const uint32_t lbo_b = p.b_mn_major ? 64 * 128 : 16;
-      const uint32_t kstep_a = p.a_mn_major ? 16 * 128 : 32;
-      const uint32_t kstep_b = p.b_mn_major ? 16 * 128 : 32;
+      // M/N-major operands: the next column of swizzle atoms along M or N is
+      // one box (kbe K rows of 128 bytes) further, and one MMA's K (16
+      // elements, 8 for TF32) spans that many 128-byte rows; TF32 tiles stored
+      // M/N-major are swizzled in 32-byte units.  K-major: the MMA's K is 32
+      // bytes of each row.
+      constexpr uint32_t kbe = TF32 ? TC_BK_TF32 : TC_BK;
+      constexpr uint32_t mma_k = TF32 ? 8 : 16;
+      const uint32_t lbo_a = p.a_mn_major ? kbe * 128 : 16;
+      const uint32_t lbo_b = p.b_mn_major ? kbe * 128 : 16;
+      const uint32_t kstep_a = p.a_mn_major ? mma_k * 128 : 32;
+      const uint32_t kstep_b = p.b_mn_major ? mma_k * 128 : 32;
+      const uint32_t lay_a = TF32 && p.a_mn_major ? SMEM_SW128_ATOM32 : SMEM_SW128;
+      const uint32_t lay_b = TF32 && p.b_mn_major ? SMEM_SW128_ATOM32 : SMEM_SW128;
       const uint32_t idesc = p.idesc;
       int stage = 0;
       uint32_t phase = 0;
@@ -747,7 +760,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1)
           tc_fence_after();
           const uint32_t sa = base + Cfg::OFF_A + stage * Cfg::A_STAGE;
           const uint32_t sb = base + Cfg::OFF_B + stage * Cfg::B_STAGE;
-          issue_stage<PAIR, TF32>(d_tmem, sa, sb, lbo_a, lbo_b, kstep_a, kstep_b, idesc, kb == x.kb_begin);
+          issue_stage<PAIR, TF32>(d_tmem, sa, sb, lbo_a, lbo_b, kstep_a, kstep_b, lay_a, lay_b, idesc,
+                                  kb == x.kb_begin);
           // stage free (in both CTAs of a pair) once these MMAs finish
           if constexpr (PAIR)
             tc_commit_pair_multicast(empty0 + 8 * stage, 0x3);

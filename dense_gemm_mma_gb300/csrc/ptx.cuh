@@ -304,19 +304,26 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
 //   bits  0-13 start address >> 4       bits 16-29 leading byte offset >> 4
 //   bits 32-45 stride byte offset >> 4  bits 46-47 descriptor version (1)
 //   bits 49-51 base offset (0: tiles are 1024-byte aligned)
-//   bits 61-63 layout: 2 = 128-byte swizzle
-// K-major operand (rows of 64 K-elements = 128 B, 8-row groups 1024 B apart):
-//   LBO unused (16), SBO = 1024; the k-th 16-element step starts k*32 bytes in.
-// MN-major operand (rows of 64 M/N-elements = 128 B along K, 8-row groups of
-//   K 1024 B apart, 64-wide M/N chunks `chunk_bytes` apart): LBO = chunk_bytes,
-//   SBO = 1024; the k-th 16-element step starts k*16 rows = k*2048 bytes in.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+//   bits 61-63 layout: 2 = 128-byte swizzle of 16-byte units, 1 = of 32-byte units
+// K-major operand (rows of 128 B of K-elements, 8-row groups 1024 B apart):
+//   LBO unused (16), SBO = 1024; the MMA's k-th step starts k*32 bytes in.
+// MN-major operand (rows of 128 B of M/N-elements along K, 8-row groups of
+//   K 1024 B apart, 128-byte-wide M/N chunks `chunk_bytes` apart): LBO =
+//   chunk_bytes, SBO = 1024; the k-th step starts k*(MMA K) rows in (16-bit:
+//   16 rows, 2048 bytes; TF32: 8 rows, 1024 bytes, with the 32-byte swizzle).
+// Layout types of the shared-memory descriptor (bits 61-63): 128-byte
+// swizzle of 16-byte units, and of 32-byte units (TF32 tiles stored M/N-major).
+constexpr uint32_t SMEM_SW128 = 2;
+constexpr uint32_t SMEM_SW128_ATOM32 = 1;
+
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                                    uint32_t layout = SMEM_SW128) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
   d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
+  d |= static_cast<uint64_t>(layout & 7u) << 61;
   return d;
 }
 

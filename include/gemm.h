@@ -86,7 +86,12 @@ typedef enum {
    * accumulation, C fp32 ("Matrix Multiplication Background User's Guide",
    * section 2.2, Table 1).  Every shape runs on the tensor cores, M = 1 or
    * N = 1 included.  Operands stored M/N-major (transA = T, transB = N) are
-   * first transposed into plan workspace: the TF32 MMAs read K-major tiles. */
+   * read by the MMAs where they are, except where the call is large enough
+   * that copying one or both K-major into plan workspace first is estimated
+   * faster (the in-place MMAs run ~10% longer with one such operand, ~44%
+   * with both; a copy reads and writes the operand): 8192^3, for instance.
+   * GEMM_TF32_TRANSPOSE=1 in the environment copies every M/N-major TF32
+   * operand, =0 none (read at every call). */
   GEMM_TF32_F32 = 4
 } gemm_dtype_t;
 

@@ -304,16 +304,34 @@ def test_input_slices_through_strides(plan):
 @pytest.mark.parametrize("ta,tb", [(False, True), (False, False), (True, True), (True, False)])
 def test_tf32_layouts_ragged(plan, ta, tb):
     """TF32 operands (fp32 words, low 13 fraction bits dropped) in every
-    layout; M/N-major operands are transposed into workspace first."""
+    layout; M/N-major operands are read by the MMAs where they are stored
+    (tiles swizzled in 32-byte units), so one launch unless K is split; with
+    GEMM_TF32_TRANSPOSE=1 they are first copied K-major into workspace."""
     r = run_case(plan, 300, 520, 333, in_fmt="tf32", ta=ta, tb=tb, seed=140 + 2 * ta + tb)
-    assert r.info["tile_k"] == 32 and r.info["launches"] >= 1 + int(ta) + int(not tb)
+    assert r.info["tile_k"] == 32
+    assert r.info["launches"] == (2 if r.info["path"] in ("tc_splitk", "tc_tail_split") else 1)
+    if ta or not tb:
+        r2 = run_case(plan, 300, 520, 333, in_fmt="tf32", ta=ta, tb=tb, seed=140 + 2 * ta + tb,
+                      env={"GEMM_TF32_TRANSPOSE": "1"})
+        assert r2.info["launches"] == r.info["launches"] + int(ta) + int(not tb)
+
+
+@pytest.mark.parametrize("M,N,K,copies", [(4096, 4096, 4096, 1), (8192, 128, 8192, 1), (600, 520, 700, 0)])
+def test_tf32_mn_major_operands_copied_only_where_it_pays(plan, M, N, K, copies):
+    """Both operands M/N-major (A stored K x M, B stored K x N): the MMAs read
+    them in place unless the estimated slowdown exceeds a copy; on 4096^3 the
+    estimate copies one operand, on 8192 x 128 x 8192 the small B (4 MB) and
+    reads the 268 MB A in place, and a small call copies nothing."""
+    r = run_case(plan, M, N, K, in_fmt="tf32", ta=True, tb=False, seed=155, sample=None if M * N < 10 ** 6 else 2048)
+    base = 2 if r.info["path"] in ("tc_splitk", "tc_tail_split") else 1
+    assert r.info["launches"] - base == copies, r.info
 
 
 @pytest.mark.parametrize("ta,tb", [(False, True), (True, False)])
 def test_tf32_tile_widths_pair_kpair_splits(plan, ta, tb):
     """Every tile mode with K-major TF32 operands and with both operands
-    M/N-major (A stored K x M, B stored K x N, both transposed into
-    workspace first)."""
+    M/N-major (A stored K x M, B stored K x N: four 32-element boxes per
+    128-row panel, swizzled in 32-byte units)."""
     envs = [{"GEMM_FORCE_TILE": "128x64"}, {"GEMM_FORCE_TILE": "128x128"}, {"GEMM_FORCE_TILE": "128x256"},
             {"GEMM_FORCE_TILE": "256x256"}, {"GEMM_SPLITK_CLUSTER": "1", "GEMM_FORCE_SPLITK": "2"},
             {"GEMM_FORCE_SPLITK": "5", "GEMM_SPLITK_CLUSTER": "0"},
@@ -347,8 +365,8 @@ def test_tf32_drops_the_low_fraction_bits(plan):
 
 
 def test_tf32_with_separate_c_and_benchmark_mode():
-    """TF32 operands through gemm_run_ex (bf16 C in, fp32 D out, both operand
-    layouts that need the transpose pre-pass) and under benchmark mode."""
+    """TF32 operands through gemm_run_ex (bf16 C in, fp32 D out, A stored
+    K x M and B stored K x N) and under benchmark mode."""
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
