@@ -348,7 +348,10 @@ gemm_status_t gemm_check_args_ex(int64_t M, int64_t N, int64_t K, const void* A,
 
 /* The planner of gemm_run as a pure host function: the decisions it would
  * make for this problem on a GPU with `sms` multiprocessors.  Does not need a
- * device.  Honours the GEMM_FORCE_TILE / GEMM_FORCE_SPLITK overrides. */
+ * device.  Honours the GEMM_FORCE_TILE / GEMM_FORCE_SPLITK overrides.
+ * `launches` counts the GEMM's own kernels: with TF32 operands stored
+ * M/N-major, gemm_run may launch a K-major copy of one or both first (see
+ * GEMM_TF32_F32), which its own record (gemm_plan_last_config) counts. */
 gemm_status_t gemm_choose_config(int64_t M, int64_t N, int64_t K, gemm_dtype_t dtype,
                                  gemm_op_t transA, gemm_op_t transB, int32_t sms,
                                  gemm_config_info_t* out);
