@@ -370,7 +370,7 @@ void distinct_panels(int64_t mb, int64_t nb, int64_t group, int64_t count, int64
 // flops of 128 x bn as well) at the rate one SM gets while `active_sms` SMs
 // run, or, when the ring waits on memory, the latency plus those MMAs spread
 // over the ring's stages.
-double kblock_time(int bn, int mode, int eb, int sms, int64_t active_sms, const Model& md) {
+double kblock_time(int bn, int mode, int eb, int64_t active_sms, const Model& md) {
   const double scale = eb == 4 ? 0.5 : 1.0;  // TF32 runs at half the 16-bit rate
   const double rate = std::min(md.peak_sm * scale, md.peak_flops * scale / double(std::max<int64_t>(1, active_sms)));
   const double t_mma = 2.0 * dg::TC_BM * bn * double(128 / eb) / (rate * tile_efficiency(bn));
@@ -409,7 +409,7 @@ double estimate(int64_t M, int64_t N, int64_t K, int bn, int mode, int splitk, i
   }
   int64_t streams = da + db;
   const int64_t active_sms = pair ? 2 * active : active;
-  const double makespan = waves * double(kbps) * kblock_time(bn, mode, eb, sms, active_sms, md) + md.fixed +
+  const double makespan = waves * double(kbps) * kblock_time(bn, mode, eb, active_sms, md) + md.fixed +
                           (waves - 1.0) * md.wave + (pair ? kPairFixed : 0.0) +
                           (kpair ? kKPairRound * (bn / 128) * waves : 0.0);
   const double unique = double(M * K + K * N) * eb;
@@ -450,7 +450,7 @@ double estimate_tail(int64_t M, int64_t N, int64_t K, int bn, int mode, int S, i
   distinct_panels(mb, nb, group, std::min<int64_t>(tiles, slots), &da, &db);
   const int64_t streams = (da + db) * (pair ? 2 : 1);
   // every SM is busy in the full waves; the tail wave's slices fill the GPU as well
-  const double tk = kblock_time(bn, mode, eb, sms, sms, md);
+  const double tk = kblock_time(bn, mode, eb, sms, md);
   const double makespan = double(W) * (double(kb) * tk + md.wave) + double(kbps) * tk + md.fixed +
                           (pair ? kPairFixed : 0.0);
   const double unique = double(M * K + K * N) * eb;

@@ -544,13 +544,17 @@ __global__ void __launch_bounds__(256) scale_kernel(int M, int N, void* D, int64
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int m = static_cast<int>(i / N);
     const int n = static_cast<int>(i - static_cast<int64_t>(m) * N);
-    const int cs = e.cin_kind == OUT_F32 ? 4 : 2, ds = e.out_kind == OUT_F32 ? 4 : 2;
     const int64_t ci = static_cast<int64_t>(m) * ldc + n, di = static_cast<int64_t>(m) * ldd + n;
-    float v = e.beta != 0.f && DG_IN(dbg, static_cast<const char*>(C) + ci * cs, cs, DBG_SCALE)
-                  ? e.beta * load_c(C, ci, e.cin_kind)
-                  : 0.f;
+#ifdef DG_DEBUG
+    const int cs = e.cin_kind == OUT_F32 ? 4 : 2, ds = e.out_kind == OUT_F32 ? 4 : 2;
+    const bool c_ok = DG_IN(dbg, static_cast<const char*>(C) + ci * cs, cs, DBG_SCALE);
+    if (!DG_IN(dbg, static_cast<char*>(D) + di * ds, ds, DBG_SCALE)) continue;
+#else
+    constexpr bool c_ok = true;
+#endif
+    float v = e.beta != 0.f && c_ok ? e.beta * load_c(C, ci, e.cin_kind) : 0.f;
     v = apply_act(v, e.act, e.slope);
-    if (DG_IN(dbg, static_cast<char*>(D) + di * ds, ds, DBG_SCALE)) store_c(D, di, v, e.out_kind);
+    store_c(D, di, v, e.out_kind);
   }
 }
 
