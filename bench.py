@@ -135,7 +135,8 @@ class ClockSampler:
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "clocks.mem,temperature.gpu")
 
     def __init__(self, gpu_index: int):
         self.samples = []
@@ -173,10 +174,16 @@ class ClockSampler:
         def parse(s):
             p = [x.strip() for x in s.split(",")]
             try:
-                return {"sm": float(p[1]), "max": float(p[2]), "power": float(p[3]),
-                        "hw_slowdown": p[5], "hw_thermal": p[6], "sw_thermal": p[7], "sw_power": p[8]}
+                r = {"sm": float(p[1]), "max": float(p[2]), "power": float(p[3]),
+                     "hw_slowdown": p[5], "hw_thermal": p[6], "sw_thermal": p[7], "sw_power": p[8]}
             except (ValueError, IndexError):
                 return None
+            for key, i in (("mem", 9), ("temp", 10)):  # (absent or "N/A" on some drivers)
+                try:
+                    r[key] = float(p[i])
+                except (ValueError, IndexError):
+                    r[key] = None
+            return r
         rows = [(t, parse(s)) for t, s in self.samples]
         rows = [(t, r) for t, r in rows if r is not None]
         if not rows:
@@ -193,8 +200,12 @@ class ClockSampler:
                               ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
                 if r[key].lower() == "active":
                     reasons.add(name)
+        mem = [r["mem"] for r in inside if r["mem"] is not None]
+        temp = [r["temp"] for r in inside if r["temp"] is not None]
         return {"sm_mhz": statistics.median(r["sm"] for r in inside),
                 "sm_max_mhz": max(r["max"] for r in inside),
+                "mem_mhz": statistics.median(mem) if mem else None,
+                "gpu_temp_c_max": max(temp) if temp else None,
                 "power_w_max": max(r["power"] for r in inside),
                 "reasons": sorted(reasons), "samples": len(inside), "note": note}
 

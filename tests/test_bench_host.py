@@ -93,3 +93,21 @@ def test_sweep_samples_on_the_default_line():
         for c in calls:
             assert c.ldb_override == ld and c.ldc_override == ld and c.N <= ld and not c.tb
     assert {c.in_fmt for c in wave} == {"f16"} and {c.in_fmt for c in tile} == {"bf16"}
+
+
+def test_clock_summary_reads_memory_clock_and_temperature():
+    """The clock record: SM clock median, memory clock median and the hottest
+    GPU temperature of the samples inside the timed region; a field the
+    driver reports as N/A is left out, not an error."""
+    import time
+    import bench
+    c = bench.ClockSampler(0)
+    t = time.time()
+    na = "Not Active"
+    c.samples = [(t, f"0, 2070, 2070, 170.5, 0x0, {na}, {na}, {na}, {na}, 3996, 45"),
+                 (t + 0.01, f"0, 2060, 2070, 171.0, 0x0, {na}, {na}, {na}, Active, N/A, 46"),
+                 (t + 5.0, f"0, 1000, 2070, 900.0, 0x0, Active, {na}, {na}, {na}, 3996, 90")]
+    s = c.summary(t - 1, t + 1)
+    assert s["sm_mhz"] == 2065.0 and s["sm_max_mhz"] == 2070.0 and s["mem_mhz"] == 3996.0
+    assert s["gpu_temp_c_max"] == 46.0 and s["power_w_max"] == 171.0
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 2
